@@ -1,0 +1,107 @@
+"""Seeded synthetic GEMM inputs, shared by the tests, the smoke check and the
+benchmark.  This module draws random numbers and casts them; it holds none of
+the product's arithmetic and imports neither the oracle nor the CUDA library.
+
+Recipe (the same for every workload): one CPU ``torch.Generator`` seeded with
+the workload's seed; A is drawn first, then B, in float32; uniform[-1, 1) is
+``2 * rand - 1``; N(0, s) is ``s * randn``; the 8192^3 workload scales both
+operands by 1/sqrt(K) in float32; the values are then rounded to fp16/bf16
+with round-to-nearest-even (``Tensor.to``).  Padding beyond the logical
+columns of a padded leading dimension is filled with NaN so that a kernel that
+reads it poisons its output.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    K: int
+    N: int
+    dtype: str          # "f16" or "bf16"
+    dist_a: str         # "uniform", "normal"
+    dist_b: str
+    scale_a: float
+    scale_b: float
+    seed: int
+    note: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def bytes_alg(self) -> int:
+        """One read of A and B (2 B/elem) and one write of C (4 B/elem)."""
+        return 2 * (self.M * self.K + self.K * self.N) + 4 * self.M * self.N
+
+
+WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("gemm256_f16", 256, 256, 256, "f16", "uniform", "uniform", 1.0, 1.0, 0,
+                 "256^3 fp16, uniform[-1,1)"),
+        Workload("ragged1023x1000x1029_f16", 1023, 1000, 1029, "f16", "uniform", "uniform", 1.0,
+                 1.0, 1, "ragged M=1023 K=1000 N=1029 fp16, uniform[-1,1)"),
+        Workload("square4096_bf16", 4096, 4096, 4096, "bf16", "normal", "normal", 1.0, 1.0, 2,
+                 "4096^3 bf16, N(0,1)"),
+        Workload("square8192_bf16", 8192, 8192, 8192, "bf16", "normal", "normal",
+                 1.0 / math.sqrt(8192), 1.0 / math.sqrt(8192), 3, "8192^3 bf16, N(0,1)/sqrt(K)"),
+        Workload("skinny16x4096x14336_bf16", 16, 4096, 14336, "bf16", "normal", "normal", 1.0,
+                 0.02, 4, "M=16 K=4096 N=14336 bf16, A N(0,1), B N(0,0.02)"),
+    ]
+}
+
+
+def _draw(g: torch.Generator, rows: int, cols: int, dist: str, scale: float) -> torch.Tensor:
+    if dist == "uniform":
+        x = torch.rand(rows, cols, generator=g, dtype=torch.float32) * 2.0 - 1.0
+    elif dist == "normal":
+        x = torch.randn(rows, cols, generator=g, dtype=torch.float32)
+    elif dist == "int4":   # integers in [-4, 4]: products and partial sums stay exact in fp32
+        x = torch.randint(-4, 5, (rows, cols), generator=g).to(torch.float32)
+    else:
+        raise ValueError(dist)
+    if scale != 1.0:
+        x = x * torch.tensor(scale, dtype=torch.float32)
+    return x
+
+
+def _place(x: torch.Tensor, ld: int | None, dtype: torch.dtype) -> torch.Tensor:
+    rows, cols = x.shape
+    if ld is None or ld == cols:
+        return x.to(dtype).contiguous()
+    if ld < cols:
+        raise ValueError(f"leading dimension {ld} < {cols}")
+    out = torch.full((rows, ld), float("nan"), dtype=dtype)
+    out[:, :cols] = x.to(dtype)
+    return out
+
+
+def make_inputs(w: Workload | str, *, lda: int | None = None, ldb: int | None = None
+                ) -> tuple[torch.Tensor, torch.Tensor]:
+    """CPU tensors (A stored as (M, lda), B stored as (K, ldb)) of the workload's dtype."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    g = torch.Generator().manual_seed(w.seed)
+    a = _draw(g, w.M, w.K, w.dist_a, w.scale_a)
+    b = _draw(g, w.K, w.N, w.dist_b, w.scale_b)
+    return _place(a, lda, w.torch_dtype), _place(b, ldb, w.torch_dtype)
+
+
+def custom(M: int, K: int, N: int, dtype: str, seed: int, dist: str = "uniform",
+           scale: float = 1.0, lda: int | None = None, ldb: int | None = None
+           ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Ad-hoc shape with the same recipe (used by the ragged sweeps and edge cases)."""
+    w = Workload(f"custom{M}x{K}x{N}", M, K, N, dtype, dist, dist, scale, scale, seed)
+    return make_inputs(w, lda=lda, ldb=ldb)
