@@ -1,0 +1,448 @@
+"""Throughput benchmark of the GB300 GEMM library (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one C = A @ B through the C ABI on the headline workload: 8192^3,
+bf16 inputs N(0,1)/sqrt(K) (seed 3), fp32 accumulate and output.  A and B
+(268 MB) are larger than the 129 MB L2, so no flush is needed between steps.
+The same line also reports the 4096^3 bf16 GEMM (L2 flushed between
+launches) and the M=16 skinny GEMM (B rotated among copies larger than L2),
+the roofline of the dominant kernel, an end-to-end number with host buffers,
+clocks sampled during the timed region, and the CPU oracle timed on a bounded
+sample as a baseline.
+
+Multi-GPU (torchrun, one process per GPU): the GEMM does not shard across
+GPUs here, so every rank runs an independent replica of the same workload;
+``value`` is the work of all ranks divided by the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (plain fp64 loops) on the host cores
+instead, on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of GB300 dense bf16 peak (4096³, 8192³); GB/s at M=16"
+HEADLINE = "square8192_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ---------------------------------------------------------------- helpers (no GPU)
+
+def load_peaks() -> tuple[dict, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_05_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    ent = rec.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_source_hash():
+        return None
+    return float(ent["dram_bytes_per_launch"])
+
+
+def aggregate(elapsed_s: float, units: float, world: int, dist=None) -> tuple[float, float]:
+    """(max elapsed over ranks, total units over ranks / max elapsed)."""
+    total_units = units * world
+    t = elapsed_s
+    if dist is not None and world > 1:
+        import torch
+        v = torch.tensor([elapsed_s], dtype=torch.float64)
+        if dist.get_backend() == "nccl":
+            v = v.cuda()
+        dist.all_reduce(v, op=dist.ReduceOp.MAX)
+        t = float(v.item())
+    return t, total_units / t
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = sorted(sm)[len(sm) // 2:] if sm else []   # upper half: samples under load
+        med = loaded[len(loaded) // 2] if loaded else None
+        return {"sm_mhz": med, "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def oracle_rate(workload, rows: int, nthreads: int = 0) -> tuple[float, float, int]:
+    """Time the oracle on the first `rows` rows of the workload: (seconds, flops, threads)."""
+    import oracle
+    import workloads
+    A, B = workloads.make_inputs(workload)
+    As = A[:rows].contiguous()
+    t0 = time.perf_counter()
+    oracle.gemm(As, B, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows * workload.N * workload.K, (nthreads or oracle.max_threads())
+
+
+def cpu_baseline(workload, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on a bounded row sample sized to ~budget_s seconds."""
+    import oracle
+    cores = oracle.max_threads()
+    dt, fl, _ = oracle_rate(workload, cores)
+    rows = max(cores, int(cores * budget_s / max(dt, 1e-3)) // cores * cores)
+    rows = min(rows, workload.M)
+    dt, fl, thr = oracle_rate(workload, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of {workload.name} ({rows}x{workload.N}x{workload.K}, "
+                      f"fp64 i-k-j loop), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+    w = workloads.WORKLOADS[HEADLINE]
+    cores = oracle.max_threads()
+    A, B = workloads.make_inputs(w)
+    # size each step so warmup + steps fit in about two minutes
+    t0 = time.perf_counter()
+    oracle.gemm(A[:cores].contiguous(), B)
+    per_row = (time.perf_counter() - t0) / cores
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = max(1, min(w.M, int(budget / max(per_row, 1e-6))))
+    As = A[:rows].contiguous()
+    for _ in range(args.warmup):
+        oracle.gemm(As, B)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(As, B)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    v = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"rows 0..{rows - 1} of {w.name} per step"},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def time_launches(torch, plan, calls, stream, between=None):
+    """Run each call (a->c) with CUDA events around the launch on `stream`; returns ms list."""
+    evs = []
+    with torch.cuda.stream(stream):
+        for fn in calls:
+            if between is not None:
+                between()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args, rank: int, world: int, dist) -> None:
+    import torch
+
+    import dense_gemm_05_gb300 as g
+    import workloads
+
+    g.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    plan = g.Plan(local)
+    peaks, peak_src = load_peaks()
+
+    w = workloads.WORKLOADS[HEADLINE]
+    A, B = workloads.make_inputs(w)
+    a, b = A.to(dev), B.to(dev)
+    c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+    cfg = plan.query(a, b, c)
+    s_handle = stream.cuda_stream
+    lda, ldb, ldc = a.stride(0), b.stride(0), c.stride(0)
+
+    def step():
+        st = g.gemm_run(plan.handle, a.data_ptr(), lda, b.data_ptr(), ldb, c.data_ptr(), ldc,
+                        w.M, w.N, w.K, g.GEMM_BF16, s_handle)
+        if st != g.GEMM_OK:
+            raise g.GemmError(st, "gemm_run")
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if dist is not None and world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_begin()
+    t_start = time.perf_counter()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        g1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None and world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.mark_end()
+    wall = time.perf_counter() - t_start
+    elapsed_ms = g0.elapsed_time(g1)
+    launch_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    clocks = sampler.stop() if sampler else None
+
+    t_max, total_flops_per_s = aggregate(elapsed_ms / 1e3, w.flops * args.steps, world, dist)
+    value = total_flops_per_s / 1e12
+    avg_launch_s = sum(launch_ms) / len(launch_ms) / 1e3
+    achieved = w.flops / avg_launch_s / 1e12
+    sustained = wall > 1.0
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(HEADLINE),
+                "kernel": f"gemm_tc_kernel BN={cfg['block_n']} ({cfg['kernel_name']})",
+                "peak_source": f"{peak_src} bf16 {'sustained' if sustained else 'burst'}",
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                "algorithmic_flops_per_launch": w.flops,
+                "avg_launch_ms": avg_launch_s * 1e3}
+
+    also = {}
+    if rank == 0 and not args.quick:
+        also = secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(torch, g, plan, w, A, B, dev, stream, max(3, min(args.steps, 10)),
+                         world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1)/sqrt(K) bf16)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
+                       "output": "fp32", "accumulate": "fp32",
+                       "l2": "inputs larger than L2 (A+B = 268 MB > 129 MB), no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "kernel": cfg},
+            "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks, "also": also,
+        }
+        print(json.dumps(line), flush=True)
+    plan.close()
+
+
+def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
+    out = {}
+    # 4096^3: inputs fit in L2, so L2 is flushed (a 512 MB write) before every timed launch.
+    w = workloads.WORKLOADS["square4096_bf16"]
+    A, B = workloads.make_inputs(w)
+    a, b = A.to(dev), B.to(dev)
+    c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    cfg = plan.query(a, b, c)
+    call = lambda: plan.run(a, b, c, stream=stream)  # noqa: E731
+    time_launches(torch, plan, [call] * 5, stream)
+    ms = time_launches(torch, plan, [call] * 50, stream, between=lambda: flush.zero_())
+    t = sorted(ms)[len(ms) // 2] / 1e3
+    tf = w.flops / t / 1e12
+    out[w.name] = {"tflops": tf, "pct_of_peak": 100 * tf / peaks["bf16_tflops"],
+                   "median_ms": t * 1e3, "l2": "flushed before each launch",
+                   "kernel": cfg["kernel_name"], "block_n": cfg["block_n"],
+                   "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst"}
+    del a, b, c, flush
+    # M=16 skinny: B copies rotated so that the working set exceeds L2 several times.
+    w = workloads.WORKLOADS["skinny16x4096x14336_bf16"]
+    A, B = workloads.make_inputs(w)
+    copies = max(3, math.ceil(3 * L2_BYTES / (B.numel() * 2)))
+    a = A.to(dev)
+    bs = [B.to(dev) for _ in range(copies)]
+    c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+    cfg = plan.query(a, bs[0], c)
+    calls = [(lambda bb=bb: plan.run(a, bb, c, stream=stream)) for bb in bs]
+    time_launches(torch, plan, calls * 3, stream)
+    ms = time_launches(torch, plan, calls * 40, stream)
+    t = sorted(ms)[len(ms) // 2] / 1e3
+    gbs = w.bytes_alg / t / 1e9
+    out[w.name] = {"gbs": gbs, "pct_of_hbm_peak": 100 * gbs / peaks["hbm_gbs"],
+                   "tflops": w.flops / t / 1e12, "median_us": t * 1e6,
+                   "l2": f"B rotated among {copies} copies ({copies * B.numel() * 2 / 1e6:.0f} MB)",
+                   "kernel": cfg["kernel_name"], "split_k": cfg["split_k"],
+                   "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                   "bytes_alg": w.bytes_alg}
+    return out
+
+
+def end_to_end(torch, g, plan, w, A, B, dev, stream, steps, world, dist) -> dict:
+    """Host (pinned) A, B -> device, C = A @ B through the C ABI, C -> host; per step."""
+    ha, hb = A.pin_memory(), B.pin_memory()
+    hc = torch.empty(w.M, w.N, dtype=torch.float32).pin_memory()
+    a = torch.empty_like(ha, device=dev)
+    b = torch.empty_like(hb, device=dev)
+    c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+
+    def one():
+        with torch.cuda.stream(stream):
+            a.copy_(ha, non_blocking=True)
+            b.copy_(hb, non_blocking=True)
+            plan.run(a, b, c, stream=stream)
+            hc.copy_(c, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    if dist is not None and world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t, rate = aggregate(e0.elapsed_time(e1) / 1e3, w.flops * steps, world, dist)
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "steps": steps,
+            "h2d_bytes_per_step": (ha.numel() + hb.numel()) * 2,
+            "d2h_bytes_per_step": hc.numel() * 4}
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+            dist_mod.init_process_group("nccl")
+            dist = dist_mod
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,244 @@
+"""Python binding of the GB300 GEMM C ABI (``include/gemm.h``).
+
+Argument marshalling only: every step of ``C = A @ B`` runs in the CUDA
+kernels of ``_build/libgemm.so``.  PyTorch supplies device memory and streams.
+There is no fallback: if the library has not been built, importing the
+binding functions raises.
+
+    plan = gemm_plan_create(0)
+    gemm_run(plan, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, M, N, K,
+             GEMM_BF16, torch.cuda.current_stream().cuda_stream)
+    gemm_plan_destroy(plan)
+
+``matmul(a, b)`` wraps the same calls for 2-D torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH, build  # noqa: F401  (re-exported for __graft_entry__)
+
+GEMM_F16 = 0
+GEMM_BF16 = 1
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_CUDA = 3
+GEMM_ERR_OOM = 4
+GEMM_ERR_TIMEOUT = 5
+
+GEMM_KERNEL_NONE = 0
+GEMM_KERNEL_ZERO_FILL = 1
+GEMM_KERNEL_TMA = 2
+GEMM_KERNEL_GENERIC = 3
+GEMM_KERNEL_SKINNY = 4
+GEMM_KERNEL_PAIR = 5
+
+KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 5: "pair"}
+
+#: Every function the header declares (checked by the tests against the library's exports).
+ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
+                 "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
+                 "gemm_wait_selftest")
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class GemmConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("kernel", "block_m", "block_n", "block_k", "stages", "split_k", "grid",
+                 "cluster", "group", "tiles")]
+
+    def as_dict(self) -> dict:
+        d = {n: int(getattr(self, n)) for n, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(d["kernel"], "?")
+        return d
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libgemm.so (built by ``build()``); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: run dense_gemm_05_gb300.build() (or "
+                "__graft_entry__.build()) first; there is no fallback implementation")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
+        L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int]
+        L.gemm_plan_create.restype = i32
+        L.gemm_run.argtypes = [vp, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, vp]
+        L.gemm_run.restype = i32
+        L.gemm_plan_destroy.argtypes = [vp]
+        L.gemm_plan_destroy.restype = i32
+        L.gemm_status_string.argtypes = [i32]
+        L.gemm_status_string.restype = ctypes.c_char_p
+        L.gemm_query.argtypes = [vp, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                 ctypes.POINTER(GemmConfig)]
+        L.gemm_query.restype = i32
+        L.gemm_plan_set_group.argtypes = [vp, i32]
+        L.gemm_plan_set_group.restype = i32
+        L.gemm_plan_force.argtypes = [vp, i32, i32]
+        L.gemm_plan_force.restype = i32
+        L.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
+                                      ctypes.POINTER(i64)]
+        L.gemm_tile_coord.restype = i32
+        L.gemm_wait_selftest.argtypes = [u32, vp]
+        L.gemm_wait_selftest.restype = i32
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+# ------------------------------------------------------------------ C-ABI mirrors
+
+def gemm_plan_create(device: int = 0) -> int:
+    """Create a plan on `device`; returns the opaque handle (an int)."""
+    h = ctypes.c_void_p()
+    st = lib().gemm_plan_create(ctypes.byref(h), int(device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan_create")
+    return h.value
+
+
+def gemm_run(plan: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M: int, N: int,
+             K: int, dtype: int, stream: int = 0) -> int:
+    """C = A @ B on `stream` (raw pointers as ints); returns the gemm_status_t code."""
+    return int(lib().gemm_run(plan, A, lda, B, ldb, C, ldc, M, N, K, dtype, stream))
+
+
+def gemm_plan_destroy(plan: int | None) -> int:
+    return int(lib().gemm_plan_destroy(plan))
+
+
+def gemm_query(plan: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M: int, N: int,
+               K: int, dtype: int) -> dict:
+    cfg = GemmConfig()
+    st = lib().gemm_query(plan, A, lda, B, ldb, C, ldc, M, N, K, dtype, ctypes.byref(cfg))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_query")
+    return cfg.as_dict()
+
+
+def gemm_plan_set_group(plan: int, group: int) -> int:
+    return int(lib().gemm_plan_set_group(plan, group))
+
+
+def gemm_plan_force(plan: int, kernel: int = 0, split_k: int = 0) -> int:
+    return int(lib().gemm_plan_force(plan, kernel, split_k))
+
+
+def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int) -> tuple[int, int]:
+    tm, tn = ctypes.c_int64(), ctypes.c_int64()
+    st = lib().gemm_tile_coord(t, tiles_m, tiles_n, group, ctypes.byref(tm), ctypes.byref(tn))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tile_coord")
+    return tm.value, tn.value
+
+
+def gemm_wait_selftest(timeout_us: int, stream: int = 0) -> int:
+    return int(lib().gemm_wait_selftest(timeout_us, stream))
+
+
+# ------------------------------------------------------------------ torch convenience
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return GEMM_F16
+    if t.dtype == torch.bfloat16:
+        return GEMM_BF16
+    raise TypeError(f"A and B must be float16 or bfloat16, got {t.dtype}")
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("matrices must be 2-D with unit inner stride (row-major)")
+    return t.stride(0) if t.size(0) > 1 else max(t.stride(0), t.size(1))
+
+
+class Plan:
+    """Owns one C-ABI plan; ``run``/``matmul`` marshal torch tensors into gemm_run."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.handle = gemm_plan_create(device)
+
+    def close(self):
+        if self.handle:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_group(self, group: int):
+        st = gemm_plan_set_group(self.handle, group)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_plan_set_group")
+
+    def force(self, kernel: int = 0, split_k: int = 0):
+        st = gemm_plan_force(self.handle, kernel, split_k)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_plan_force")
+
+    def query(self, a, b, c, M=None, N=None, K=None) -> dict:
+        M = a.size(0) if M is None else M
+        K = a.size(1) if K is None else K
+        N = b.size(1) if N is None else N
+        return gemm_query(self.handle, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), c.data_ptr(),
+                          _ld(c), M, N, K, _dtype_code(a))
+
+    def run(self, a, b, c, M=None, N=None, K=None, stream=None) -> None:
+        """c[:M, :N] = a[:M, :K] @ b[:K, :N] (fp32 c); raises GemmError on failure."""
+        import torch
+        if a.dtype != b.dtype:
+            raise TypeError("A and B must have the same dtype")
+        if c.dtype != torch.float32:
+            raise TypeError("C must be float32")
+        M = a.size(0) if M is None else M
+        K = a.size(1) if K is None else K
+        N = b.size(1) if N is None else N
+        s = (torch.cuda.current_stream(a.device) if stream is None else stream).cuda_stream
+        st = gemm_run(self.handle, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), c.data_ptr(),
+                      _ld(c), M, N, K, _dtype_code(a), s)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_run")
+
+    def matmul(self, a, b):
+        import torch
+        if a.size(1) != b.size(0):
+            raise ValueError(f"inner dimensions differ: {tuple(a.shape)} @ {tuple(b.shape)}")
+        c = torch.empty((a.size(0), b.size(1)), dtype=torch.float32, device=a.device)
+        self.run(a, b, c)
+        return c
+
+
+_default_plans: dict = {}
+
+
+def matmul(a, b):
+    """fp32 C = A @ B for 2-D fp16/bf16 CUDA tensors, through a per-device default plan."""
+    dev = a.device.index or 0
+    if dev not in _default_plans:
+        _default_plans[dev] = Plan(dev)
+    return _default_plans[dev].matmul(a, b)

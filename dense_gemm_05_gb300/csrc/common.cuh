@@ -1,0 +1,103 @@
+// common.cuh -- parameters, tile order and launcher declarations shared by the
+// kernel translation units and the C-ABI layer of the GEMM library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dg {
+
+constexpr int kBM = 128;                 // rows of C per CTA tile (TMEM lanes)
+constexpr int kBK = 64;                  // K depth of one stage: 64 x 2 B = one 128-B swizzle row
+constexpr int kAStageBytes = kBM * kBK * 2;
+constexpr int kSubN = 64;                // columns of one MN-major swizzle sub-tile (128 B)
+constexpr int kSubTileBytes = kSubN * kBK * 2;   // 8 KB: 64 K-rows of 128 B
+
+// Status word written by a kernel whose bounded wait gave up.
+constexpr int kDevTimeout = 1;
+
+struct Params {
+    const uint16_t* A;
+    const uint16_t* B;
+    float* C;
+    int64_t lda, ldb, ldc;
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n, num_kb;
+    int32_t group;          // group-major strip height (0 = row-major)
+    int32_t split_k;        // skinny: K slices per output tile
+    int32_t kb_per_split;   // skinny: K blocks per slice
+    int32_t a_vec, b_vec;   // generic producer: 16-byte vector loads are legal
+    int32_t c_vec;          // 16-byte vector stores of C are legal
+    float* ws;              // skinny: split-K partial sums
+    int* counters;          // skinny: per-tile arrival counters (zero between launches)
+    int* status;            // device error word (kDevTimeout on a wait that gave up)
+    uint64_t timeout_ns;    // limit of every device-side wait
+};
+
+// Linear work index t -> (tile row, tile column).
+// group > 0: group-major order of "I Wrote a GPU Matmul Kernel From Scratch in
+// Triton", Step 4 -- strips of `group` tile rows, walked column by column,
+// the last strip only as tall as the rows that remain.  group <= 0: row-major
+// order of the "Triton 04" teaching kernel.
+__host__ __device__ __forceinline__ void tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n,
+                                                    int group, int64_t& tm, int64_t& tn) {
+    if (group <= 0) {
+        tm = t / tiles_n;
+        tn = t - tm * tiles_n;
+        return;
+    }
+    const int64_t per_strip = static_cast<int64_t>(group) * tiles_n;
+    const int64_t strip = t / per_strip;
+    const int64_t first = strip * group;
+    const int64_t rem = tiles_m - first;
+    const int64_t height = rem < group ? rem : group;
+    const int64_t local = t - strip * per_strip;
+    tm = first + local % height;
+    tn = local / height;
+}
+
+__device__ __forceinline__ void tile_coord32(int t, int tiles_m, int tiles_n, int group, int& tm,
+                                             int& tn) {
+    if (group <= 0) {
+        tm = t / tiles_n;
+        tn = t - tm * tiles_n;
+        return;
+    }
+    const int per_strip = group * tiles_n;
+    const int strip = t / per_strip;
+    const int first = strip * group;
+    const int rem = tiles_m - first;
+    const int height = rem < group ? rem : group;
+    const int local = t - strip * per_strip;
+    tm = first + local % height;
+    tn = local / height;
+}
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error; none synchronises.
+
+// Persistent tcgen05 kernel, operands by TMA. bn in {128, 256}.
+int tma_smem_bytes(int bn);
+int tma_stages(int bn);
+cudaError_t tma_prepare();
+cudaError_t launch_tma(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
+                       uint32_t idesc, int grid, cudaStream_t stream);
+
+// Same pipeline, operands staged by ordinary loads (any alignment). bn = 128.
+int generic_smem_bytes();
+int generic_stages();
+cudaError_t generic_prepare();
+cudaError_t launch_generic(const Params& p, uint32_t idesc, int grid, cudaStream_t stream);
+
+// Skinny M: swap-AB + split-K. ms in {16, 32, 64} (MMA N = padded M).
+int skinny_smem_bytes(int ms);
+int skinny_stages(int ms);
+cudaError_t skinny_prepare();
+cudaError_t launch_skinny(int ms, const CUtensorMap& mapB, const CUtensorMap& mapA,
+                          const Params& p, uint32_t idesc, int grid, cudaStream_t stream);
+
+// Wait self-test: one block waits on a barrier nobody completes.
+cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace dg

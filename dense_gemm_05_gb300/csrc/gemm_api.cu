@@ -1,0 +1,530 @@
+// gemm_api.cu -- the C ABI declared in include/gemm.h: argument checks, the
+// plan (workspace, device facts, options), kernel selection (the offline
+// replacement of the autotune step of "I Wrote a GPU Matmul Kernel From
+// Scratch in Triton", Step 5), TMA descriptor encoding and launches.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gemm.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+struct gemm_plan_s {
+    int device = 0;
+    int num_sms = 0;
+    float* ws = nullptr;          // split-K partial tiles
+    size_t ws_bytes = 0;
+    int* counters = nullptr;      // split-K per-tile arrival counters (kept at zero)
+    int counters_len = 0;
+    int* status = nullptr;        // device error word
+    int group = 8;
+    int force_kernel = 0;
+    int force_split = 0;
+    bool debug_sync = false;
+    uint64_t timeout_ns = 2000000000ull;
+};
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = size_t(32) << 20;   // split-K partials
+constexpr int kMaxCounters = 1 << 16;                   // output tiles that may be split
+constexpr int64_t kMaxDim = INT32_MAX - 1024;   // headroom for tile-edge arithmetic in int32
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// Row-major [outer, inner] 16-bit matrix with row pitch ld (elements), tiles of
+// box_outer x box_inner elements, 128-byte swizzle, zero fill out of bounds.
+bool encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* ptr, int64_t inner, int64_t outer,
+               int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map,
+                    dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tma_ok(const void* ptr, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(ptr) % 16u) == 0u && ((ld * 2) % 16) == 0;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Args {
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    const float* C;
+    int64_t ldc;
+    int64_t M, N, K;
+    gemm_dtype_t dtype;
+};
+
+struct Choice {
+    int kernel = GEMM_KERNEL_NONE;
+    int bn = 0;          // TMA/GENERIC: tile columns
+    int ms = 0;          // SKINNY: padded M (MMA N)
+    int split = 1;
+    int kbps = 0;
+    int tiles_m = 0, tiles_n = 0, num_kb = 0;
+    int units = 0;
+    int grid = 0;
+    int stages = 0;
+};
+
+// Last byte (exclusive) touched by a row-major rows x cols region with pitch ld.
+bool region_end(int64_t rows, int64_t cols, int64_t ld, int64_t esize, uint64_t* end_bytes) {
+    // rows, cols <= 2^31 - 1 and ld <= 2^40 were checked by the caller.
+    const unsigned __int128 e =
+        (static_cast<unsigned __int128>(rows - 1) * static_cast<uint64_t>(ld) +
+         static_cast<uint64_t>(cols)) *
+        static_cast<uint64_t>(esize);
+    if (e > static_cast<unsigned __int128>(UINT64_MAX / 2)) return false;
+    *end_bytes = static_cast<uint64_t>(e);
+    return true;
+}
+
+bool overlaps(const void* p, uint64_t plen, const void* q, uint64_t qlen) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + qlen && b < a + plen;
+}
+
+gemm_status_t check_args(const Args& a) {
+    if (a.M < 0 || a.N < 0 || a.K < 0) return GEMM_ERR_INVALID_ARG;
+    if (a.dtype != GEMM_F16 && a.dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+    if (a.M > kMaxDim || a.N > kMaxDim || a.K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+    if (a.M == 0 || a.N == 0) return GEMM_OK;
+    constexpr int64_t kMaxLd = int64_t(1) << 40;
+    if (a.C == nullptr || a.ldc < a.N) return GEMM_ERR_INVALID_ARG;
+    if (a.ldc > kMaxLd) return GEMM_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(a.C) % 4u != 0u) return GEMM_ERR_INVALID_ARG;
+    uint64_t c_end = 0;
+    if (!region_end(a.M, a.N, a.ldc, 4, &c_end)) return GEMM_ERR_UNSUPPORTED;
+    if (a.K == 0) return GEMM_OK;
+    if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return GEMM_ERR_INVALID_ARG;
+    if (a.lda > kMaxLd || a.ldb > kMaxLd) return GEMM_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(a.A) % 2u != 0u || reinterpret_cast<uintptr_t>(a.B) % 2u != 0u)
+        return GEMM_ERR_INVALID_ARG;
+    uint64_t a_end = 0, b_end = 0;
+    if (!region_end(a.M, a.K, a.lda, 2, &a_end) || !region_end(a.K, a.N, a.ldb, 2, &b_end))
+        return GEMM_ERR_UNSUPPORTED;
+    if (overlaps(a.C, c_end, a.A, a_end) || overlaps(a.C, c_end, a.B, b_end))
+        return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+// Skinny split: the number of K slices S that minimises the longest CTA's
+// K-block count, ceil(units / SMs) * ceil(num_kb / S), within the workspace.
+void choose_split(const gemm_plan_s* plan, Choice* c) {
+    const int64_t per_split_bytes = int64_t(c->tiles_n) * c->ms * 128 * 4;
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    const int max_s = c->num_kb < 64 ? c->num_kb : 64;
+    for (int s = 1; s <= max_s; ++s) {
+        const int kbps = static_cast<int>(cdiv(c->num_kb, s));
+        if (cdiv(c->num_kb, kbps) != s) continue;                 // every slice non-empty
+        if (s > 1 && (c->tiles_n > plan->counters_len ||
+                      per_split_bytes * s > static_cast<int64_t>(plan->ws_bytes)))
+            break;
+        const int64_t waves = cdiv(int64_t(c->tiles_n) * s, plan->num_sms);
+        const int64_t cost = waves * (kbps + 1);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    c->split = best;
+}
+
+gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
+    *c = Choice{};
+    if (a.M == 0 || a.N == 0) {
+        c->kernel = GEMM_KERNEL_NONE;
+        return GEMM_OK;
+    }
+    if (a.K == 0) {
+        c->kernel = GEMM_KERNEL_ZERO_FILL;
+        return GEMM_OK;
+    }
+    const bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
+    int kernel = plan->force_kernel;
+    if (kernel == 0) {
+        if (tma && a.M <= 64)
+            kernel = GEMM_KERNEL_SKINNY;
+        else if (tma)
+            kernel = GEMM_KERNEL_TMA;
+        else
+            kernel = GEMM_KERNEL_GENERIC;
+    }
+    if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY) && !tma)
+        return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_SKINNY && a.M > 64) return GEMM_ERR_UNSUPPORTED;
+    if (kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_SKINNY &&
+        kernel != GEMM_KERNEL_GENERIC)
+        return GEMM_ERR_UNSUPPORTED;
+    c->kernel = kernel;
+    c->num_kb = static_cast<int>(cdiv(a.K, dg::kBK));
+    if (kernel == GEMM_KERNEL_SKINNY) {
+        c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : 64);
+        c->tiles_m = 1;
+        c->tiles_n = static_cast<int>(cdiv(a.N, 128));
+        if (plan->force_split > 0) {
+            int s = plan->force_split < c->num_kb ? plan->force_split : c->num_kb;
+            const int kbps = static_cast<int>(cdiv(c->num_kb, s));
+            s = static_cast<int>(cdiv(c->num_kb, kbps));
+            const int64_t need = int64_t(c->tiles_n) * c->ms * 128 * 4 * s;
+            if (s > 1 && (c->tiles_n > plan->counters_len ||
+                          need > static_cast<int64_t>(plan->ws_bytes)))
+                return GEMM_ERR_UNSUPPORTED;
+            c->split = s;
+        } else {
+            choose_split(plan, c);
+        }
+        c->kbps = static_cast<int>(cdiv(c->num_kb, c->split));
+        c->units = c->tiles_n * c->split;
+        c->stages = dg::skinny_stages(c->ms);
+    } else {
+        const int64_t tm = cdiv(a.M, dg::kBM);
+        if (kernel == GEMM_KERNEL_TMA) {
+            const int64_t t256 = tm * cdiv(a.N, 256);
+            c->bn = (t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128;
+            c->stages = dg::tma_stages(c->bn);
+        } else {
+            c->bn = 128;
+            c->stages = dg::generic_stages();
+        }
+        c->tiles_m = static_cast<int>(tm);
+        c->tiles_n = static_cast<int>(cdiv(a.N, c->bn));
+        const int64_t units = int64_t(c->tiles_m) * c->tiles_n;
+        if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+        c->units = static_cast<int>(units);
+    }
+    c->grid = c->units < plan->num_sms ? c->units : plan->num_sms;
+    return GEMM_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            prev = -1;
+        }
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+        if (!ok) (void)cudaGetLastError();
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) (void)cudaSetDevice(prev);
+    }
+};
+
+bool env_flag(const char* name) {
+    const char* v = std::getenv(name);
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
+}  // namespace
+
+namespace dg {
+
+__global__ void wait_selftest_kernel(int* out, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1u);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // Nothing ever arrives on `bar`: the bounded wait must give up.
+        const bool ok = mbar_wait(smem_u32(&bar), 0u, &abort_flag, timeout_ns);
+        *out = ok ? 1 : 2;
+    }
+}
+
+cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(out, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace dg
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_OOM: return "GEMM_ERR_OOM";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
+    if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
+    if (encode_fn() == nullptr) return GEMM_ERR_CUDA;
+    if (dg::tma_prepare() != cudaSuccess || dg::generic_prepare() != cudaSuccess ||
+        dg::skinny_prepare() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
+    if (p == nullptr) return GEMM_ERR_OOM;
+    p->device = device;
+    p->num_sms = sms;
+    p->debug_sync = env_flag("GEMM_DEBUG_SYNC");
+    if (const char* t = std::getenv("GEMM_WAIT_TIMEOUT_MS")) {
+        const long long ms = std::atoll(t);
+        if (ms > 0) p->timeout_ns = static_cast<uint64_t>(ms) * 1000000ull;
+    }
+    if (cudaMalloc(&p->ws, kWorkspaceBytes) != cudaSuccess ||
+        cudaMalloc(&p->counters, sizeof(int) * kMaxCounters) != cudaSuccess ||
+        cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cudaFree(p->ws);
+        cudaFree(p->counters);
+        cudaFree(p->status);
+        delete p;
+        return GEMM_ERR_OOM;
+    }
+    p->ws_bytes = kWorkspaceBytes;
+    p->counters_len = kMaxCounters;
+    if (cudaMemset(p->counters, 0, sizeof(int) * kMaxCounters) != cudaSuccess ||
+        cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cudaFree(p->ws);
+        cudaFree(p->counters);
+        cudaFree(p->status);
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
+    if (plan == nullptr) return GEMM_OK;
+    DeviceGuard guard(plan->device);
+    cudaFree(plan->ws);
+    cudaFree(plan->counters);
+    cudaFree(plan->status);
+    delete plan;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group) {
+    if (plan == nullptr || group < 0 || group > 64) return GEMM_ERR_INVALID_ARG;
+    plan->group = group;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k) {
+    if (plan == nullptr || split_k < 0) return GEMM_ERR_INVALID_ARG;
+    if (kernel != 0 && kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_GENERIC &&
+        kernel != GEMM_KERNEL_SKINNY && kernel != GEMM_KERNEL_PAIR)
+        return GEMM_ERR_INVALID_ARG;
+    plan->force_kernel = kernel;
+    plan->force_split = split_k;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group,
+                              int64_t* tile_m, int64_t* tile_n) {
+    if (tile_m == nullptr || tile_n == nullptr || tiles_m <= 0 || tiles_n <= 0 || group < 0 ||
+        tiles_m > kMaxDim || tiles_n > kMaxDim || t < 0 || t >= tiles_m * tiles_n)
+        return GEMM_ERR_INVALID_ARG;
+    dg::tile_coord(t, tiles_m, tiles_n, group, *tile_m, *tile_n);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
+                         const float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         gemm_dtype_t dtype, gemm_config_t* out) {
+    if (plan == nullptr || out == nullptr) return GEMM_ERR_INVALID_ARG;
+    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    gemm_status_t st = check_args(a);
+    if (st != GEMM_OK) return st;
+    Choice c;
+    st = choose(plan, a, &c);
+    if (st != GEMM_OK) return st;
+    gemm_config_t cfg{};
+    cfg.kernel = c.kernel;
+    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY) ? c.ms : dg::kBM;
+    cfg.block_n = (c.kernel == GEMM_KERNEL_SKINNY) ? 128 : c.bn;
+    cfg.block_k = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : dg::kBK;
+    cfg.stages = c.stages;
+    cfg.split_k = c.split;
+    cfg.grid = c.grid;
+    cfg.cluster = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : 1;
+    cfg.group = (c.kernel == GEMM_KERNEL_TMA || c.kernel == GEMM_KERNEL_GENERIC) ? plan->group : 0;
+    cfg.tiles = c.units;
+    *out = cfg;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                       gemm_dtype_t dtype, struct CUstream_st* stream_handle) {
+    if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    gemm_status_t st = check_args(a);
+    if (st != GEMM_OK) return st;
+    Choice c;
+    st = choose(plan, a, &c);
+    if (st != GEMM_OK) return st;
+    if (c.kernel == GEMM_KERNEL_NONE) return GEMM_OK;
+
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    cudaError_t err = cudaSuccess;
+
+    if (c.kernel == GEMM_KERNEL_ZERO_FILL) {
+        err = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4u, 0, static_cast<size_t>(N) * 4u,
+                                static_cast<size_t>(M), stream);
+    } else {
+        dg::Params p{};
+        p.A = static_cast<const uint16_t*>(A);
+        p.B = static_cast<const uint16_t*>(B);
+        p.C = C;
+        p.lda = lda;
+        p.ldb = ldb;
+        p.ldc = ldc;
+        p.M = static_cast<int32_t>(M);
+        p.N = static_cast<int32_t>(N);
+        p.K = static_cast<int32_t>(K);
+        p.tiles_m = c.tiles_m;
+        p.tiles_n = c.tiles_n;
+        p.num_kb = c.num_kb;
+        p.group = plan->group;
+        p.split_k = c.split;
+        p.kb_per_split = c.kbps;
+        p.a_vec = tma_ok(A, lda) ? 1 : 0;
+        p.b_vec = tma_ok(B, ldb) ? 1 : 0;
+        p.c_vec = ((reinterpret_cast<uintptr_t>(C) % 16u) == 0u && ldc % 4 == 0) ? 1 : 0;
+        p.ws = plan->ws;
+        p.counters = plan->counters;
+        p.status = plan->status;
+        p.timeout_ns = plan->timeout_ns;
+        const bool bf16 = dtype == GEMM_BF16;
+        if (c.kernel == GEMM_KERNEL_TMA) {
+            CUtensorMap ma, mb;
+            if (!encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
+                !encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+                return GEMM_ERR_CUDA;
+            err = dg::launch_tma(c.bn, ma, mb, p, dg::idesc_f16(bf16, false, true, dg::kBM, c.bn),
+                                 c.grid, stream);
+        } else if (c.kernel == GEMM_KERNEL_GENERIC) {
+            err = dg::launch_generic(p, dg::idesc_f16(bf16, false, true, dg::kBM, 128), c.grid,
+                                     stream);
+        } else {
+            CUtensorMap mb, ma;
+            if (!encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK) ||
+                !encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, static_cast<uint32_t>(c.ms)))
+                return GEMM_ERR_CUDA;
+            err = dg::launch_skinny(c.ms, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, c.ms),
+                                    c.grid, stream);
+        }
+    }
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (plan->debug_sync) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        int dev_status = 0;
+        if (cudaMemcpy(&dev_status, plan->status, sizeof(int), cudaMemcpyDeviceToHost) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (dev_status != 0) {
+            (void)cudaMemset(plan->status, 0, sizeof(int));
+            (void)cudaMemset(plan->counters, 0, sizeof(int) * plan->counters_len);
+            return GEMM_ERR_TIMEOUT;
+        }
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st* stream_handle) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+    int* d = nullptr;
+    if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int h = 0;
+    gemm_status_t st = GEMM_OK;
+    if (cudaMemsetAsync(d, 0, sizeof(int), stream) != cudaSuccess ||
+        dg::launch_wait_selftest(d, static_cast<uint64_t>(timeout_us) * 1000ull, stream) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(&h, d, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        st = GEMM_ERR_CUDA;
+    } else if (h == 2) {
+        st = GEMM_ERR_TIMEOUT;
+    } else if (h != 1) {
+        st = GEMM_ERR_CUDA;
+    }
+    cudaFree(d);
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,347 @@
+// gemm_skinny.cu -- small-M GEMM for sm_103a: swap-AB + split-K.
+//
+// For M <= 64 the product is computed transposed, C^T[N, M] = B^T[N, K] A^T[K, M],
+// so N fills the 128 rows of the tcgen05 MMA and the padded M (16, 32 or 64)
+// is the MMA's N.  B, the large operand, is read once from HBM: the problem is
+// bound by that stream, not by the tensor cores.  To put every SM on the
+// stream, each 128-column tile of C is split into S slices along K (the
+// K-sum of "Writing GPU kernels in Triton", section 3.3, regrouped; the
+// regrouping is exact up to rounding because the sum is associative).
+// Each (tile, slice) unit writes its fp32 partial tile to the plan's
+// workspace; the last unit of a tile to arrive (a per-tile counter) adds the S
+// partials in slice order 0..S-1 and writes C, so the result is the same bits
+// on every run, whatever order the units finish in.  It then resets the
+// counter to zero for the next launch.
+//
+// Warp roles are those of gemm_tc.cu: warp 0 MMA issuer + TMEM owner, warps
+// 1..4 epilogue, warp 5 TMA producer.
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dg {
+
+template <int MS, int STAGES>
+struct SkCfg {
+    static constexpr int kBtStageBytes = 128 * kBK * 2;   // B^T tile: 128 n x 64 k (two sub-tiles)
+    static constexpr int kAStageBytes = MS * kBK * 2;      // A tile: MS m x 64 k, K-major
+    static constexpr int kStageBytes = kBtStageBytes + kAStageBytes;
+    static constexpr int kTmemCols = (2 * MS < 32) ? 32 : 2 * MS;
+    static constexpr int kThreads = 192;
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 8 * kNumBars + 16;
+    static_assert(MS == 16 || MS == 32 || MS == 64, "MS");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+template <int MS>
+__device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[MS]) {
+    if constexpr (MS == 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(taddr, r);
+        tmem_ld_wait(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < MS / 32; ++h) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(h * 32), r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[h * 32 + i] = __uint_as_float(r[i]);
+        }
+    }
+}
+
+template <int MS, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapB,
+                       const __grid_constant__ CUtensorMap mapA, const Params p,
+                       const uint32_t idesc) {
+    using Cfg = SkCfg<MS, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sBt = smem;
+    uint8_t* sA = smem + STAGES * Cfg::kBtStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sA + STAGES * Cfg::kAStageBytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = abort_flag + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1u);
+            mbar_init(smem_u32(&empty[s]), 1u);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1u);
+            mbar_init(smem_u32(&tempty[a]), 128u);
+        }
+        mbar_init(smem_u32(drain), 1u);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 5 && lane == 0) {
+        prefetch_tmap(&mapA);
+        prefetch_tmap(&mapB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int S = p.split_k;
+    const int units = p.tiles_n * S;
+    const int num_kb = p.num_kb;
+    const int kbps = p.kb_per_split;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool failed = false;
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
+                const int split = u % S;
+                const int kb0 = split * kbps;
+                const int kb1 = min(num_kb, kb0 + kbps);
+                if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MS);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.timeout_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a0 = sdesc_sw128(smem_u32(sBt + stage * Cfg::kBtStageBytes),
+                                                    static_cast<uint32_t>(kSubTileBytes), 1024u);
+                    const uint64_t b0 =
+                        sdesc_sw128(smem_u32(sA + stage * Cfg::kAStageBytes), 16u, 1024u);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        tc_mma_f16(d_tmem, a0 + static_cast<uint64_t>((k * 16 * 128) >> 4),
+                                   b0 + static_cast<uint64_t>((k * 32) >> 4), idesc,
+                                   (kb != kb0 || k != 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (failed) break;
+                tc_commit(smem_u32(&tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (failed) {
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                const volatile int never = 0;
+                tc_commit(smem_u32(drain));
+                mbar_wait(smem_u32(drain), 0u, &never, 100000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp <= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int r = q * 32 + lane;            // row of the transposed tile = column of C
+        const int et = threadIdx.x - 32;        // 0..127
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int n_tile = u / S;
+            const int split = u - n_tile * S;
+            const bool ok =
+                mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
+            // One decision for all 128 epilogue threads: they share named barriers below.
+            if (!named_bar_and(1, 128, ok)) {
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                break;
+            }
+            tc_fence_after();
+            float v[MS];
+            load_acc<MS>(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * MS),
+                         v);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+
+            const int n = n_tile * 128 + r;
+            if (S == 1) {
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MS; ++m)
+                        if (m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = v[m];
+                }
+                continue;
+            }
+            // Split-K: publish this slice's partial tile, then let the last arriver reduce.
+            float* wsp = p.ws + (static_cast<int64_t>(split) * p.tiles_n + n_tile) * (MS * 128) + r;
+#pragma unroll
+            for (int m = 0; m < MS; ++m) __stcg(wsp + m * 128, v[m]);
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (et == 0) {
+                const int old = atomicAdd(&p.counters[n_tile], 1);
+                *last_flag = (old == S - 1) ? 1 : 0;
+            }
+            named_bar_sync(1, 128);
+            if (*last_flag) {
+                __threadfence();
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MS; ++m) {
+                        if (m < p.M) {
+                            float s = 0.0f;
+                            for (int sp = 0; sp < S; ++sp)
+                                s += __ldcg(p.ws +
+                                            (static_cast<int64_t>(sp) * p.tiles_n + n_tile) *
+                                                (MS * 128) +
+                                            m * 128 + r);
+                            p.C[static_cast<int64_t>(m) * p.ldc + n] = s;
+                        }
+                    }
+                }
+                if (et == 0) p.counters[n_tile] = 0;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool failed = false;
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t armed = 0;
+            const uint64_t pol_stream = l2_policy_evict_first();   // B: read once
+            const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every tile
+            for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
+                const int n_tile = u / S;
+                const int split = u - n_tile * S;
+                const int kb0 = split * kbps;
+                const int kb1 = min(num_kb, kb0 + kbps);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                   p.timeout_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tma_load_2d_hint(
+                            smem_u32(sBt + stage * Cfg::kBtStageBytes + j * kSubTileBytes), &mapB,
+                            fb, n_tile * 128 + j * kSubN, kb * kBK, pol_stream);
+                    tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb,
+                                     kb * kBK, 0, pol_keep);
+                    ++armed;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (failed) {
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                const volatile int never = 0;
+                const int64_t rounds = armed / STAGES;
+                for (int s = 0; s < STAGES; ++s) {
+                    uint32_t parity;
+                    if (s < stage) {
+                        parity = phase;
+                    } else if (rounds >= 1) {
+                        parity = phase ^ 1u;
+                    } else {
+                        continue;
+                    }
+                    mbar_wait(smem_u32(&full[s]), parity, &never, 50000000ull);
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+constexpr int kStages16 = 12;
+constexpr int kStages32 = 10;
+constexpr int kStages64 = 8;
+
+template <int MS, int STAGES>
+cudaError_t set_attrs() {
+    return cudaFuncSetAttribute(gemm_skinny_kernel<MS, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SkCfg<MS, STAGES>::kSmemBytes);
+}
+
+template <int MS, int STAGES>
+cudaError_t launch(const CUtensorMap& b, const CUtensorMap& a, const Params& p, uint32_t idesc,
+                   int grid, cudaStream_t s) {
+    gemm_skinny_kernel<MS, STAGES>
+        <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p, idesc);
+    return cudaGetLastError();
+}
+}  // namespace
+
+int skinny_smem_bytes(int ms) {
+    if (ms == 16) return SkCfg<16, kStages16>::kSmemBytes;
+    if (ms == 32) return SkCfg<32, kStages32>::kSmemBytes;
+    return SkCfg<64, kStages64>::kSmemBytes;
+}
+
+int skinny_stages(int ms) { return ms == 16 ? kStages16 : (ms == 32 ? kStages32 : kStages64); }
+
+cudaError_t skinny_prepare() {
+    cudaError_t e = set_attrs<16, kStages16>();
+    if (e == cudaSuccess) e = set_attrs<32, kStages32>();
+    if (e == cudaSuccess) e = set_attrs<64, kStages64>();
+    return e;
+}
+
+cudaError_t launch_skinny(int ms, const CUtensorMap& mapB, const CUtensorMap& mapA,
+                          const Params& p, uint32_t idesc, int grid, cudaStream_t stream) {
+    if (ms == 16) return launch<16, kStages16>(mapB, mapA, p, idesc, grid, stream);
+    if (ms == 32) return launch<32, kStages32>(mapB, mapA, p, idesc, grid, stream);
+    return launch<64, kStages64>(mapB, mapA, p, idesc, grid, stream);
+}
+
+}  // namespace dg

@@ -1,0 +1,408 @@
+// gemm_tc.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// One CTA per SM walks output tiles of 128 x BN in the scheduler's order.
+// Each tile is the K-loop of "acc += A_tile @ B_tile" ("Writing GPU kernels in
+// Triton: Vector Add, Softmax, MatMul", section 3.3; "Triton 04", section
+// "Why have acc"), with the fp32 accumulator held in tensor memory.
+//
+// Warp roles (one CTA):
+//   warp 0        MMA issuer (one thread) and TMEM owner
+//   warps 1..4    epilogue: TMEM -> registers -> masked global stores of C
+//   warp 5        TMA producer (TMA variant), or
+//   warps 5..8    load/store producer (generic variant, any alignment)
+//
+// Shared memory holds a ring of STAGES {A 128x64, B 64xBN} tiles in the
+// 128-byte-swizzled layout; "full" barriers hand a stage to the MMA issuer,
+// "empty" barriers (tcgen05.commit) hand it back.  Two TMEM accumulators of
+// 128 x BN fp32 let the epilogue drain tile i while the MMAs of tile i+1 run.
+//
+// Masking: TMA fills elements outside the global tensor with zeros (the
+// masked load with other=0 of "I Wrote a GPU Matmul Kernel From Scratch in
+// Triton", Step 3); the generic producer writes zeros itself; the epilogue
+// stores only rows < M and columns < N (the masked store).
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace dg {
+
+template <int BN, int STAGES, bool GENERIC>
+struct TcCfg {
+    static constexpr int kBStageBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+    static constexpr int kTmemCols = 2 * BN;               // two fp32 accumulators, power of 2
+    static constexpr int kProducerWarps = GENERIC ? 4 : 1;
+    static constexpr int kThreads = 32 * (1 + 4 + kProducerWarps);
+    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 8 * kNumBars + 16;
+    static_assert(BN % kSubN == 0 && BN >= 64 && BN <= 256, "BN");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void raise_abort(const Params& p, volatile int* abort_flag) {
+    *abort_flag = 1;
+    if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+}
+
+// Eight consecutive 16-bit elements starting at base[off]; elements at or
+// beyond `remaining`, or the whole chunk when !row_ok, read as zero.
+__device__ __forceinline__ uint4 load8(const uint16_t* base, int64_t off, bool row_ok,
+                                       int remaining, int vec) {
+    uint4 r = make_uint4(0u, 0u, 0u, 0u);
+    if (!row_ok || remaining <= 0) return r;
+    const uint16_t* ptr = base + off;
+    if (vec && remaining >= 8) return __ldg(reinterpret_cast<const uint4*>(ptr));
+    uint32_t e[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = (i < remaining) ? static_cast<uint32_t>(__ldg(ptr + i)) : 0u;
+    r.x = e[0] | (e[1] << 16);
+    r.y = e[2] | (e[3] << 16);
+    r.z = e[4] | (e[5] << 16);
+    r.w = e[6] | (e[7] << 16);
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// 32 consecutive fp32 values of one C row, the first `ncols` of them in range.
+__device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], int ncols,
+                                            int vec) {
+    if (vec && ncols >= 32) {
+        float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i < ncols) dst[i] = __uint_as_float(v[i]);
+    }
+}
+
+template <int BN, int STAGES, bool GENERIC>
+__global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
+                   const __grid_constant__ CUtensorMap mapB, const Params p,
+                   const uint32_t idesc) {
+    using Cfg = TcCfg<BN, STAGES, GENERIC>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * kAStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBStageBytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + STAGES;
+    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), GENERIC ? 128u : 1u);
+            mbar_init(smem_u32(&empty[s]), 1u);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1u);
+            mbar_init(smem_u32(&tempty[a]), 128u);
+        }
+        mbar_init(smem_u32(drain), 1u);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    if (!GENERIC && warp == 5 && lane == 0) {
+        prefetch_tmap(&mapA);
+        prefetch_tmap(&mapB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total = p.tiles_m * p.tiles_n;
+    const int num_kb = p.num_kb;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool failed = false;
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.timeout_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t a0 =
+                        sdesc_sw128(smem_u32(sA + stage * kAStageBytes), 16u, 1024u);
+                    const uint64_t b0 = sdesc_sw128(smem_u32(sB + stage * Cfg::kBStageBytes),
+                                                    static_cast<uint32_t>(kSubTileBytes), 1024u);
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        // K-major A: +32 B per 16 elements inside the swizzle row.
+                        // MN-major B: +16 K-rows of 128 B.
+                        tc_mma_f16(d_tmem, a0 + static_cast<uint64_t>((k * 32) >> 4),
+                                   b0 + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc,
+                                   (kb | k) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (failed) break;
+                tc_commit(smem_u32(&tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (failed) {
+                raise_abort(p, abort_flag);
+                // Let every MMA already issued finish before TMEM is released.
+                const volatile int never = 0;
+                tc_commit(smem_u32(drain));
+                mbar_wait(smem_u32(drain), 0u, &never, 100000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp <= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int tm, tn;
+            tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+            const bool ok =
+                mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
+            if (!__all_sync(0xffffffffu, ok)) {
+                raise_abort(p, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const int row = tm * kBM + row_in_tile;
+            const int col0 = tn * BN;
+            float* crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+            const bool row_ok = row < p.M;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
+                tmem_ld_wait(v);
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(&tempty[acc]));
+                }
+                if (row_ok) store_row32(crow + c * 32, v, p.N - (col0 + c * 32), p.c_vec);
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    } else if (!GENERIC) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool failed = false;
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t armed = 0;
+            for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+                int tm, tn;
+                tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
+                                   p.timeout_ns)) {
+                        failed = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
+                    tma_load_2d(smem_u32(sA + stage * kAStageBytes), &mapA, fb, kb * kBK,
+                                tm * kBM);
+#pragma unroll
+                    for (int j = 0; j < BN / kSubN; ++j)
+                        tma_load_2d(smem_u32(sB + stage * Cfg::kBStageBytes + j * kSubTileBytes),
+                                    &mapB, fb, tn * BN + j * kSubN, kb * kBK);
+                    ++armed;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (failed) {
+                raise_abort(p, abort_flag);
+                // Wait (bounded) for the copies already issued to land before the CTA exits.
+                const volatile int never = 0;
+                const int64_t rounds = armed / STAGES;
+                for (int s = 0; s < STAGES; ++s) {
+                    uint32_t parity;
+                    if (s < stage) {
+                        parity = phase;
+                    } else if (rounds >= 1) {
+                        parity = phase ^ 1u;
+                    } else {
+                        continue;
+                    }
+                    mbar_wait(smem_u32(&full[s]), parity, &never, 50000000ull);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ generic producer
+        const int pt = threadIdx.x - 160;     // 0..127
+        int stage = 0;
+        uint32_t phase = 0;
+        constexpr int kBChunks = (kBK * BN / 8) / 128;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            int tm, tn;
+            tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+            bool failed = false;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
+                    failed = true;
+                    break;
+                }
+                const int k0 = kb * kBK;
+                uint4 ra[8];
+                uint4 rb[kBChunks];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = pt + i * 128;
+                    const int r = c >> 3, kc = c & 7;
+                    const int m = tm * kBM + r, k = k0 + kc * 8;
+                    ra[i] = load8(p.A, static_cast<int64_t>(m) * p.lda + k, m < p.M, p.K - k,
+                                  p.a_vec);
+                }
+#pragma unroll
+                for (int i = 0; i < kBChunks; ++i) {
+                    const int c = pt + i * 128;
+                    const int kr = c / (BN / 8), nc = c % (BN / 8);
+                    const int k = k0 + kr, n = tn * BN + nc * 8;
+                    rb[i] = load8(p.B, static_cast<int64_t>(k) * p.ldb + n, k < p.K, p.N - n,
+                                  p.b_vec);
+                }
+                const uint32_t a_dst = smem_u32(sA + stage * kAStageBytes);
+                const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStageBytes);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int c = pt + i * 128;
+                    const int r = c >> 3, kc = c & 7;
+                    st_shared_v4(a_dst + r * 128 + ((kc ^ (r & 7)) << 4), ra[i]);
+                }
+#pragma unroll
+                for (int i = 0; i < kBChunks; ++i) {
+                    const int c = pt + i * 128;
+                    const int kr = c / (BN / 8), nc = c % (BN / 8);
+                    st_shared_v4(b_dst + (nc >> 3) * kSubTileBytes + kr * 128 +
+                                     (((nc & 7) ^ (kr & 7)) << 4),
+                                 rb[i]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (failed) {
+                raise_abort(p, abort_flag);
+                break;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+constexpr int kTmaStages256 = 4;
+constexpr int kTmaStages128 = 6;
+constexpr int kGenericStages = 4;
+
+template <int BN, int STAGES, bool GENERIC>
+cudaError_t set_attrs() {
+    using Cfg = TcCfg<BN, STAGES, GENERIC>;
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, GENERIC>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+}
+
+template <int BN, int STAGES, bool GENERIC>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, uint32_t idesc,
+                   int grid, cudaStream_t s) {
+    using Cfg = TcCfg<BN, STAGES, GENERIC>;
+    gemm_tc_kernel<BN, STAGES, GENERIC><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p,
+                                                                                    idesc);
+    return cudaGetLastError();
+}
+}  // namespace
+
+int tma_smem_bytes(int bn) {
+    return bn == 256 ? TcCfg<256, kTmaStages256, false>::kSmemBytes
+                     : TcCfg<128, kTmaStages128, false>::kSmemBytes;
+}
+
+int tma_stages(int bn) { return bn == 256 ? kTmaStages256 : kTmaStages128; }
+
+cudaError_t tma_prepare() {
+    cudaError_t e = set_attrs<256, kTmaStages256, false>();
+    if (e != cudaSuccess) return e;
+    return set_attrs<128, kTmaStages128, false>();
+}
+
+cudaError_t launch_tma(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
+                       uint32_t idesc, int grid, cudaStream_t stream) {
+    if (bn == 256) return launch<256, kTmaStages256, false>(mapA, mapB, p, idesc, grid, stream);
+    return launch<128, kTmaStages128, false>(mapA, mapB, p, idesc, grid, stream);
+}
+
+int generic_smem_bytes() { return TcCfg<128, kGenericStages, true>::kSmemBytes; }
+
+int generic_stages() { return kGenericStages; }
+
+cudaError_t generic_prepare() { return set_attrs<128, kGenericStages, true>(); }
+
+cudaError_t launch_generic(const Params& p, uint32_t idesc, int grid, cudaStream_t stream) {
+    CUtensorMap dummy;
+    memset(&dummy, 0, sizeof(dummy));
+    return launch<128, kGenericStages, true>(dummy, dummy, p, idesc, grid, stream);
+}
+
+}  // namespace dg

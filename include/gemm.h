@@ -1,0 +1,177 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense matrix multiply library.
+ *
+ * Operation (the tiled matmul of "I Wrote a GPU Matmul Kernel From Scratch in
+ * Triton", Steps 1-5, and of "Triton 04: Matmul, Autotune and PyTorch
+ * integration", section "A teaching matmul kernel"):
+ *
+ *     C[i, j] = sum_{k=0}^{K-1} A[i, k] * B[k, j]      0 <= i < M, 0 <= j < N
+ *
+ * with A and B in fp16 or bf16 (both the same type), products accumulated in
+ * fp32, and C written in fp32 (the output type of the teaching kernel's
+ * wrapper on the "Triton 04" page).  All three matrices are row-major with
+ * unit inner stride and an explicit leading dimension, in ELEMENTS, as in
+ * section 4.1 of "Writing GPU kernels in Triton: Vector Add, Softmax, MatMul":
+ *
+ *     A[i, k] at A + i*lda + k     (lda >= K)
+ *     B[k, j] at B + k*ldb + j     (ldb >= N)
+ *     C[i, j] at C + i*ldc + j     (ldc >= N)
+ *
+ * Ragged edges are masked: elements outside the M x K, K x N and M x N
+ * rectangles are never read (they act as zeros, the masked loads with
+ * other=0 of Step 3) and never written (the masked store).  C is overwritten;
+ * its previous contents never matter.
+ *
+ * Threading / ownership: the caller owns A, B, C (device memory) and the
+ * stream.  A plan owns a small device workspace (split-K partial sums and
+ * tile counters) and must not be used by two gemm_run calls that can be in
+ * flight at the same time on different streams; use one plan per stream.
+ * Nothing here synchronises the stream unless GEMM_DEBUG_SYNC=1 is set in the
+ * environment (then gemm_run waits for the kernel and reports device-side
+ * timeouts as GEMM_ERR_TIMEOUT).
+ */
+#ifndef DENSE_GEMM_05_GB300_GEMM_H
+#define DENSE_GEMM_05_GB300_GEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                         /* == cudaStream_t / CUstream */
+typedef struct gemm_plan_s *gemm_plan_t;    /* opaque */
+
+typedef enum {
+    GEMM_F16 = 0,   /* IEEE binary16 inputs */
+    GEMM_BF16 = 1   /* bfloat16 inputs */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* null pointer / plan, negative size, ld too small, overlap,
+                                   misaligned element pointer */
+    GEMM_ERR_UNSUPPORTED = 2,   /* unknown dtype, not an sm_103 device, size beyond 2^31-1 */
+    GEMM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch error etc.) */
+    GEMM_ERR_OOM = 4,           /* workspace allocation failed */
+    GEMM_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (debug-sync mode) */
+} gemm_status_t;
+
+/* Which kernel gemm_run selects for a problem (see gemm_query). */
+typedef enum {
+    GEMM_KERNEL_NONE = 0,       /* M == 0 or N == 0: nothing is launched */
+    GEMM_KERNEL_ZERO_FILL = 1,  /* K == 0: C is set to zero (the empty sum) */
+    GEMM_KERNEL_TMA = 2,        /* persistent warp-specialised tcgen05 kernel fed by TMA */
+    GEMM_KERNEL_GENERIC = 3,    /* same pipeline, operands staged by ordinary loads
+                                   (leading dimensions or pointers not 16-byte aligned) */
+    GEMM_KERNEL_SKINNY = 4,     /* small M: swap-AB + split-K, deterministic reduction */
+    GEMM_KERNEL_PAIR = 5        /* 2-SM (cta_group::2) pair tiles for large problems */
+} gemm_kernel_t;
+
+typedef struct {
+    int32_t kernel;       /* gemm_kernel_t */
+    int32_t block_m;      /* rows of C per tile (per CTA pair for GEMM_KERNEL_PAIR) */
+    int32_t block_n;      /* columns of C per tile */
+    int32_t block_k;      /* K depth of one pipeline stage */
+    int32_t stages;       /* shared-memory ring depth */
+    int32_t split_k;      /* K slices per output tile (1 = none) */
+    int32_t grid;         /* CTAs launched (persistent kernels: one per SM or fewer) */
+    int32_t cluster;      /* CTAs per cluster */
+    int32_t group;        /* group-major strip height in tiles (0 = row-major order) */
+    int32_t tiles;        /* output tiles (work units for split-K) */
+} gemm_config_t;
+
+/*
+ * Create a plan on CUDA device `device` (that device becomes current for the
+ * call).  Checks that the device is compute capability 10.3, queries the SM
+ * count, sets kernel attributes and allocates the plan's workspace.
+ * Errors: INVALID_ARG (out == NULL), UNSUPPORTED (not sm_103), CUDA, OOM.
+ * On error *out is set to NULL.
+ */
+GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t *out, int device);
+
+/*
+ * C = A @ B (see the top of this file).  Asynchronous on `stream` (NULL = the
+ * legacy default stream); A, B, C are device pointers; dtype is the type of
+ * both A and B.  A and B must be 2-byte aligned, C 4-byte aligned.
+ * The region written, rows [0, M) x columns [0, N) of C, must not overlap the
+ * regions read from A or B.
+ * M == 0 or N == 0: no-op.  K == 0: C[0:M, 0:N] = 0.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA (launch failure), TIMEOUT (only in
+ * debug-sync mode).  Nothing is launched when an error is returned, except
+ * for CUDA/TIMEOUT, which report a failure of the launched work itself.
+ */
+GEMM_API gemm_status_t gemm_run(gemm_plan_t plan,
+                       const void *A, int64_t lda,
+                       const void *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       int64_t M, int64_t N, int64_t K,
+                       gemm_dtype_t dtype, struct CUstream_st *stream);
+
+/* Release the plan and its workspace.  NULL-safe.  Waits for nothing: the
+ * caller must make sure no gemm_run using the plan is still in flight. */
+GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+GEMM_API const char *gemm_status_string(gemm_status_t s);
+
+/*
+ * Report the kernel and configuration gemm_run would use for these
+ * arguments, without launching anything (the offline-tuned replacement of the
+ * autotune step of Step 5 / the "What autotune selects" section).
+ * Same argument checks and errors as gemm_run.
+ */
+GEMM_API gemm_status_t gemm_query(gemm_plan_t plan,
+                         const void *A, int64_t lda,
+                         const void *B, int64_t ldb,
+                         const float *C, int64_t ldc,
+                         int64_t M, int64_t N, int64_t K,
+                         gemm_dtype_t dtype, gemm_config_t *out);
+
+/*
+ * Override the plan's tile order for the persistent kernels: group > 0 is the
+ * group-major order of Step 4 with strips `group` tiles tall; group == 0 is
+ * the row-major order of the "Triton 04" teaching kernel.  Default 8.
+ * Errors: INVALID_ARG (null plan, group < 0 or > 64).
+ */
+GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
+
+/*
+ * Force the next gemm_run calls on this plan to use `kernel` (a
+ * gemm_kernel_t of TMA, GENERIC, SKINNY or PAIR; 0 = automatic choice), and
+ * `split_k` K-slices for SKINNY (0 = automatic).  For tests and tuning.
+ * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
+ * arguments (e.g. TMA with a leading dimension that is not a multiple of 8).
+ */
+GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k);
+
+/*
+ * The scheduler's tile order, evaluated on the host by the same function the
+ * kernels use: linear work index t -> (tile_m, tile_n) for a grid of
+ * tiles_m x tiles_n tiles and strip height `group` (0 = row-major).
+ * Errors: INVALID_ARG (null outputs, t outside [0, tiles_m*tiles_n), bad sizes).
+ */
+GEMM_API gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group,
+                              int64_t *tile_m, int64_t *tile_n);
+
+/*
+ * Device-side wait self-test: launches one block that waits on a shared-memory
+ * barrier nobody arrives on, with a limit of `timeout_us` microseconds, then
+ * synchronises `stream`.  Returns GEMM_ERR_TIMEOUT when the bounded wait gave
+ * up as designed (the expected result), GEMM_OK if it did not time out, or
+ * GEMM_ERR_CUDA.  Used by tests to check that every spin-wait in the kernels
+ * ends; the CUDA context stays usable afterwards.
+ */
+GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_05_GB300_GEMM_H */

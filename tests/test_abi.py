@@ -1,0 +1,79 @@
+"""C-ABI library checks that need no GPU: it loads, exports every function the
+header declares, and its host-side logic (status strings, argument checks that
+precede any CUDA call, the scheduler's tile order) behaves as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_gemm_05_gb300 as g
+from oracle import schedule
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    g.build()
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += [n for n in re.findall(r"GEMM_API\s+[\w\s\*]*?\b(\w+)\s*\(", text) if n.startswith("gemm_")]
+    return names
+
+
+def test_header_declares_the_binding_functions():
+    assert sorted(declared_functions()) == sorted(g.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(g.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert g.status_string(0) == "GEMM_OK"
+    assert g.status_string(1) == "GEMM_ERR_INVALID_ARG"
+    assert g.status_string(5) == "GEMM_ERR_TIMEOUT"
+    assert g.status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_null_plan_is_rejected_before_any_cuda_call():
+    assert g.gemm_run(None, 0, 1, 0, 1, 0, 1, 1, 1, 1, g.GEMM_F16, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan_destroy(None) == g.GEMM_OK
+    assert g.gemm_plan_set_group(None, 8) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan_force(None, 0, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.lib().gemm_plan_create(None, 0) == g.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("tm,tn,grp", [(4, 4, 2), (5, 3, 2), (64, 32, 8), (7, 11, 3), (13, 1, 8),
+                                       (1, 9, 4), (32, 32, 16), (9, 5, 1), (6, 6, 0), (3, 17, 0)])
+def test_tile_order_matches_the_oracle(tm, tn, grp):
+    for t in range(tm * tn):
+        want = (schedule.row_major_tile(t, tn) if grp == 0
+                else schedule.group_major_tile(t, tm, tn, grp))
+        assert g.gemm_tile_coord(t, tm, tn, grp) == want
+
+
+def test_tile_order_rejects_bad_arguments():
+    with pytest.raises(g.GemmError):
+        g.gemm_tile_coord(16, 4, 4, 2)
+    with pytest.raises(g.GemmError):
+        g.gemm_tile_coord(-1, 4, 4, 2)
+    with pytest.raises(g.GemmError):
+        g.gemm_tile_coord(0, 0, 4, 2)
+
+
+def test_plan_create_without_a_usable_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = g.lib().gemm_plan_create(ctypes.byref(h), 0)
+    assert st in (g.GEMM_ERR_CUDA, g.GEMM_ERR_INVALID_ARG) and not h.value

@@ -1,0 +1,317 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerance (the problem's stated bar): |C_gpu - C_ref| <= 1e-3 * sum_k |A_ik||B_kj| + 1e-5
+element-wise.  Integer-valued inputs (entries in [-4, 4], |sums| < 2^24) must
+match bit for bit.  Every C buffer carries guard cells (extra rows and a padded
+leading dimension filled with a sentinel) that must survive unchanged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_05_gb300 as g
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = 1234.5
+REL, ABS = 1e-3, 1e-5
+
+
+@pytest.fixture(scope="module")
+def plan():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.build()
+    p = g.Plan(0)
+    yield p
+    p.close()
+
+
+def run(plan, A, B, M, N, K, *, ldc=None, kernel=0, split=0, group=None, expect=None):
+    """Copy A, B (CPU, possibly padded) to the GPU, run the C ABI, return the C buffer."""
+    ldc = N if ldc is None else ldc
+    dev = torch.device("cuda:0")
+    a, b = A.to(dev), B.to(dev)
+    cbuf = torch.full((M + 2, max(ldc, 1)), SENTINEL, dtype=torch.float32, device=dev)
+    plan.force(kernel, split)
+    if group is not None:
+        plan.set_group(group)
+    try:
+        if expect is not None:
+            cfg = plan.query(a, b, cbuf, M, N, K)
+            assert cfg["kernel"] == expect, cfg
+        plan.run(a, b, cbuf, M, N, K)
+        torch.cuda.synchronize()
+    finally:
+        plan.force(0, 0)
+        if group is not None:
+            plan.set_group(8)
+    return cbuf.cpu().double().numpy()
+
+
+def assert_guards(cbuf, M, N):
+    assert np.all(cbuf[:M, N:] == SENTINEL), "a store landed right of column N"
+    assert np.all(cbuf[M:, :] == SENTINEL), "a store landed below row M"
+
+
+def assert_close(got, A, B, M, N, K, what=""):
+    ref = oracle.gemm(A, B, K=K, N=N)
+    bnd = oracle.absbound(A, B, K=K, N=N)
+    ok = np.abs(got - ref) <= REL * bnd + ABS
+    if not ok.all():
+        idx = np.argwhere(~ok)
+        i, j = idx[0]
+        raise AssertionError(
+            f"{what}: {len(idx)} of {ok.size} entries outside tolerance; first at ({i}, {j}): "
+            f"gpu {got[i, j]!r} oracle {ref[i, j]!r} bound {bnd[i, j]!r}")
+    return ref
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_wait_selftest_gives_up_and_context_survives(plan):
+    st = g.gemm_wait_selftest(2000, torch.cuda.current_stream().cuda_stream)
+    assert st == g.GEMM_ERR_TIMEOUT
+    A, B = workloads.custom(64, 64, 64, "f16", seed=0)
+    got = run(plan, A, B, 64, 64, 64)
+    assert_close(got[:64, :64], A, B, 64, 64, 64, "after self-test")
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def test_workload_256_f16_full(plan):
+    w = workloads.WORKLOADS["gemm256_f16"]
+    A, B = workloads.make_inputs(w)
+    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_TMA)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+
+
+def test_workload_ragged_f16_full(plan):
+    """M=1023 K=1000 N=1029: ldb = 1029 halves is not a 16-byte pitch -> generic producer."""
+    w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
+    A, B = workloads.make_inputs(w)
+    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_GENERIC)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+
+
+def test_workload_ragged_f16_padded_pitch_uses_tma(plan):
+    """Same logical shape with 16-byte pitches (NaN padding): TMA path, ragged edges."""
+    w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
+    A, B = workloads.make_inputs(w, lda=1008, ldb=1032)
+    got = run(plan, A, B, w.M, w.N, w.K, ldc=1032, expect=g.GEMM_KERNEL_TMA)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " padded")
+
+
+def test_workload_skinny_full_and_deterministic(plan):
+    w = workloads.WORKLOADS["skinny16x4096x14336_bf16"]
+    A, B = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
+    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY and cfg["split_k"] > 1, cfg
+    got1 = run(plan, A, B, w.M, w.N, w.K)
+    got2 = run(plan, A, B, w.M, w.N, w.K)
+    assert_guards(got1, w.M, w.N)
+    assert np.array_equal(got1, got2), "split-K result changed between runs"
+    assert_close(got1[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+
+
+def _sample_entries(M, N, bm, bn, n_random, seed):
+    """n_random uniform entries plus, for every tile on the border of C, its four
+    corners and 16 random entries."""
+    rng = np.random.default_rng(seed)
+    rows = list(rng.integers(0, M, n_random))
+    cols = list(rng.integers(0, N, n_random))
+    tm, tn = -(-M // bm), -(-N // bn)
+    for ti in range(tm):
+        for tj in range(tn):
+            if ti not in (0, tm - 1) and tj not in (0, tn - 1):
+                continue
+            r0, c0 = ti * bm, tj * bn
+            r1, c1 = min(M, r0 + bm) - 1, min(N, c0 + bn) - 1
+            rows += [r0, r0, r1, r1] + list(rng.integers(r0, r1 + 1, 16))
+            cols += [c0, c1, c0, c1] + list(rng.integers(c0, c1 + 1, 16))
+    return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["square4096_bf16", "square8192_bf16"])
+def test_workload_square_sampled(plan, name):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    a, b = A.to(dev), B.to(dev)
+    c = torch.full((w.M, w.N), float("nan"), dtype=torch.float32, device=dev)
+    cfg = plan.query(a, b, c)
+    assert cfg["kernel"] == g.GEMM_KERNEL_TMA, cfg
+    plan.run(a, b, c)
+    torch.cuda.synchronize()
+    assert not torch.isnan(c).any().item(), "some C entries were never written"
+    rows, cols = _sample_entries(w.M, w.N, cfg["block_m"], cfg["block_n"], 4096, w.seed)
+    got = c[torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)].cpu().double().numpy()
+    ref, bnd = oracle.gemm_entries(A, B, rows, cols)
+    ok = np.abs(got - ref) <= REL * bnd + ABS
+    assert ok.all(), f"{name}: {int((~ok).sum())} of {ok.size} sampled entries outside tolerance"
+
+
+# ---------------------------------------------------------------- exactness
+
+def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
+    gen = torch.Generator().manual_seed(seed)
+    td = torch.float16 if dtype == "f16" else torch.bfloat16
+    A = torch.randint(-4, 5, (M, K), generator=gen).to(td)
+    B = torch.randint(-4, 5, (K, N), generator=gen).to(td)
+    if lda is not None:
+        Ap = torch.full((M, lda), float("nan"), dtype=td)
+        Ap[:, :K] = A
+        A = Ap
+    if ldb is not None:
+        Bp = torch.full((K, ldb), float("nan"), dtype=td)
+        Bp[:, :N] = B
+        B = Bp
+    return A, B
+
+
+@pytest.mark.parametrize("kernel,split,shape,dtype", [
+    (g.GEMM_KERNEL_TMA, 0, (300, 1000, 520), "bf16"),
+    (g.GEMM_KERNEL_TMA, 0, (1024, 2048, 1024), "f16"),
+    (g.GEMM_KERNEL_GENERIC, 0, (300, 1000, 520), "f16"),
+    (g.GEMM_KERNEL_SKINNY, 1, (16, 4096, 1024), "bf16"),
+    (g.GEMM_KERNEL_SKINNY, 4, (16, 4096, 1024), "bf16"),
+    (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
+    (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
+])
+def test_small_integer_inputs_are_bit_exact(plan, kernel, split, shape, dtype):
+    M, K, N = shape
+    A, B = int_inputs(M, K, N, dtype, seed=M + K + N)
+    got = run(plan, A, B, M, N, K, kernel=kernel, split=split, expect=kernel)
+    assert_guards(got, M, N)
+    ref = oracle.gemm(A, B)
+    assert np.array_equal(got[:M, :N], ref), f"max diff {np.abs(got[:M, :N] - ref).max()}"
+
+
+def test_mn_major_layout_pin(plan):
+    """A = I, B with distinct entries: C must equal B exactly (a transposed or
+    mis-swizzled B tile shows up as a permutation)."""
+    M = K = 192
+    N = 320
+    A = torch.eye(M, K, dtype=torch.bfloat16)
+    B = (torch.arange(K * N, dtype=torch.float32).reshape(K, N) % 251).to(torch.bfloat16)
+    for kernel in (g.GEMM_KERNEL_TMA, g.GEMM_KERNEL_GENERIC):
+        got = run(plan, A, B, M, N, K, kernel=kernel)
+        assert np.array_equal(got[:M, :N], B.double().numpy()), kernel
+    # skinny: first 16 rows of the identity
+    A16 = torch.eye(16, K, dtype=torch.bfloat16)
+    got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SKINNY, split=2)
+    assert np.array_equal(got[:16, :N], B[:16].double().numpy())
+
+
+# ---------------------------------------------------------------- ragged sweep
+
+SWEEP = [(m, n, k) for m in (1, 17, 128, 129, 255) for n in (1, 15, 128, 257)
+         for k in (1, 16, 63, 130)] + [(1000, 1023, 127), (127, 255, 1000), (65, 4096, 96)]
+
+
+@pytest.mark.parametrize("M,N,K", SWEEP)
+def test_ragged_sweep(plan, M, N, K):
+    A, B = workloads.custom(M, K, N, "f16", seed=M * 7 + N * 3 + K)
+    got = run(plan, A, B, M, N, K)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(129, 257, 130), (17, 128, 63), (255, 15, 1000)])
+def test_ragged_sweep_padded_pitches_tma(plan, M, N, K):
+    lda, ldb = -(-K // 8) * 8 + 8, -(-N // 8) * 8 + 8
+    A, B = workloads.custom(M, K, N, "bf16", seed=K, lda=lda, ldb=ldb)
+    got = run(plan, A, B, M, N, K, ldc=N + 3)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"padded {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- degenerate sizes
+
+def test_k_zero_writes_zeros(plan):
+    A = torch.zeros(5, 0, dtype=torch.float16)
+    B = torch.zeros(0, 7, dtype=torch.float16)
+    dev = torch.device("cuda:0")
+    cbuf = torch.full((7, 9), SENTINEL, dtype=torch.float32, device=dev)
+    st = g.gemm_run(plan.handle, 0, 0, 0, 7, cbuf.data_ptr(), 9, 5, 7, 0, g.GEMM_F16,
+                    torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == g.GEMM_OK
+    c = cbuf.cpu().numpy()
+    assert np.all(c[:5, :7] == 0.0)
+    assert np.all(c[:5, 7:] == SENTINEL) and np.all(c[5:] == SENTINEL)
+    del A, B
+
+
+@pytest.mark.parametrize("M,N", [(0, 7), (5, 0), (0, 0)])
+def test_empty_output_is_a_no_op(plan, M, N):
+    dev = torch.device("cuda:0")
+    cbuf = torch.full((4, 8), SENTINEL, dtype=torch.float32, device=dev)
+    a = torch.ones(8, 8, dtype=torch.float16, device=dev)
+    st = g.gemm_run(plan.handle, a.data_ptr(), 8, a.data_ptr(), 8, cbuf.data_ptr(), 8, M, N, 8,
+                    g.GEMM_F16, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == g.GEMM_OK
+    assert torch.all(cbuf == SENTINEL).item()
+
+
+# ---------------------------------------------------------------- scheduler order
+
+@pytest.mark.parametrize("group", [0, 1, 3, 8, 16])
+def test_tile_order_does_not_change_bits(plan, group):
+    A, B = workloads.custom(1000, 512, 1300, "bf16", seed=21, dist="normal")
+    base = run(plan, A, B, 1000, 1300, 512, group=8)
+    got = run(plan, A, B, 1000, 1300, 512, group=group)
+    assert np.array_equal(base, got)
+
+
+# ---------------------------------------------------------------- argument checks
+
+def test_argument_errors(plan):
+    dev = torch.device("cuda:0")
+    a = torch.ones(64, 64, dtype=torch.bfloat16, device=dev)
+    c = torch.empty(64, 64, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    h = plan.handle
+    A, C = a.data_ptr(), c.data_ptr()
+    E = g.GEMM_ERR_INVALID_ARG
+    U = g.GEMM_ERR_UNSUPPORTED
+    assert g.gemm_run(h, A, 63, A, 64, C, 64, 64, 64, 64, g.GEMM_BF16, s) == E      # lda < K
+    assert g.gemm_run(h, A, 64, A, 63, C, 64, 64, 64, 64, g.GEMM_BF16, s) == E      # ldb < N
+    assert g.gemm_run(h, A, 64, A, 64, C, 63, 64, 64, 64, g.GEMM_BF16, s) == E      # ldc < N
+    assert g.gemm_run(h, A, 64, A, 64, C, 64, -1, 64, 64, g.GEMM_BF16, s) == E      # M < 0
+    assert g.gemm_run(h, 0, 64, A, 64, C, 64, 64, 64, 64, g.GEMM_BF16, s) == E      # A null
+    assert g.gemm_run(h, A, 64, A, 64, 0, 64, 64, 64, 64, g.GEMM_BF16, s) == E      # C null
+    assert g.gemm_run(h, A + 1, 64, A, 64, C, 64, 64, 64, 64, g.GEMM_BF16, s) == E  # odd address
+    assert g.gemm_run(h, A, 64, A, 64, C + 2, 64, 64, 64, 64, g.GEMM_BF16, s) == E  # C misaligned
+    assert g.gemm_run(h, A, 64, A, 64, A, 64, 32, 32, 64, g.GEMM_BF16, s) == E      # C overlaps A
+    assert g.gemm_run(h, A, 64, A, 64, C, 64, 64, 64, 64, 7, s) == U                # dtype
+    assert g.gemm_run(h, A, 64, A, 64, C, 64, 1 << 31, 64, 64, g.GEMM_BF16, s) == U
+    plan.force(g.GEMM_KERNEL_TMA, 0)
+    try:
+        assert g.gemm_run(h, A, 63, A, 64, C, 64, 64, 64, 63, g.GEMM_BF16, s) == U  # TMA pitch
+    finally:
+        plan.force(0, 0)
+    torch.cuda.synchronize()
+
+
+def test_kernel_selection(plan):
+    dev = torch.device("cuda:0")
+    def q(M, K, N, lda=None, ldb=None):
+        a = torch.empty(M, lda or K, dtype=torch.bfloat16, device=dev)
+        b = torch.empty(K, ldb or N, dtype=torch.bfloat16, device=dev)
+        c = torch.empty(M, N, dtype=torch.float32, device=dev)
+        return plan.query(a, b, c, M, N, K)
+    assert q(8192, 8192, 8192)["kernel"] == g.GEMM_KERNEL_TMA
+    assert q(8192, 8192, 8192)["block_n"] == 256
+    assert q(1023, 1000, 1029)["kernel"] == g.GEMM_KERNEL_GENERIC
+    s = q(16, 4096, 14336)
+    assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["split_k"] > 1 and s["block_m"] == 16
+    assert q(64, 512, 512)["kernel"] == g.GEMM_KERNEL_SKINNY
+    assert q(65, 512, 512)["kernel"] == g.GEMM_KERNEL_TMA
