@@ -410,6 +410,28 @@ def end_to_end(torch, g, plan, w, A, B, dev, stream, steps, world, dist) -> dict
             "d2h_bytes_per_step": hc.numel() * 4}
 
 
+def run_case(args) -> None:
+    """Profiling helper: `--launches` back-to-back GEMMs of one workload, nothing else."""
+    import torch
+
+    import dense_gemm_05_gb300 as g
+    import workloads
+    g.build()
+    w = workloads.WORKLOADS[args.case]
+    A, B = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    a, b = A.to(dev), B.to(dev)
+    c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+    plan = g.Plan(0)
+    cfg = plan.query(a, b, c)
+    torch.cuda.synchronize()
+    for _ in range(args.launches):
+        plan.run(a, b, c)
+    torch.cuda.synchronize()
+    print(json.dumps({"case": w.name, "launches": args.launches, "kernel": cfg}), flush=True)
+    plan.close()
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -419,7 +441,13 @@ def main() -> None:
     ap.add_argument("--quick", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="profiling: run only this workload's GEMM --launches times")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
 
