@@ -42,7 +42,12 @@ KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 
 #: Every function the header declares (checked by the tests against the library's exports).
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
-                 "gemm_wait_selftest")
+                 "gemm_wait_selftest", "gemm_run_noalloc")
+
+#: Limits of gemm_run_noalloc (mirrors of the header's macros).
+GEMM_NOALLOC_MAX_M = 64
+GEMM_NOALLOC_MAX_N = 131072
+GEMM_NOALLOC_SCRATCH_BYTES = 8392704
 
 
 class GemmError(RuntimeError):
@@ -98,6 +103,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_tile_coord.restype = i32
         L.gemm_wait_selftest.argtypes = [u32, vp]
         L.gemm_wait_selftest.restype = i32
+        L.gemm_run_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, vp]
+        L.gemm_run_noalloc.restype = i32
         _lib = L
         return L
 
@@ -154,6 +161,13 @@ def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int) -> tuple[int
 
 def gemm_wait_selftest(timeout_us: int, stream: int = 0) -> int:
     return int(lib().gemm_wait_selftest(timeout_us, stream))
+
+
+def gemm_run_noalloc(A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M: int, N: int,
+                     K: int, dtype: int, stream: int = 0) -> int:
+    """Small-M C = A @ B on the current device with no plan and no allocation (for
+    callers that cannot allocate device memory); returns the gemm_status_t code."""
+    return int(lib().gemm_run_noalloc(A, lda, B, ldb, C, ldc, M, N, K, dtype, stream))
 
 
 # ------------------------------------------------------------------ torch convenience

@@ -170,6 +170,44 @@ GEMM_API gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles
  */
 GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st *stream);
 
+/*
+ * gemm_run_noalloc -- C = A @ B for small M without a plan and without any
+ * allocation.  The pages have no counterpart to this entry point; it exists
+ * for callers that cannot allocate device memory.  A serving process that
+ * gives all free device memory to its own pool at start-up has none left for
+ * a library's workspace, and a latency-sensitive loop that shares the GPU
+ * with other streams cannot take the device-wide synchronisation that
+ * cudaMalloc/cudaFree may cause.  Such callers pass A, B and C as usual; the
+ * scratch the split-K kernel needs (fp32 partial tiles and per-tile counters)
+ * lives in one static device array of GEMM_NOALLOC_SCRATCH_BYTES that every
+ * GPU which loads this library holds until the process exits.
+ *
+ * Same operation, layout and argument rules as gemm_run, on the CURRENT device
+ * and `stream`.  Limits: M <= GEMM_NOALLOC_MAX_M, N <= GEMM_NOALLOC_MAX_N,
+ * A and B 16-byte aligned with lda and ldb multiples of 8 elements; anything
+ * beyond them returns GEMM_ERR_UNSUPPORTED and launches nothing.  The K split
+ * is chosen to fit the scratch.  This call never calls cudaMalloc, cudaFree or
+ * any allocating routine.
+ *
+ * The first call on a device does a one-time set-up for that device (checks
+ * the architecture, sets kernel attributes and looks up the scratch array's
+ * device address); make that first call before any stream capture.  Every
+ * call on a device shares the one scratch array, which keeps the last call's
+ * contents (each call clears the counters it uses): calls that can overlap on
+ * the GPU -- on different streams, or from different threads -- race and give
+ * wrong results.  Serialise them.
+ * Errors: INVALID_ARG and UNSUPPORTED as above, CUDA for a failed set-up or
+ * launch.
+ */
+#define GEMM_NOALLOC_MAX_M 64
+#define GEMM_NOALLOC_MAX_N 131072
+#define GEMM_NOALLOC_SCRATCH_BYTES 8392704   /* 8 MiB of partial tiles + 4 KiB of counters */
+GEMM_API gemm_status_t gemm_run_noalloc(const void *A, int64_t lda,
+                                        const void *B, int64_t ldb,
+                                        float *C, int64_t ldc,
+                                        int64_t M, int64_t N, int64_t K,
+                                        gemm_dtype_t dtype, struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif
