@@ -96,7 +96,7 @@ def lib() -> ctypes.CDLL:
         L.gemm_query.restype = i32
         L.gemm_plan_set_group.argtypes = [vp, i32]
         L.gemm_plan_set_group.restype = i32
-        L.gemm_plan_force.argtypes = [vp, i32, i32]
+        L.gemm_plan_force.argtypes = [vp, i32, i32, i32]
         L.gemm_plan_force.restype = i32
         L.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
                                       ctypes.POINTER(i64)]
@@ -147,8 +147,8 @@ def gemm_plan_set_group(plan: int, group: int) -> int:
     return int(lib().gemm_plan_set_group(plan, group))
 
 
-def gemm_plan_force(plan: int, kernel: int = 0, split_k: int = 0) -> int:
-    return int(lib().gemm_plan_force(plan, kernel, split_k))
+def gemm_plan_force(plan: int, kernel: int = 0, split_k: int = 0, block_n: int = 0) -> int:
+    return int(lib().gemm_plan_force(plan, kernel, split_k, block_n))
 
 
 def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int) -> tuple[int, int]:
@@ -210,8 +210,8 @@ class Plan:
         if st != GEMM_OK:
             raise GemmError(st, "gemm_plan_set_group")
 
-    def force(self, kernel: int = 0, split_k: int = 0):
-        st = gemm_plan_force(self.handle, kernel, split_k)
+    def force(self, kernel: int = 0, split_k: int = 0, block_n: int = 0):
+        st = gemm_plan_force(self.handle, kernel, split_k, block_n)
         if st != GEMM_OK:
             raise GemmError(st, "gemm_plan_force")
 

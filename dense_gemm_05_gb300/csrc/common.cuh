@@ -97,6 +97,14 @@ cudaError_t skinny_prepare();
 cudaError_t launch_skinny(int ms, const CUtensorMap& mapB, const CUtensorMap& mapA,
                           const Params& p, uint32_t idesc, int grid, cudaStream_t stream);
 
+// CTA-pair (cta_group::2) kernel, 256 x bn pair tiles, operands by TMA. bn in {128, 256}.
+int pair_smem_bytes(int bn);
+int pair_stages(int bn);
+cudaError_t pair_prepare();
+int pair_max_clusters(int bn);   // co-resident 2-CTA clusters on the current device (0 = unknown)
+cudaError_t launch_pair(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
+                        uint32_t idesc, int grid, cudaStream_t stream);
+
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);
 

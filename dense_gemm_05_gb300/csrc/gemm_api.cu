@@ -25,6 +25,8 @@ struct gemm_plan_s {
     int group = 8;
     int force_kernel = 0;
     int force_split = 0;
+    int force_bn = 0;
+    int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
     bool debug_sync = false;
     uint64_t timeout_ns = 2000000000ull;
 };
@@ -188,11 +190,13 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         else
             kernel = GEMM_KERNEL_GENERIC;
     }
-    if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY) && !tma)
+    if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY ||
+         kernel == GEMM_KERNEL_PAIR) && !tma)
         return GEMM_ERR_UNSUPPORTED;
     if (kernel == GEMM_KERNEL_SKINNY && a.M > 64) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_PAIR && plan->pair_clusters[0] <= 0) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_SKINNY &&
-        kernel != GEMM_KERNEL_GENERIC)
+        kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR)
         return GEMM_ERR_UNSUPPORTED;
     c->kernel = kernel;
     c->num_kb = static_cast<int>(cdiv(a.K, dg::kBK));
@@ -215,11 +219,26 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         c->kbps = static_cast<int>(cdiv(c->num_kb, c->split));
         c->units = c->tiles_n * c->split;
         c->stages = dg::skinny_stages(c->ms);
+    } else if (kernel == GEMM_KERNEL_PAIR) {
+        const int64_t tm = cdiv(a.M, 2 * dg::kBM);
+        const int64_t t256 = tm * cdiv(a.N, 256);
+        c->bn = plan->force_bn ? plan->force_bn
+                               : ((t256 >= 2 * int64_t(plan->pair_clusters[1])) ? 256 : 128);
+        c->stages = dg::pair_stages(c->bn);
+        c->tiles_m = static_cast<int>(tm);
+        c->tiles_n = static_cast<int>(cdiv(a.N, c->bn));
+        const int64_t units = int64_t(c->tiles_m) * c->tiles_n;
+        if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
+        c->units = static_cast<int>(units);
+        const int clusters = plan->pair_clusters[c->bn == 256 ? 1 : 0];
+        c->grid = 2 * (c->units < clusters ? c->units : clusters);
+        return GEMM_OK;
     } else {
         const int64_t tm = cdiv(a.M, dg::kBM);
         if (kernel == GEMM_KERNEL_TMA) {
             const int64_t t256 = tm * cdiv(a.N, 256);
-            c->bn = (t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128;
+            c->bn = plan->force_bn ? plan->force_bn
+                                   : ((t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128);
             c->stages = dg::tma_stages(c->bn);
         } else {
             c->bn = 128;
@@ -318,7 +337,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
     if (encode_fn() == nullptr) return GEMM_ERR_CUDA;
     if (dg::tma_prepare() != cudaSuccess || dg::generic_prepare() != cudaSuccess ||
-        dg::skinny_prepare() != cudaSuccess) {
+        dg::skinny_prepare() != cudaSuccess || dg::pair_prepare() != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -326,6 +345,10 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     if (p == nullptr) return GEMM_ERR_OOM;
     p->device = device;
     p->num_sms = sms;
+    // Pair tiles need both SMs of a cluster resident at once; size their
+    // persistent grids by what the device can co-schedule.
+    p->pair_clusters[0] = dg::pair_max_clusters(128);
+    p->pair_clusters[1] = dg::pair_max_clusters(256);
     p->debug_sync = env_flag("GEMM_DEBUG_SYNC");
     if (const char* t = std::getenv("GEMM_WAIT_TIMEOUT_MS")) {
         const long long ms = std::atoll(t);
@@ -372,13 +395,16 @@ gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group) {
     return GEMM_OK;
 }
 
-gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k) {
+gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
+                              int32_t block_n) {
     if (plan == nullptr || split_k < 0) return GEMM_ERR_INVALID_ARG;
+    if (block_n != 0 && block_n != 128 && block_n != 256) return GEMM_ERR_INVALID_ARG;
     if (kernel != 0 && kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_GENERIC &&
         kernel != GEMM_KERNEL_SKINNY && kernel != GEMM_KERNEL_PAIR)
         return GEMM_ERR_INVALID_ARG;
     plan->force_kernel = kernel;
     plan->force_split = split_k;
+    plan->force_bn = block_n;
     return GEMM_OK;
 }
 
@@ -403,14 +429,20 @@ gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const voi
     if (st != GEMM_OK) return st;
     gemm_config_t cfg{};
     cfg.kernel = c.kernel;
-    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY) ? c.ms : dg::kBM;
+    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY) ? c.ms
+                  : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM : dg::kBM);
     cfg.block_n = (c.kernel == GEMM_KERNEL_SKINNY) ? 128 : c.bn;
     cfg.block_k = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : dg::kBK;
     cfg.stages = c.stages;
     cfg.split_k = c.split;
     cfg.grid = c.grid;
-    cfg.cluster = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : 1;
-    cfg.group = (c.kernel == GEMM_KERNEL_TMA || c.kernel == GEMM_KERNEL_GENERIC) ? plan->group : 0;
+    cfg.cluster = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL)
+                      ? 0
+                      : (c.kernel == GEMM_KERNEL_PAIR ? 2 : 1);
+    cfg.group = (c.kernel == GEMM_KERNEL_TMA || c.kernel == GEMM_KERNEL_GENERIC ||
+                 c.kernel == GEMM_KERNEL_PAIR)
+                    ? plan->group
+                    : 0;
     cfg.tiles = c.units;
     *out = cfg;
     return GEMM_OK;
@@ -468,6 +500,15 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
                 return GEMM_ERR_CUDA;
             err = dg::launch_tma(c.bn, ma, mb, p, dg::idesc_f16(bf16, false, true, dg::kBM, c.bn),
                                  c.grid, stream);
+        } else if (c.kernel == GEMM_KERNEL_PAIR) {
+            // Each CTA of a pair loads 128 rows of A and 64-column sub-tiles of its half of B.
+            CUtensorMap ma, mb;
+            if (!encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
+                !encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+                return GEMM_ERR_CUDA;
+            err = dg::launch_pair(c.bn, ma, mb, p,
+                                  dg::idesc_f16(bf16, false, true, 2 * dg::kBM, c.bn), c.grid,
+                                  stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {
             err = dg::launch_generic(p, dg::idesc_f16(bf16, false, true, dg::kBM, 128), c.grid,
                                      stream);

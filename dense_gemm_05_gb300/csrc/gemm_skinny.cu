@@ -13,6 +13,11 @@
 // on every run, whatever order the units finish in.  It then resets the
 // counter to zero for the next launch.
 //
+// Work units are numbered slice-major (u = split * tiles_n + n_tile), so the
+// CTAs running at the same time stream the same K rows of B across all of its
+// columns: whole rows of B are read together instead of 256-byte strips
+// scattered over DRAM pages.
+//
 // Warp roles are those of gemm_tc.cu: warp 0 MMA issuer + TMEM owner, warps
 // 1..4 epilogue, warp 5 TMA producer.
 #include "common.cuh"
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-                const int split = u % S;
+                const int split = u / p.tiles_n;
                 const int kb0 = split * kbps;
                 const int kb1 = min(num_kb, kb0 + kbps);
                 if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -173,8 +178,8 @@ __global__ void __launch_bounds__(192, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int n_tile = u / S;
-            const int split = u - n_tile * S;
+            const int split = u / p.tiles_n;
+            const int n_tile = u - split * p.tiles_n;
             const bool ok =
                 mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
             // One decision for all 128 epilogue threads: they share named barriers below.
@@ -244,8 +249,8 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t pol_stream = l2_policy_evict_first();   // B: read once
             const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every tile
             for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-                const int n_tile = u / S;
-                const int split = u - n_tile * S;
+                const int split = u / p.tiles_n;
+                const int n_tile = u - split * p.tiles_n;
                 const int kb0 = split * kbps;
                 const int kb1 = min(num_kb, kb0 + kbps);
                 for (int kb = kb0; kb < kb1; ++kb) {

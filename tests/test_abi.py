@@ -48,7 +48,7 @@ def test_null_plan_is_rejected_before_any_cuda_call():
     assert g.gemm_run(None, 0, 1, 0, 1, 0, 1, 1, 1, 1, g.GEMM_F16, 0) == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_plan_destroy(None) == g.GEMM_OK
     assert g.gemm_plan_set_group(None, 8) == g.GEMM_ERR_INVALID_ARG
-    assert g.gemm_plan_force(None, 0, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan_force(None, 0, 0, 0) == g.GEMM_ERR_INVALID_ARG
     assert g.lib().gemm_plan_create(None, 0) == g.GEMM_ERR_INVALID_ARG
 
 

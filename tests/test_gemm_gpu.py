@@ -29,13 +29,14 @@ def plan():
     p.close()
 
 
-def run(plan, A, B, M, N, K, *, ldc=None, kernel=0, split=0, group=None, expect=None):
+def run(plan, A, B, M, N, K, *, ldc=None, kernel=0, split=0, block_n=0, group=None,
+        expect=None):
     """Copy A, B (CPU, possibly padded) to the GPU, run the C ABI, return the C buffer."""
     ldc = N if ldc is None else ldc
     dev = torch.device("cuda:0")
     a, b = A.to(dev), B.to(dev)
     cbuf = torch.full((M + 2, max(ldc, 1)), SENTINEL, dtype=torch.float32, device=dev)
-    plan.force(kernel, split)
+    plan.force(kernel, split, block_n)
     if group is not None:
         plan.set_group(group)
     try:
@@ -45,7 +46,7 @@ def run(plan, A, B, M, N, K, *, ldc=None, kernel=0, split=0, group=None, expect=
         plan.run(a, b, cbuf, M, N, K)
         torch.cuda.synchronize()
     finally:
-        plan.force(0, 0)
+        plan.force(0, 0, 0)
         if group is not None:
             plan.set_group(8)
     return cbuf.cpu().double().numpy()
@@ -157,6 +158,50 @@ def test_workload_square_sampled(plan, name):
     assert ok.all(), f"{name}: {int((~ok).sum())} of {ok.size} sampled entries outside tolerance"
 
 
+@pytest.mark.parametrize("name,block_n", [("square4096_bf16", 128), ("square4096_bf16", 256),
+                                          ("square8192_bf16", 256)])
+def test_workload_square_sampled_pair(plan, name, block_n):
+    """The 2-SM pair-tile kernel on the square workloads."""
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    dev = torch.device("cuda:0")
+    a, b = A.to(dev), B.to(dev)
+    c = torch.full((w.M, w.N), float("nan"), dtype=torch.float32, device=dev)
+    plan.force(g.GEMM_KERNEL_PAIR, 0, block_n)
+    try:
+        cfg = plan.query(a, b, c)
+        assert cfg["kernel"] == g.GEMM_KERNEL_PAIR and cfg["cluster"] == 2, cfg
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+    finally:
+        plan.force(0, 0, 0)
+    assert not torch.isnan(c).any().item(), "some C entries were never written"
+    rows, cols = _sample_entries(w.M, w.N, cfg["block_m"], cfg["block_n"], 4096, w.seed)
+    got = c[torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)].cpu().double().numpy()
+    ref, bnd = oracle.gemm_entries(A, B, rows, cols)
+    ok = np.abs(got - ref) <= REL * bnd + ABS
+    assert ok.all(), f"{name} pair: {int((~ok).sum())} of {ok.size} sampled entries outside tolerance"
+
+
+@pytest.mark.parametrize("M,N,K,block_n", [(257, 130, 70, 128), (1, 64, 64, 128),
+                                           (129, 520, 1000, 256), (1023, 1029, 1000, 256)])
+def test_pair_ragged_padded(plan, M, N, K, block_n):
+    lda, ldb = -(-K // 8) * 8, -(-N // 8) * 8
+    A, B = workloads.custom(M, K, N, "f16", seed=M + N, lda=lda, ldb=ldb)
+    got = run(plan, A, B, M, N, K, ldc=N + 5, kernel=g.GEMM_KERNEL_PAIR, block_n=block_n,
+              expect=g.GEMM_KERNEL_PAIR)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"pair {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("group", [0, 3, 8])
+def test_pair_tile_order_does_not_change_bits(plan, group):
+    A, B = workloads.custom(1000, 512, 1300, "bf16", seed=22, dist="normal")
+    base = run(plan, A, B, 1000, 1300, 512, kernel=g.GEMM_KERNEL_PAIR, group=8)
+    got = run(plan, A, B, 1000, 1300, 512, kernel=g.GEMM_KERNEL_PAIR, group=group)
+    assert np.array_equal(base, got)
+
+
 # ---------------------------------------------------------------- exactness
 
 def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
@@ -183,11 +228,18 @@ def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
     (g.GEMM_KERNEL_SKINNY, 4, (16, 4096, 1024), "bf16"),
     (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
     (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
+    (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1100), "bf16"),
+    (g.GEMM_KERNEL_PAIR, 256, (600, 1024, 1100), "f16"),
+    (g.GEMM_KERNEL_PAIR, 256, (1024, 4096, 1024), "bf16"),
 ])
 def test_small_integer_inputs_are_bit_exact(plan, kernel, split, shape, dtype):
+    """For the pair kernel the second parameter is the pair tile width (block_n)."""
     M, K, N = shape
     A, B = int_inputs(M, K, N, dtype, seed=M + K + N)
-    got = run(plan, A, B, M, N, K, kernel=kernel, split=split, expect=kernel)
+    if kernel == g.GEMM_KERNEL_PAIR:
+        got = run(plan, A, B, M, N, K, kernel=kernel, block_n=split, expect=kernel)
+    else:
+        got = run(plan, A, B, M, N, K, kernel=kernel, split=split, expect=kernel)
     assert_guards(got, M, N)
     ref = oracle.gemm(A, B)
     assert np.array_equal(got[:M, :N], ref), f"max diff {np.abs(got[:M, :N] - ref).max()}"
@@ -200,7 +252,7 @@ def test_mn_major_layout_pin(plan):
     N = 320
     A = torch.eye(M, K, dtype=torch.bfloat16)
     B = (torch.arange(K * N, dtype=torch.float32).reshape(K, N) % 251).to(torch.bfloat16)
-    for kernel in (g.GEMM_KERNEL_TMA, g.GEMM_KERNEL_GENERIC):
+    for kernel in (g.GEMM_KERNEL_TMA, g.GEMM_KERNEL_GENERIC, g.GEMM_KERNEL_PAIR):
         got = run(plan, A, B, M, N, K, kernel=kernel)
         assert np.array_equal(got[:M, :N], B.double().numpy()), kernel
     # skinny: first 16 rows of the identity
