@@ -25,8 +25,8 @@ struct Params {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_kb;
     int32_t group;          // group-major strip height (0 = row-major)
-    int32_t split_k;        // skinny: K slices per output tile
-    int32_t kb_per_split;   // skinny: K blocks per slice
+    int32_t shares;         // skinny: equal shares of the (tile, K block) iterations
+    int32_t max_slots;      // skinny: partial-tile slots per output tile in the workspace
     int32_t a_vec, b_vec;   // generic producer: 16-byte vector loads are legal
     int32_t c_vec;          // 16-byte vector stores of C are legal
     float* ws;              // skinny: split-K partial sums
@@ -72,6 +72,24 @@ __device__ __forceinline__ void tile_coord32(int t, int tiles_m, int tiles_n, in
     const int local = t - strip * per_strip;
     tm = first + local % height;
     tn = local / height;
+}
+
+// Stream-K shares of the skinny kernel.  The T = tiles * num_kb (tile, K block)
+// iterations, tile-major, are cut into G contiguous shares; share c covers
+// [c*T/G, (c+1)*T/G).  G <= 4096 and T < 2^49 keep the products in int64.
+__host__ __device__ __forceinline__ int64_t share_begin(int64_t c, int64_t T, int64_t G) {
+    return c * T / G;
+}
+
+// The share that contains iteration i (the largest c with share_begin(c) <= i).
+__host__ __device__ __forceinline__ int64_t share_of(int64_t i, int64_t T, int64_t G) {
+    return ((i + 1) * G - 1) / T;
+}
+
+// Upper bound on how many shares can touch one tile's num_kb iterations.
+__host__ __device__ __forceinline__ int shares_per_tile_bound(int64_t T, int64_t G, int num_kb) {
+    const int64_t shortest = T / G;   // every share has at least this many iterations
+    return static_cast<int>((num_kb + shortest - 1) / shortest) + 1;
 }
 
 // ---------------------------------------------------------------- launchers

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include <cuda.h>
@@ -98,8 +99,9 @@ struct Choice {
     int kernel = GEMM_KERNEL_NONE;
     int bn = 0;          // TMA/GENERIC: tile columns
     int ms = 0;          // SKINNY: padded M (MMA N)
-    int split = 1;
-    int kbps = 0;
+    int split = 1;       // SKINNY: most stream-K shares that touch one tile
+    int shares = 0;      // SKINNY: stream-K shares
+    int max_slots = 0;   // SKINNY: workspace slots per tile
     int tiles_m = 0, tiles_n = 0, num_kb = 0;
     int units = 0;
     int grid = 0;
@@ -147,27 +149,36 @@ gemm_status_t check_args(const Args& a) {
     return GEMM_OK;
 }
 
-// Skinny split: the number of K slices S that minimises the longest CTA's
-// K-block count, ceil(units / SMs) * ceil(num_kb / S), within the workspace.
-void choose_split(const gemm_plan_s* plan, Choice* c) {
-    const int64_t per_split_bytes = int64_t(c->tiles_n) * c->ms * 128 * 4;
-    int best = 1;
-    int64_t best_cost = INT64_MAX;
-    const int max_s = c->num_kb < 64 ? c->num_kb : 64;
-    for (int s = 1; s <= max_s; ++s) {
-        const int kbps = static_cast<int>(cdiv(c->num_kb, s));
-        if (cdiv(c->num_kb, kbps) != s) continue;                 // every slice non-empty
-        if (s > 1 && (c->tiles_n > plan->counters_len ||
-                      per_split_bytes * s > static_cast<int64_t>(plan->ws_bytes)))
-            break;
-        const int64_t waves = cdiv(int64_t(c->tiles_n) * s, plan->num_sms);
-        const int64_t cost = waves * (kbps + 1);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = s;
-        }
+constexpr int kMinShareKb = 4;     // a stream-K share streams at least this many K blocks
+constexpr int64_t kMaxShares = 4096;
+
+// Skinny stream-K shares.  `shares` <= 0: one share per SM (each at least
+// kMinShareKb K blocks); otherwise that many shares.  Falls back to one share
+// per tile (no partial tiles) when the workspace or counters cannot hold the
+// partials.  Returns false if even that is impossible.
+bool choose_shares(const gemm_plan_s* plan, Choice* c, int64_t shares) {
+    const int64_t T = int64_t(c->tiles_n) * c->num_kb;
+    int64_t G = shares > 0 ? shares : std::min<int64_t>(plan->num_sms, T / kMinShareKb);
+    G = std::max<int64_t>(1, std::min<int64_t>({G, T, kMaxShares}));
+    const int slots = dg::shares_per_tile_bound(T, G, c->num_kb);
+    const int64_t need = int64_t(c->tiles_n) * slots * c->ms * 128 * 4;
+    const bool aligned = (G % c->tiles_n == 0) && (G / c->tiles_n == 1);   // one share per tile
+    if (!aligned &&
+        (c->tiles_n > plan->counters_len || need > static_cast<int64_t>(plan->ws_bytes))) {
+        if (shares > 0 || c->tiles_n > kMaxShares) return false;
+        G = c->tiles_n;
     }
-    c->split = best;
+    c->shares = static_cast<int>(G);
+    c->max_slots = dg::shares_per_tile_bound(T, G, c->num_kb);
+    // Most shares touching one tile (the "K split" a tile sees), for reporting.
+    int most = 1;
+    for (int64_t t = 0; t < c->tiles_n && t < 65536; ++t) {
+        const int64_t first = dg::share_of(t * c->num_kb, T, G);
+        const int64_t last = dg::share_of((t + 1) * c->num_kb - 1, T, G);
+        most = std::max<int>(most, static_cast<int>(last - first + 1));
+    }
+    c->split = most;
+    return true;
 }
 
 gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
@@ -183,8 +194,13 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
     const bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
     int kernel = plan->force_kernel;
     if (kernel == 0) {
+        // Pair tiles (256 x 256 per two SMs) once there is at least a full wave of them;
+        // they stage half as much B per flop as one-CTA tiles.
+        const int64_t pair_tiles = cdiv(a.M, 2 * dg::kBM) * cdiv(a.N, 256);
         if (tma && a.M <= 64)
             kernel = GEMM_KERNEL_SKINNY;
+        else if (tma && plan->pair_clusters[1] > 0 && pair_tiles >= plan->pair_clusters[1])
+            kernel = GEMM_KERNEL_PAIR;
         else if (tma)
             kernel = GEMM_KERNEL_TMA;
         else
@@ -204,26 +220,16 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : 64);
         c->tiles_m = 1;
         c->tiles_n = static_cast<int>(cdiv(a.N, 128));
-        if (plan->force_split > 0) {
-            int s = plan->force_split < c->num_kb ? plan->force_split : c->num_kb;
-            const int kbps = static_cast<int>(cdiv(c->num_kb, s));
-            s = static_cast<int>(cdiv(c->num_kb, kbps));
-            const int64_t need = int64_t(c->tiles_n) * c->ms * 128 * 4 * s;
-            if (s > 1 && (c->tiles_n > plan->counters_len ||
-                          need > static_cast<int64_t>(plan->ws_bytes)))
-                return GEMM_ERR_UNSUPPORTED;
-            c->split = s;
-        } else {
-            choose_split(plan, c);
-        }
-        c->kbps = static_cast<int>(cdiv(c->num_kb, c->split));
-        c->units = c->tiles_n * c->split;
+        // A forced split S means S equal shares per tile (S * tiles shares in all).
+        const int64_t forced = plan->force_split > 0 ? int64_t(plan->force_split) * c->tiles_n : 0;
+        if (!choose_shares(plan, c, forced)) return GEMM_ERR_UNSUPPORTED;
+        c->units = c->shares;
         c->stages = dg::skinny_stages(c->ms);
     } else if (kernel == GEMM_KERNEL_PAIR) {
         const int64_t tm = cdiv(a.M, 2 * dg::kBM);
         const int64_t t256 = tm * cdiv(a.N, 256);
         c->bn = plan->force_bn ? plan->force_bn
-                               : ((t256 >= 2 * int64_t(plan->pair_clusters[1])) ? 256 : 128);
+                               : ((t256 >= int64_t(plan->pair_clusters[1])) ? 256 : 128);
         c->stages = dg::pair_stages(c->bn);
         c->tiles_m = static_cast<int>(tm);
         c->tiles_n = static_cast<int>(cdiv(a.N, c->bn));
@@ -444,6 +450,7 @@ gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const voi
                     ? plan->group
                     : 0;
     cfg.tiles = c.units;
+    cfg.shares = c.shares;
     *out = cfg;
     return GEMM_OK;
 }
@@ -483,8 +490,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
         p.tiles_n = c.tiles_n;
         p.num_kb = c.num_kb;
         p.group = plan->group;
-        p.split_k = c.split;
-        p.kb_per_split = c.kbps;
+        p.shares = c.shares;
+        p.max_slots = c.max_slots;
         p.a_vec = tma_ok(A, lda) ? 1 : 0;
         p.b_vec = tma_ok(B, ldb) ? 1 : 0;
         p.c_vec = ((reinterpret_cast<uintptr_t>(C) % 16u) == 0u && ldc % 4 == 0) ? 1 : 0;

@@ -168,27 +168,21 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     std::call_once(s->once, setup_device, s, dev);
     if (s->status != GEMM_OK) return s->status;
 
-    // Split K so the longest CTA streams the fewest K blocks, within the scratch.
+    // Stream-K shares: one per SM (each at least 4 K blocks); if their partial
+    // tiles would not fit the scratch, one share per tile (no partials).
     const int ms = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int tiles_n = static_cast<int>(cdiv(N, 128));
     const int num_kb = static_cast<int>(cdiv(K, dg::kBK));
-    const int64_t per_split = int64_t(tiles_n) * ms * 128 * 4;
-    int split = 1;
-    int64_t best = INT64_MAX;
-    for (int sp = 1; sp <= (num_kb < 64 ? num_kb : 64); ++sp) {
-        const int kbps = static_cast<int>(cdiv(num_kb, sp));
-        if (cdiv(num_kb, kbps) != sp) continue;
-        if (sp > 1 && per_split * sp > kScratchWsBytes) break;
-        const int64_t cost = cdiv(int64_t(tiles_n) * sp, s->num_sms) * (kbps + 1);
-        if (cost < best) {
-            best = cost;
-            split = sp;
-        }
-    }
-    const int kbps = static_cast<int>(cdiv(num_kb, split));
+    const int64_t T = int64_t(tiles_n) * num_kb;
+    int64_t shares = T / 4 < s->num_sms ? T / 4 : s->num_sms;
+    if (shares < 1) shares = 1;
+    if (int64_t(tiles_n) * dg::shares_per_tile_bound(T, shares, num_kb) * ms * 128 * 4 >
+        kScratchWsBytes)
+        shares = tiles_n;
+    const int max_slots = dg::shares_per_tile_bound(T, shares, num_kb);
     int* counters = reinterpret_cast<int*>(s->scratch + kScratchWsBytes);
     // The array keeps whatever the previous call left: the counters must start at zero.
-    if (split > 1 && cudaMemsetAsync(counters, 0, sizeof(int) * tiles_n, stream) != cudaSuccess) {
+    if (cudaMemsetAsync(counters, 0, sizeof(int) * tiles_n, stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -211,8 +205,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.tiles_n = tiles_n;
     p.num_kb = num_kb;
     p.group = 0;
-    p.split_k = split;
-    p.kb_per_split = kbps;
+    p.shares = static_cast<int32_t>(shares);
+    p.max_slots = max_slots;
     p.a_vec = 1;
     p.b_vec = 1;
     p.c_vec = 0;
@@ -220,8 +214,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.counters = counters;
     p.status = nullptr;
     p.timeout_ns = 2000000000ull;
-    const int units = tiles_n * split;
-    const int grid = units < s->num_sms ? units : s->num_sms;
+    const int grid = shares < s->num_sms ? static_cast<int>(shares) : s->num_sms;
     const bool bf16 = dtype == GEMM_BF16;
     if (dg::launch_skinny(ms, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, ms), grid,
                           stream) != cudaSuccess) {

@@ -1,25 +1,25 @@
-// gemm_skinny.cu -- small-M GEMM for sm_103a: swap-AB + split-K.
+// gemm_skinny.cu -- small-M GEMM for sm_103a: swap-AB + stream-K split of K.
 //
 // For M <= 64 the product is computed transposed, C^T[N, M] = B^T[N, K] A^T[K, M],
 // so N fills the 128 rows of the tcgen05 MMA and the padded M (16, 32 or 64)
 // is the MMA's N.  B, the large operand, is read once from HBM: the problem is
-// bound by that stream, not by the tensor cores.  To put every SM on the
-// stream, each 128-column tile of C is split into S slices along K (the
-// K-sum of "Writing GPU kernels in Triton", section 3.3, regrouped; the
-// regrouping is exact up to rounding because the sum is associative).
-// Each (tile, slice) unit writes its fp32 partial tile to the plan's
-// workspace; the last unit of a tile to arrive (a per-tile counter) adds the S
-// partials in slice order 0..S-1 and writes C, so the result is the same bits
-// on every run, whatever order the units finish in.  It then resets the
-// counter to zero for the next launch.
+// bound by that stream, not by the tensor cores.
 //
-// Work units are numbered slice-major (u = split * tiles_n + n_tile), so the
-// CTAs running at the same time stream the same K rows of B across all of its
-// columns: whole rows of B are read together instead of 256-byte strips
-// scattered over DRAM pages.
+// To put every SM on the stream, the (tile, K block) iterations of all
+// 128-column tiles, taken tile by tile, are cut into G equal contiguous shares
+// (one per CTA): each CTA streams the same number of K blocks of B, and a tile
+// is computed by at most a few consecutive CTAs, each summing its own run of
+// K blocks (the K-sum of "Writing GPU kernels in Triton", section 3.3,
+// regrouped; the regrouping is exact up to rounding because the sum is
+// associative).  A CTA that covers a whole tile stores C directly.  Otherwise
+// it writes its fp32 partial tile to slot (share - first share of the tile) of
+// the plan's workspace; the last of the tile's shares to arrive (a per-tile
+// counter) adds the partials in slot order 0, 1, ... and writes C, so the
+// result is the same bits on every run whatever order the shares finish in.
+// It then resets the counter to zero for the next launch.
 //
 // Warp roles are those of gemm_tc.cu: warp 0 MMA issuer + TMEM owner, warps
-// 1..4 epilogue, warp 5 TMA producer.
+// 1..4 epilogue, warp 5 TMA producer.  All three walk the same segments.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -36,6 +36,40 @@ struct SkCfg {
     static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 8 * kNumBars + 16;
     static_assert(MS == 16 || MS == 32 || MS == 64, "MS");
     static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+// One contiguous run of K blocks [kb0, kb1) of one tile, inside one share.
+struct Segment {
+    int tile;
+    int kb0, kb1;
+};
+
+// Walks the segments of the shares this CTA owns (share c = blockIdx.x, then
+// += gridDim.x), in the same order in every role.
+struct SegmentWalker {
+    int64_t T, G;
+    int num_kb;
+    int64_t share, it, end;
+
+    __device__ SegmentWalker(int tiles, int nkb, int shares)
+        : T(int64_t(tiles) * nkb), G(shares), num_kb(nkb), share(blockIdx.x) {
+        it = share < G ? share_begin(share, T, G) : 0;
+        end = share < G ? share_begin(share + 1, T, G) : 0;
+    }
+    __device__ bool next(Segment& s) {
+        while (it >= end) {
+            share += gridDim.x;
+            if (share >= G) return false;
+            it = share_begin(share, T, G);
+            end = share_begin(share + 1, T, G);
+        }
+        s.tile = static_cast<int>(it / num_kb);
+        s.kb0 = static_cast<int>(it - int64_t(s.tile) * num_kb);
+        const int64_t left = end - it;
+        s.kb1 = (num_kb - s.kb0 < left) ? num_kb : s.kb0 + static_cast<int>(left);
+        it += s.kb1 - s.kb0;
+        return true;
+    }
 };
 
 template <int MS>
@@ -108,11 +142,7 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
-    const int S = p.split_k;
-    const int units = p.tiles_n * S;
     const int num_kb = p.num_kb;
-    const int kbps = p.kb_per_split;
 
     if (warp == 0) {
         // ------------------------------------------------------------ MMA issuer
@@ -122,17 +152,16 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-                const int split = u / p.tiles_n;
-                const int kb0 = split * kbps;
-                const int kb1 = min(num_kb, kb0 + kbps);
+            SegmentWalker walk(p.tiles_n, num_kb, p.shares);
+            Segment sg;
+            while (!failed && walk.next(sg)) {
                 if (!mbar_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, p.timeout_ns)) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MS);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.timeout_ns)) {
                         failed = true;
                         break;
@@ -146,7 +175,7 @@ __global__ void __launch_bounds__(192, 1)
                     for (int k = 0; k < kBK / 16; ++k) {
                         tc_mma_f16(d_tmem, a0 + static_cast<uint64_t>((k * 16 * 128) >> 4),
                                    b0 + static_cast<uint64_t>((k * 32) >> 4), idesc,
-                                   (kb != kb0 || k != 0) ? 1u : 0u);
+                                   (kb != sg.kb0 || k != 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
@@ -175,11 +204,12 @@ __global__ void __launch_bounds__(192, 1)
         const int q = warp & 3;
         const int r = q * 32 + lane;            // row of the transposed tile = column of C
         const int et = threadIdx.x - 32;        // 0..127
+        const int64_t T = int64_t(p.tiles_n) * num_kb;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const int split = u / p.tiles_n;
-            const int n_tile = u - split * p.tiles_n;
+        SegmentWalker walk(p.tiles_n, num_kb, p.shares);
+        Segment sg;
+        while (walk.next(sg)) {
             const bool ok =
                 mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
             // One decision for all 128 epilogue threads: they share named barriers below.
@@ -200,8 +230,9 @@ __global__ void __launch_bounds__(192, 1)
                 acc_phase ^= 1u;
             }
 
-            const int n = n_tile * 128 + r;
-            if (S == 1) {
+            const int n = sg.tile * 128 + r;
+            if (sg.kb0 == 0 && sg.kb1 == num_kb) {
+                // This share covers the whole tile: store C directly.
                 if (n < p.N) {
 #pragma unroll
                     for (int m = 0; m < MS; ++m)
@@ -209,34 +240,46 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 continue;
             }
-            // Split-K: publish this slice's partial tile, then let the last arriver reduce.
-            float* wsp = p.ws + (static_cast<int64_t>(split) * p.tiles_n + n_tile) * (MS * 128) + r;
+            // Partial tile: publish it in this share's slot, then let the last arriver reduce.
+            const int64_t first = share_of(int64_t(sg.tile) * num_kb, T, p.shares);
+            const int64_t last = share_of(int64_t(sg.tile + 1) * num_kb - 1, T, p.shares);
+            const int nslots = static_cast<int>(last - first + 1);
+            const int slot = static_cast<int>(walk.share - first);
+            float* tile_ws = p.ws + static_cast<int64_t>(sg.tile) * p.max_slots * (MS * 128);
+            float* mine = tile_ws + static_cast<int64_t>(slot) * (MS * 128) + r;
 #pragma unroll
-            for (int m = 0; m < MS; ++m) __stcg(wsp + m * 128, v[m]);
+            for (int m = 0; m < MS; ++m) __stcg(mine + m * 128, v[m]);
             __threadfence();
             named_bar_sync(1, 128);
             if (et == 0) {
-                const int old = atomicAdd(&p.counters[n_tile], 1);
-                *last_flag = (old == S - 1) ? 1 : 0;
+                const int old = atomicAdd(&p.counters[sg.tile], 1);
+                *last_flag = (old == nslots - 1) ? 1 : 0;
             }
             named_bar_sync(1, 128);
             if (*last_flag) {
                 __threadfence();
-                if (n < p.N) {
+                float s[MS];
 #pragma unroll
-                    for (int m = 0; m < MS; ++m) {
-                        if (m < p.M) {
-                            float s = 0.0f;
-                            for (int sp = 0; sp < S; ++sp)
-                                s += __ldcg(p.ws +
-                                            (static_cast<int64_t>(sp) * p.tiles_n + n_tile) *
-                                                (MS * 128) +
-                                            m * 128 + r);
-                            p.C[static_cast<int64_t>(m) * p.ldc + n] = s;
-                        }
+                for (int m = 0; m < MS; ++m) s[m] = 0.0f;
+                for (int j = 0; j < nslots; ++j) {
+                    if (j == slot) {
+#pragma unroll
+                        for (int m = 0; m < MS; ++m) s[m] += v[m];   // the value stored above
+                    } else {
+                        const float* src = tile_ws + static_cast<int64_t>(j) * (MS * 128) + r;
+                        float t[MS];
+#pragma unroll
+                        for (int m = 0; m < MS; ++m) t[m] = __ldcg(src + m * 128);
+#pragma unroll
+                        for (int m = 0; m < MS; ++m) s[m] += t[m];
                     }
                 }
-                if (et == 0) p.counters[n_tile] = 0;
+                if (n < p.N) {
+#pragma unroll
+                    for (int m = 0; m < MS; ++m)
+                        if (m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = s[m];
+                }
+                if (et == 0) p.counters[sg.tile] = 0;
             }
         }
     } else {
@@ -248,12 +291,10 @@ __global__ void __launch_bounds__(192, 1)
             int64_t armed = 0;
             const uint64_t pol_stream = l2_policy_evict_first();   // B: read once
             const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every tile
-            for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
-                const int split = u / p.tiles_n;
-                const int n_tile = u - split * p.tiles_n;
-                const int kb0 = split * kbps;
-                const int kb1 = min(num_kb, kb0 + kbps);
-                for (int kb = kb0; kb < kb1; ++kb) {
+            SegmentWalker walk(p.tiles_n, num_kb, p.shares);
+            Segment sg;
+            while (!failed && walk.next(sg)) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
                                    p.timeout_ns)) {
                         failed = true;
@@ -265,7 +306,7 @@ __global__ void __launch_bounds__(192, 1)
                     for (int j = 0; j < 2; ++j)
                         tma_load_2d_hint(
                             smem_u32(sBt + stage * Cfg::kBtStageBytes + j * kSubTileBytes), &mapB,
-                            fb, n_tile * 128 + j * kSubN, kb * kBK, pol_stream);
+                            fb, sg.tile * 128 + j * kSubN, kb * kBK, pol_stream);
                     tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb,
                                      kb * kBK, 0, pol_keep);
                     ++armed;

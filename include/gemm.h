@@ -80,11 +80,12 @@ typedef struct {
     int32_t block_n;      /* columns of C per tile */
     int32_t block_k;      /* K depth of one pipeline stage */
     int32_t stages;       /* shared-memory ring depth */
-    int32_t split_k;      /* K slices per output tile (1 = none) */
+    int32_t split_k;      /* most K slices any output tile is split into (1 = none) */
     int32_t grid;         /* CTAs launched (persistent kernels: one per SM or fewer) */
     int32_t cluster;      /* CTAs per cluster */
     int32_t group;        /* group-major strip height in tiles (0 = row-major order) */
-    int32_t tiles;        /* output tiles (work units for split-K) */
+    int32_t tiles;        /* work units: output tiles, or stream-K shares for SKINNY */
+    int32_t shares;       /* SKINNY: equal contiguous shares of the (tile, K block) iterations */
 } gemm_config_t;
 
 /*

@@ -121,6 +121,20 @@ def test_workload_skinny_full_and_deterministic(plan):
     assert_close(got1[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
 
 
+@pytest.mark.parametrize("M,K,N,dtype", [
+    (8, 1024, 65600, "bf16"),     # 513 tiles: shares span several tiles
+    (33, 2048, 640, "f16"),       # 5 tiles, MMA N = 64, tiles split across many shares
+    (1, 8192, 136, "bf16"),       # 2 tiles, 128 K blocks, ragged last tile
+])
+def test_skinny_stream_k_shapes(plan, M, K, N, dtype):
+    A, B = workloads.custom(M, K, N, dtype, seed=M + K + N, dist="normal")
+    got1 = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_SKINNY)
+    got2 = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_SKINNY)
+    assert_guards(got1, M, N)
+    assert np.array_equal(got1, got2), "stream-K result changed between runs"
+    assert_close(got1[:M, :N], A, B, M, N, K, f"skinny {M}x{N}x{K}")
+
+
 def _sample_entries(M, N, bm, bn, n_random, seed):
     """n_random uniform entries plus, for every tile on the border of C, its four
     corners and 16 random entries."""
@@ -139,17 +153,24 @@ def _sample_entries(M, N, bm, bn, n_random, seed):
     return np.array(rows, dtype=np.int64), np.array(cols, dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["square4096_bf16", "square8192_bf16"])
-def test_workload_square_sampled(plan, name):
+@pytest.mark.parametrize("name,kernel", [("square4096_bf16", 0), ("square8192_bf16", 0),
+                                         ("square4096_bf16", g.GEMM_KERNEL_TMA),
+                                         ("square8192_bf16", g.GEMM_KERNEL_TMA)])
+def test_workload_square_sampled(plan, name, kernel):
+    """The square workloads with the automatic choice (pair tiles) and the one-CTA kernel."""
     w = workloads.WORKLOADS[name]
     A, B = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
     a, b = A.to(dev), B.to(dev)
     c = torch.full((w.M, w.N), float("nan"), dtype=torch.float32, device=dev)
-    cfg = plan.query(a, b, c)
-    assert cfg["kernel"] == g.GEMM_KERNEL_TMA, cfg
-    plan.run(a, b, c)
-    torch.cuda.synchronize()
+    plan.force(kernel, 0, 0)
+    try:
+        cfg = plan.query(a, b, c)
+        assert cfg["kernel"] == (kernel or g.GEMM_KERNEL_PAIR), cfg
+        plan.run(a, b, c)
+        torch.cuda.synchronize()
+    finally:
+        plan.force(0, 0, 0)
     assert not torch.isnan(c).any().item(), "some C entries were never written"
     rows, cols = _sample_entries(w.M, w.N, cfg["block_m"], cfg["block_n"], 4096, w.seed)
     got = c[torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)].cpu().double().numpy()
@@ -228,8 +249,8 @@ def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
     (g.GEMM_KERNEL_SKINNY, 4, (16, 4096, 1024), "bf16"),
     (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
     (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
-    (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1100), "bf16"),
-    (g.GEMM_KERNEL_PAIR, 256, (600, 1024, 1100), "f16"),
+    (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1104), "bf16"),
+    (g.GEMM_KERNEL_PAIR, 256, (600, 1024, 1104), "f16"),
     (g.GEMM_KERNEL_PAIR, 256, (1024, 4096, 1024), "bf16"),
 ])
 def test_small_integer_inputs_are_bit_exact(plan, kernel, split, shape, dtype):
@@ -360,7 +381,7 @@ def test_kernel_selection(plan):
         b = torch.empty(K, ldb or N, dtype=torch.bfloat16, device=dev)
         c = torch.empty(M, N, dtype=torch.float32, device=dev)
         return plan.query(a, b, c, M, N, K)
-    assert q(8192, 8192, 8192)["kernel"] == g.GEMM_KERNEL_TMA
+    assert q(8192, 8192, 8192)["kernel"] == g.GEMM_KERNEL_PAIR
     assert q(8192, 8192, 8192)["block_n"] == 256
     assert q(1023, 1000, 1029)["kernel"] == g.GEMM_KERNEL_GENERIC
     s = q(16, 4096, 14336)
