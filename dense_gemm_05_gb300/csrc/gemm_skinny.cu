@@ -249,29 +249,41 @@ __global__ void __launch_bounds__(192, 1)
             float* mine = tile_ws + static_cast<int64_t>(slot) * (MS * 128) + r;
 #pragma unroll
             for (int m = 0; m < MS; ++m) __stcg(mine + m * 128, v[m]);
-            __threadfence();
+            // The barrier orders every epilogue thread's partial stores before thread 0's
+            // release at GPU scope; its acquire half (and the second barrier) make the
+            // partials of the shares that arrived earlier visible to the whole CTA.
             named_bar_sync(1, 128);
             if (et == 0) {
-                const int old = atomicAdd(&p.counters[sg.tile], 1);
+                const int old = atomic_add_acq_rel_gpu(&p.counters[sg.tile], 1);
                 *last_flag = (old == nslots - 1) ? 1 : 0;
             }
             named_bar_sync(1, 128);
             if (*last_flag) {
-                __threadfence();
+                // Sum the slots in order 0, 1, ...; the loads of kBatch slots are issued
+                // together so the reduction pays one L2 round trip per batch.
+                constexpr int kBatch = MS <= 16 ? 4 : (MS == 32 ? 2 : 1);
                 float s[MS];
 #pragma unroll
                 for (int m = 0; m < MS; ++m) s[m] = 0.0f;
-                for (int j = 0; j < nslots; ++j) {
-                    if (j == slot) {
+                for (int j0 = 0; j0 < nslots; j0 += kBatch) {
+                    float t[kBatch][MS];
 #pragma unroll
-                        for (int m = 0; m < MS; ++m) s[m] += v[m];   // the value stored above
-                    } else {
-                        const float* src = tile_ws + static_cast<int64_t>(j) * (MS * 128) + r;
-                        float t[MS];
+                    for (int b = 0; b < kBatch; ++b) {
+                        const int j = j0 + b;
+                        if (j < nslots && j != slot) {
+                            const float* src =
+                                tile_ws + static_cast<int64_t>(j) * (MS * 128) + r;
 #pragma unroll
-                        for (int m = 0; m < MS; ++m) t[m] = __ldcg(src + m * 128);
+                            for (int m = 0; m < MS; ++m) t[b][m] = __ldcg(src + m * 128);
+                        }
+                    }
 #pragma unroll
-                        for (int m = 0; m < MS; ++m) s[m] += t[m];
+                    for (int b = 0; b < kBatch; ++b) {
+                        const int j = j0 + b;
+                        if (j < nslots) {
+#pragma unroll
+                            for (int m = 0; m < MS; ++m) s[m] += (j == slot) ? v[m] : t[b][m];
+                        }
                     }
                 }
                 if (n < p.N) {
@@ -279,7 +291,7 @@ __global__ void __launch_bounds__(192, 1)
                     for (int m = 0; m < MS; ++m)
                         if (m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = s[m];
                 }
-                if (et == 0) p.counters[sg.tile] = 0;
+                if (et == 0) store_relaxed_gpu(&p.counters[sg.tile], 0);
             }
         }
     } else {

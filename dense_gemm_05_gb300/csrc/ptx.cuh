@@ -91,6 +91,19 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
     return r != 0;
 }
 
+// GPU-scope fetch-and-add with acquire+release semantics (one thread publishes
+// what its CTA wrote before a barrier, and acquires what earlier arrivals wrote).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void store_relaxed_gpu(int* addr, int v) {
+    asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
