@@ -15,7 +15,23 @@
 #include "common.cuh"
 #include "ptx.cuh"
 
+// Recently encoded TMA descriptors, keyed by everything they encode (address,
+// extents, pitch, type, box): repeated calls on the same operands skip the
+// driver's encoder.  The descriptor is passed to the kernel by value, so a
+// cached entry never aliases one that a launch in flight still uses.
+struct TmapCacheEntry {
+    bool valid = false;
+    const void* ptr = nullptr;
+    int64_t inner = 0, outer = 0, ld = 0;
+    int dtype = 0;
+    uint32_t box_inner = 0, box_outer = 0;
+    CUtensorMap map;
+};
+
 struct gemm_plan_s {
+    std::mutex cache_mu;
+    TmapCacheEntry cache[8];
+    int cache_next = 0;
     int device = 0;
     int num_sms = 0;
     float* ws = nullptr;          // split-K partial tiles
@@ -76,6 +92,33 @@ bool encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* ptr, int64_t inner
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool cached_encode_2d(gemm_plan_s* plan, CUtensorMap* map, gemm_dtype_t dt, const void* ptr,
+                      int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
+                      uint32_t box_outer) {
+    std::lock_guard<std::mutex> lock(plan->cache_mu);
+    for (const TmapCacheEntry& e : plan->cache) {
+        if (e.valid && e.ptr == ptr && e.inner == inner && e.outer == outer && e.ld == ld &&
+            e.dtype == static_cast<int>(dt) && e.box_inner == box_inner &&
+            e.box_outer == box_outer) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!encode_2d(map, dt, ptr, inner, outer, ld, box_inner, box_outer)) return false;
+    TmapCacheEntry& e = plan->cache[plan->cache_next];
+    plan->cache_next = (plan->cache_next + 1) % 8;
+    e.valid = true;
+    e.ptr = ptr;
+    e.inner = inner;
+    e.outer = outer;
+    e.ld = ld;
+    e.dtype = static_cast<int>(dt);
+    e.box_inner = box_inner;
+    e.box_outer = box_outer;
+    e.map = *map;
+    return true;
 }
 
 bool tma_ok(const void* ptr, int64_t ld) {
@@ -502,16 +545,16 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
         const bool bf16 = dtype == GEMM_BF16;
         if (c.kernel == GEMM_KERNEL_TMA) {
             CUtensorMap ma, mb;
-            if (!encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
-                !encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+            if (!cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
+                !cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
                 return GEMM_ERR_CUDA;
             err = dg::launch_tma(c.bn, ma, mb, p, dg::idesc_f16(bf16, false, true, dg::kBM, c.bn),
                                  c.grid, stream);
         } else if (c.kernel == GEMM_KERNEL_PAIR) {
             // Each CTA of a pair loads 128 rows of A and 64-column sub-tiles of its half of B.
             CUtensorMap ma, mb;
-            if (!encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
-                !encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+            if (!cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
+                !cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
                 return GEMM_ERR_CUDA;
             err = dg::launch_pair(c.bn, ma, mb, p,
                                   dg::idesc_f16(bf16, false, true, 2 * dg::kBM, c.bn), c.grid,
@@ -521,8 +564,8 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
                                      stream);
         } else {
             CUtensorMap mb, ma;
-            if (!encode_2d(&mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK) ||
-                !encode_2d(&ma, dtype, A, K, M, lda, dg::kBK, static_cast<uint32_t>(c.ms)))
+            if (!cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK) ||
+                !cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, static_cast<uint32_t>(c.ms)))
                 return GEMM_ERR_CUDA;
             err = dg::launch_skinny(c.ms, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, c.ms),
                                     c.grid, stream);
