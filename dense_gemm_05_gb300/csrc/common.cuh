@@ -92,6 +92,44 @@ __host__ __device__ __forceinline__ int shares_per_tile_bound(int64_t T, int64_t
     return static_cast<int>((num_kb + shortest - 1) / shortest) + 1;
 }
 
+// Cost model of the skinny kernel, in units of one 64-deep K block streamed by
+// one SM (measured on GB300 with graph-replayed launches): HBM saturates at
+// about 100 SMs streaming at once, and a split tile's fix-up (partial stores,
+// arrival counter, last-arriver reduction) costs about 10 K blocks.
+constexpr int64_t kSkinnyDramStreams = 100;
+constexpr int64_t kSkinnyFixupKb = 10;
+constexpr int64_t kSkinnyMinShareKb = 4;   // a split share streams at least this many K blocks
+constexpr int64_t kSkinnyMaxShares = 4096;
+
+inline int64_t skinny_cost(int64_t T, int64_t G, int num_sms, int tiles) {
+    const int64_t waves = (G + num_sms - 1) / num_sms;
+    const int64_t longest = waves * ((T + G - 1) / G);
+    const int64_t dram = (T + kSkinnyDramStreams - 1) / kSkinnyDramStreams;
+    const bool split = G != tiles;   // one share per tile covers every tile whole
+    return (longest > dram ? longest : dram) + (split ? kSkinnyFixupKb : 0);
+}
+
+// The cheapest share count under skinny_cost among one share per tile, 2-4
+// equal shares per tile, and one share per SM.
+inline int64_t skinny_auto_shares(int tiles, int num_kb, int num_sms) {
+    const int64_t T = int64_t(tiles) * num_kb;
+    const int64_t per_sm = (T / kSkinnyMinShareKb < num_sms) ? T / kSkinnyMinShareKb : num_sms;
+    const int64_t cands[5] = {tiles, 2 * int64_t(tiles), 3 * int64_t(tiles), 4 * int64_t(tiles),
+                              per_sm};
+    int64_t best_g = tiles, best = -1;
+    for (int64_t g : cands) {
+        if (g > T) g = T;
+        if (g > kSkinnyMaxShares) g = kSkinnyMaxShares;
+        if (g < 1) g = 1;
+        const int64_t cost = skinny_cost(T, g, num_sms, tiles);
+        if (best < 0 || cost < best) {
+            best = cost;
+            best_g = g;
+        }
+    }
+    return best_g;
+}
+
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; none synchronises.
 

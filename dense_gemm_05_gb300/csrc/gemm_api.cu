@@ -192,16 +192,15 @@ gemm_status_t check_args(const Args& a) {
     return GEMM_OK;
 }
 
-constexpr int kMinShareKb = 4;     // a stream-K share streams at least this many K blocks
-constexpr int64_t kMaxShares = 4096;
+constexpr int64_t kMaxShares = dg::kSkinnyMaxShares;
 
-// Skinny stream-K shares.  `shares` <= 0: one share per SM (each at least
-// kMinShareKb K blocks); otherwise that many shares.  Falls back to one share
-// per tile (no partial tiles) when the workspace or counters cannot hold the
-// partials.  Returns false if even that is impossible.
+// Skinny stream-K shares.  `shares` <= 0: dg::skinny_auto_shares; otherwise
+// exactly that many shares.  Falls back to one share per tile (no partial
+// tiles) when the workspace or counters cannot hold the partials.  Returns
+// false if even that is impossible.
 bool choose_shares(const gemm_plan_s* plan, Choice* c, int64_t shares) {
     const int64_t T = int64_t(c->tiles_n) * c->num_kb;
-    int64_t G = shares > 0 ? shares : std::min<int64_t>(plan->num_sms, T / kMinShareKb);
+    int64_t G = shares > 0 ? shares : dg::skinny_auto_shares(c->tiles_n, c->num_kb, plan->num_sms);
     G = std::max<int64_t>(1, std::min<int64_t>({G, T, kMaxShares}));
     const int slots = dg::shares_per_tile_bound(T, G, c->num_kb);
     const int64_t need = int64_t(c->tiles_n) * slots * c->ms * 128 * 4;
@@ -263,9 +262,8 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : 64);
         c->tiles_m = 1;
         c->tiles_n = static_cast<int>(cdiv(a.N, 128));
-        // A forced split S means S equal shares per tile (S * tiles shares in all).
-        const int64_t forced = plan->force_split > 0 ? int64_t(plan->force_split) * c->tiles_n : 0;
-        if (!choose_shares(plan, c, forced)) return GEMM_ERR_UNSUPPORTED;
+        // A forced split is the total number of stream-K shares.
+        if (!choose_shares(plan, c, plan->force_split)) return GEMM_ERR_UNSUPPORTED;
         c->units = c->shares;
         c->stages = dg::skinny_stages(c->ms);
     } else if (kernel == GEMM_KERNEL_PAIR) {

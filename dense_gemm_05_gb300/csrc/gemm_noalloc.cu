@@ -168,16 +168,16 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     std::call_once(s->once, setup_device, s, dev);
     if (s->status != GEMM_OK) return s->status;
 
-    // Stream-K shares: one per SM (each at least 4 K blocks); if their partial
-    // tiles would not fit the scratch, one share per tile (no partials).
+    // Stream-K shares as gemm_run chooses them; if their partial tiles would not
+    // fit the scratch, one share per tile (no partials).
     const int ms = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
     const int tiles_n = static_cast<int>(cdiv(N, 128));
     const int num_kb = static_cast<int>(cdiv(K, dg::kBK));
     const int64_t T = int64_t(tiles_n) * num_kb;
-    int64_t shares = T / 4 < s->num_sms ? T / 4 : s->num_sms;
-    if (shares < 1) shares = 1;
-    if (int64_t(tiles_n) * dg::shares_per_tile_bound(T, shares, num_kb) * ms * 128 * 4 >
-        kScratchWsBytes)
+    int64_t shares = dg::skinny_auto_shares(tiles_n, num_kb, s->num_sms);
+    if (shares != tiles_n &&
+        int64_t(tiles_n) * dg::shares_per_tile_bound(T, shares, num_kb) * ms * 128 * 4 >
+            kScratchWsBytes)
         shares = tiles_n;
     const int max_slots = dg::shares_per_tile_bound(T, shares, num_kb);
     int* counters = reinterpret_cast<int*>(s->scratch + kScratchWsBytes);

@@ -146,7 +146,9 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
 /*
  * Force the next gemm_run calls on this plan to use `kernel` (a
  * gemm_kernel_t of TMA, GENERIC, SKINNY or PAIR; 0 = automatic choice),
- * `split_k` K-slices for SKINNY (0 = automatic) and `block_n` tile columns for
+ * `split_k` stream-K shares for SKINNY -- the (tile, K block) iterations of
+ * all tiles are cut into that many equal contiguous runs, one CTA each
+ * (0 = automatic) -- and `block_n` tile columns for
  * TMA/PAIR (128 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
  * arguments (e.g. TMA with a leading dimension that is not a multiple of 8).

@@ -113,7 +113,7 @@ def test_workload_skinny_full_and_deterministic(plan):
     A, B = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
     cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
-    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY and cfg["split_k"] > 1, cfg
+    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY, cfg
     got1 = run(plan, A, B, w.M, w.N, w.K)
     got2 = run(plan, A, B, w.M, w.N, w.K)
     assert_guards(got1, w.M, w.N)
@@ -121,18 +121,21 @@ def test_workload_skinny_full_and_deterministic(plan):
     assert_close(got1[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
 
 
-@pytest.mark.parametrize("M,K,N,dtype", [
-    (8, 1024, 65600, "bf16"),     # 513 tiles: shares span several tiles
-    (33, 2048, 640, "f16"),       # 5 tiles, MMA N = 64, tiles split across many shares
-    (1, 8192, 136, "bf16"),       # 2 tiles, 128 K blocks, ragged last tile
+@pytest.mark.parametrize("M,K,N,dtype,shares", [
+    (8, 1024, 65600, "bf16", 152),   # 513 tiles in 152 shares: shares span several tiles
+    (8, 1024, 65600, "bf16", 0),     # automatic choice
+    (33, 2048, 640, "f16", 0),       # 5 tiles, MMA N = 64, tiles split across many shares
+    (1, 8192, 136, "bf16", 0),       # 2 tiles, 128 K blocks, ragged last tile
+    (16, 4096, 14336, "bf16", 152),  # the M=16 workload's shape, one share per SM
+    (16, 4096, 14336, "bf16", 448),  # four shares per tile
 ])
-def test_skinny_stream_k_shapes(plan, M, K, N, dtype):
+def test_skinny_stream_k_shapes(plan, M, K, N, dtype, shares):
     A, B = workloads.custom(M, K, N, dtype, seed=M + K + N, dist="normal")
-    got1 = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_SKINNY)
-    got2 = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_SKINNY)
+    got1 = run(plan, A, B, M, N, K, split=shares, expect=g.GEMM_KERNEL_SKINNY)
+    got2 = run(plan, A, B, M, N, K, split=shares, expect=g.GEMM_KERNEL_SKINNY)
     assert_guards(got1, M, N)
     assert np.array_equal(got1, got2), "stream-K result changed between runs"
-    assert_close(got1[:M, :N], A, B, M, N, K, f"skinny {M}x{N}x{K}")
+    assert_close(got1[:M, :N], A, B, M, N, K, f"skinny {M}x{N}x{K} shares={shares}")
 
 
 def _sample_entries(M, N, bm, bn, n_random, seed):
@@ -246,7 +249,7 @@ def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
     (g.GEMM_KERNEL_TMA, 0, (1024, 2048, 1024), "f16"),
     (g.GEMM_KERNEL_GENERIC, 0, (300, 1000, 520), "f16"),
     (g.GEMM_KERNEL_SKINNY, 1, (16, 4096, 1024), "bf16"),
-    (g.GEMM_KERNEL_SKINNY, 4, (16, 4096, 1024), "bf16"),
+    (g.GEMM_KERNEL_SKINNY, 12, (16, 4096, 1024), "bf16"),
     (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
     (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
     (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1104), "bf16"),
@@ -385,6 +388,10 @@ def test_kernel_selection(plan):
     assert q(8192, 8192, 8192)["block_n"] == 256
     assert q(1023, 1000, 1029)["kernel"] == g.GEMM_KERNEL_GENERIC
     s = q(16, 4096, 14336)
-    assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["split_k"] > 1 and s["block_m"] == 16
+    assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["block_m"] == 16
+    # 112 tiles of 128 columns already saturate HBM: one share per tile, no split.
+    assert s["shares"] == 112 and s["split_k"] == 1, s
+    t = q(16, 4096, 4864)    # 38 tiles: stream-K spreads them over the SMs
+    assert t["shares"] > 38 and t["split_k"] > 1, t
     assert q(64, 512, 512)["kernel"] == g.GEMM_KERNEL_SKINNY
     assert q(65, 512, 512)["kernel"] == g.GEMM_KERNEL_TMA
