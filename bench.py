@@ -97,7 +97,8 @@ class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "timestamp")
 
     def __init__(self, index: int):
         self.index = index
@@ -135,21 +136,29 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.out.close()
+        import datetime
         rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    try:
+                        ts = datetime.datetime.strptime(parts[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    except ValueError:
+                        ts = None
+                    rows.append((ts, parts))
         os.unlink(self.path)
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        # samples taken inside the timed region (all of them if none fell inside)
+        inside = [p for ts, p in rows
+                  if ts is not None and self.t0 is not None and self.t0 <= ts <= (self.t1 or ts)]
+        use = inside or [p for _, p in rows]
+        sm = sorted(float(r[1]) for r in use if r[1].replace(".", "").isdigit())
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        loaded = sorted(sm)[len(sm) // 2:] if sm else []   # upper half: samples under load
-        med = loaded[len(loaded) // 2] if loaded else None
-        return {"sm_mhz": med, "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run (no sample inside the timed region)"}
 
 
 def oracle_rate(workload, rows: int, nthreads: int = 0) -> tuple[float, float, int]:
