@@ -56,6 +56,33 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the C signatures on a loaded oracle library (also used by the
+    mutation tests, which load deliberately broken builds of the same source)."""
+    u16p = ctypes.POINTER(ctypes.c_uint16)
+    f64p = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    i32 = ctypes.c_int
+    lib.oracle_gemm.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64, i64, i32]
+    lib.oracle_gemm.restype = i32
+    lib.oracle_absbound.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64, i64, i32]
+    lib.oracle_absbound.restype = i32
+    lib.oracle_gemm_entries.argtypes = [i32, u16p, i64, u16p, i64, i64, i64, i64,
+                                        i64p, i64p, i64, f64p, f64p, i32]
+    lib.oracle_gemm_entries.restype = i32
+    lib.oracle_gemm_blockwise.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64,
+                                          i64, i64]
+    lib.oracle_gemm_blockwise.restype = i32
+    lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f64.restype = ctypes.c_double
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f64.restype = ctypes.c_double
+    lib.oracle_max_threads.argtypes = []
+    lib.oracle_max_threads.restype = i32
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
@@ -63,30 +90,8 @@ def _load():
             return _lib
         if not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
             build()
-        lib = ctypes.CDLL(_LIB_PATH)
-        u16p = ctypes.POINTER(ctypes.c_uint16)
-        f64p = ctypes.POINTER(ctypes.c_double)
-        i64p = ctypes.POINTER(ctypes.c_int64)
-        i64 = ctypes.c_int64
-        i32 = ctypes.c_int
-        lib.oracle_gemm.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64, i64, i32]
-        lib.oracle_gemm.restype = i32
-        lib.oracle_absbound.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64, i64, i32]
-        lib.oracle_absbound.restype = i32
-        lib.oracle_gemm_entries.argtypes = [i32, u16p, i64, u16p, i64, i64, i64, i64,
-                                            i64p, i64p, i64, f64p, f64p, i32]
-        lib.oracle_gemm_entries.restype = i32
-        lib.oracle_gemm_blockwise.argtypes = [i32, u16p, i64, u16p, i64, f64p, i64, i64, i64,
-                                              i64, i64]
-        lib.oracle_gemm_blockwise.restype = i32
-        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
-        lib.oracle_f16_to_f64.restype = ctypes.c_double
-        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
-        lib.oracle_bf16_to_f64.restype = ctypes.c_double
-        lib.oracle_max_threads.argtypes = []
-        lib.oracle_max_threads.restype = i32
-        _lib = lib
-        return lib
+        _lib = bind(ctypes.CDLL(_LIB_PATH))
+        return _lib
 
 
 def _bits(x) -> tuple[np.ndarray, int]:
