@@ -30,6 +30,13 @@ GEMM_ERR_CUDA = 3
 GEMM_ERR_OOM = 4
 GEMM_ERR_TIMEOUT = 5
 
+GEMM_OP_N = 0
+GEMM_OP_T = 1
+
+GEMM_OUT_F32 = 0
+GEMM_OUT_F16 = 1
+GEMM_OUT_BF16 = 2
+
 GEMM_KERNEL_NONE = 0
 GEMM_KERNEL_ZERO_FILL = 1
 GEMM_KERNEL_TMA = 2
@@ -42,7 +49,7 @@ KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 
 #: Every function the header declares (checked by the tests against the library's exports).
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
-                 "gemm_wait_selftest", "gemm_run_noalloc")
+                 "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex")
 
 #: Limits of gemm_run_noalloc (mirrors of the header's macros).
 GEMM_NOALLOC_MAX_M = 64
@@ -105,6 +112,12 @@ def lib() -> ctypes.CDLL:
         L.gemm_wait_selftest.restype = i32
         L.gemm_run_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, vp]
         L.gemm_run_noalloc.restype = i32
+        L.gemm_run_ex.argtypes = [vp, i32, i32, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64,
+                                  i32, vp]
+        L.gemm_run_ex.restype = i32
+        L.gemm_query_ex.argtypes = [vp, i32, i32, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64,
+                                    i32, ctypes.POINTER(GemmConfig)]
+        L.gemm_query_ex.restype = i32
         _lib = L
         return L
 
@@ -128,6 +141,23 @@ def gemm_run(plan: int, A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M:
              K: int, dtype: int, stream: int = 0) -> int:
     """C = A @ B on `stream` (raw pointers as ints); returns the gemm_status_t code."""
     return int(lib().gemm_run(plan, A, lda, B, ldb, C, ldc, M, N, K, dtype, stream))
+
+
+def gemm_run_ex(plan: int, op_a: int, op_b: int, A: int, lda: int, B: int, ldb: int, C: int,
+                ldc: int, c_type: int, M: int, N: int, K: int, dtype: int, stream: int = 0) -> int:
+    """C = A @ B with A/B stored as op_a/op_b describe and C of type c_type."""
+    return int(lib().gemm_run_ex(plan, op_a, op_b, A, lda, B, ldb, C, ldc, c_type, M, N, K,
+                                 dtype, stream))
+
+
+def gemm_query_ex(plan: int, op_a: int, op_b: int, A: int, lda: int, B: int, ldb: int, C: int,
+                  ldc: int, c_type: int, M: int, N: int, K: int, dtype: int) -> dict:
+    cfg = GemmConfig()
+    st = lib().gemm_query_ex(plan, op_a, op_b, A, lda, B, ldb, C, ldc, c_type, M, N, K, dtype,
+                             ctypes.byref(cfg))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_query_ex")
+    return cfg.as_dict()
 
 
 def gemm_plan_destroy(plan: int | None) -> int:
@@ -187,6 +217,27 @@ def _ld(t) -> int:
     return t.stride(0) if t.size(0) > 1 else max(t.stride(0), t.size(1))
 
 
+def _operand(t) -> tuple[int, int]:
+    """(op, ld) of a 2-D logical operand view: row-major storage is GEMM_OP_N; a
+    transposed view of row-major storage (unit stride along dim 0) is GEMM_OP_T."""
+    if t.dim() != 2:
+        raise ValueError("matrices must be 2-D")
+    if t.stride(1) == 1 and (t.size(0) <= 1 or t.stride(0) >= t.size(1)):
+        return GEMM_OP_N, max(t.stride(0), t.size(1))
+    if t.stride(0) == 1 and (t.size(1) <= 1 or t.stride(1) >= t.size(0)):
+        return GEMM_OP_T, max(t.stride(1), t.size(0))
+    raise ValueError("each operand must be row-major or a transposed view of row-major storage")
+
+
+def _out_code(t) -> int:
+    import torch
+    codes = {torch.float32: GEMM_OUT_F32, torch.float16: GEMM_OUT_F16,
+             torch.bfloat16: GEMM_OUT_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"C must be float32, float16 or bfloat16, got {t.dtype}")
+    return codes[t.dtype]
+
+
 class Plan:
     """Owns one C-ABI plan; ``run``/``matmul`` marshal torch tensors into gemm_run."""
 
@@ -238,21 +289,50 @@ class Plan:
         if st != GEMM_OK:
             raise GemmError(st, "gemm_run")
 
-    def matmul(self, a, b):
+    def run_ex(self, a, b, c, stream=None) -> None:
+        """c = a @ b for logical views a (M x K), b (K x N), c (M x N): each of a, b
+        row-major or a transposed view of row-major storage; c row-major fp32/fp16/bf16."""
+        import torch
+        if a.dtype != b.dtype:
+            raise TypeError("A and B must have the same dtype")
+        M, K = a.shape
+        K2, N = b.shape
+        if K != K2 or tuple(c.shape) != (M, N):
+            raise ValueError(f"shapes {tuple(a.shape)} @ {tuple(b.shape)} -> {tuple(c.shape)}")
+        op_a, lda = _operand(a)
+        op_b, ldb = _operand(b)
+        s = (torch.cuda.current_stream(a.device) if stream is None else stream).cuda_stream
+        st = gemm_run_ex(self.handle, op_a, op_b, a.data_ptr(), lda, b.data_ptr(), ldb,
+                         c.data_ptr(), _ld(c), _out_code(c), M, N, K, _dtype_code(a), s)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_run_ex")
+
+    def query_ex(self, a, b, c) -> dict:
+        M, K = a.shape
+        N = b.shape[1]
+        op_a, lda = _operand(a)
+        op_b, ldb = _operand(b)
+        return gemm_query_ex(self.handle, op_a, op_b, a.data_ptr(), lda, b.data_ptr(), ldb,
+                             c.data_ptr(), _ld(c), _out_code(c), M, N, K, _dtype_code(a))
+
+    def matmul(self, a, b, out_dtype=None):
+        """C = a @ b (fp32 by default); a and b may be transposed views."""
         import torch
         if a.size(1) != b.size(0):
             raise ValueError(f"inner dimensions differ: {tuple(a.shape)} @ {tuple(b.shape)}")
-        c = torch.empty((a.size(0), b.size(1)), dtype=torch.float32, device=a.device)
-        self.run(a, b, c)
+        c = torch.empty((a.size(0), b.size(1)), dtype=out_dtype or torch.float32,
+                        device=a.device)
+        self.run_ex(a, b, c)
         return c
 
 
 _default_plans: dict = {}
 
 
-def matmul(a, b):
-    """fp32 C = A @ B for 2-D fp16/bf16 CUDA tensors, through a per-device default plan."""
+def matmul(a, b, out_dtype=None):
+    """C = A @ B for 2-D fp16/bf16 CUDA tensors (either may be a transposed view),
+    fp32 accumulation, C in fp32 or `out_dtype`, through a per-device default plan."""
     dev = a.device.index or 0
     if dev not in _default_plans:
         _default_plans[dev] = Plan(dev)
-    return _default_plans[dev].matmul(a, b)
+    return _default_plans[dev].matmul(a, b, out_dtype)

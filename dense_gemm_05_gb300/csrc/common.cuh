@@ -20,7 +20,8 @@ constexpr int kDevTimeout = 1;
 struct Params {
     const uint16_t* A;
     const uint16_t* B;
-    float* C;
+    void* C;                // fp32, fp16 or bf16 elements (c_type)
+    int32_t c_type;         // 0 fp32, 1 fp16, 2 bf16
     int64_t lda, ldb, ldc;
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_kb;
@@ -133,24 +134,29 @@ inline int64_t skinny_auto_shares(int tiles, int num_kb, int num_sms) {
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; none synchronises.
 
+// a_mn: A is stored K x M (transposed, M contiguous); otherwise M x K.
+// b_mn: B is stored K x N (N contiguous); otherwise N x K (transposed).
+
 // Persistent tcgen05 kernel, operands by TMA. bn in {128, 256}.
 int tma_smem_bytes(int bn);
 int tma_stages(int bn);
 cudaError_t tma_prepare();
-cudaError_t launch_tma(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
-                       uint32_t idesc, int grid, cudaStream_t stream);
+cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+                       const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
+                       cudaStream_t stream);
 
 // Same pipeline, operands staged by ordinary loads (any alignment). bn = 128.
 int generic_smem_bytes();
 int generic_stages();
 cudaError_t generic_prepare();
-cudaError_t launch_generic(const Params& p, uint32_t idesc, int grid, cudaStream_t stream);
+cudaError_t launch_generic(bool a_mn, bool b_mn, const Params& p, uint32_t idesc, int grid,
+                           cudaStream_t stream);
 
-// Skinny M: swap-AB + split-K. ms in {16, 32, 64} (MMA N = padded M).
+// Skinny M: swap-AB + stream-K. ms in {16, 32, 64} (MMA N = padded M); A is M x K.
 int skinny_smem_bytes(int ms);
 int skinny_stages(int ms);
 cudaError_t skinny_prepare();
-cudaError_t launch_skinny(int ms, const CUtensorMap& mapB, const CUtensorMap& mapA,
+cudaError_t launch_skinny(int ms, bool b_mn, const CUtensorMap& mapB, const CUtensorMap& mapA,
                           const Params& p, uint32_t idesc, int grid, cudaStream_t stream);
 
 // CTA-pair (cta_group::2) kernel, 256 x bn pair tiles, operands by TMA. bn in {128, 256}.
@@ -158,8 +164,9 @@ int pair_smem_bytes(int bn);
 int pair_stages(int bn);
 cudaError_t pair_prepare();
 int pair_max_clusters(int bn);   // co-resident 2-CTA clusters on the current device (0 = unknown)
-cudaError_t launch_pair(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
-                        uint32_t idesc, int grid, cudaStream_t stream);
+cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+                        const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
+                        cudaStream_t stream);
 
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);

@@ -132,10 +132,20 @@ struct Args {
     int64_t lda;
     const void* B;
     int64_t ldb;
-    const float* C;
+    const void* C;
     int64_t ldc;
     int64_t M, N, K;
     gemm_dtype_t dtype;
+    int op_a = GEMM_OP_N;       // GEMM_OP_T: A stored K x M
+    int op_b = GEMM_OP_N;       // GEMM_OP_T: B stored N x K
+    int c_type = GEMM_OUT_F32;
+
+    int64_t c_esize() const { return c_type == GEMM_OUT_F32 ? 4 : 2; }
+    // Stored shapes (rows x cols, row pitch = ld) of A and B.
+    int64_t a_rows() const { return op_a == GEMM_OP_N ? M : K; }
+    int64_t a_cols() const { return op_a == GEMM_OP_N ? K : M; }
+    int64_t b_rows() const { return op_b == GEMM_OP_N ? K : N; }
+    int64_t b_cols() const { return op_b == GEMM_OP_N ? N : K; }
 };
 
 struct Choice {
@@ -170,22 +180,30 @@ bool overlaps(const void* p, uint64_t plen, const void* q, uint64_t qlen) {
 
 gemm_status_t check_args(const Args& a) {
     if (a.M < 0 || a.N < 0 || a.K < 0) return GEMM_ERR_INVALID_ARG;
+    if ((a.op_a != GEMM_OP_N && a.op_a != GEMM_OP_T) ||
+        (a.op_b != GEMM_OP_N && a.op_b != GEMM_OP_T))
+        return GEMM_ERR_INVALID_ARG;
     if (a.dtype != GEMM_F16 && a.dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+    if (a.c_type != GEMM_OUT_F32 && a.c_type != GEMM_OUT_F16 && a.c_type != GEMM_OUT_BF16)
+        return GEMM_ERR_UNSUPPORTED;
     if (a.M > kMaxDim || a.N > kMaxDim || a.K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     if (a.M == 0 || a.N == 0) return GEMM_OK;
     constexpr int64_t kMaxLd = int64_t(1) << 40;
     if (a.C == nullptr || a.ldc < a.N) return GEMM_ERR_INVALID_ARG;
     if (a.ldc > kMaxLd) return GEMM_ERR_UNSUPPORTED;
-    if (reinterpret_cast<uintptr_t>(a.C) % 4u != 0u) return GEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(a.C) % static_cast<uintptr_t>(a.c_esize()) != 0u)
+        return GEMM_ERR_INVALID_ARG;
     uint64_t c_end = 0;
-    if (!region_end(a.M, a.N, a.ldc, 4, &c_end)) return GEMM_ERR_UNSUPPORTED;
+    if (!region_end(a.M, a.N, a.ldc, a.c_esize(), &c_end)) return GEMM_ERR_UNSUPPORTED;
     if (a.K == 0) return GEMM_OK;
-    if (a.A == nullptr || a.B == nullptr || a.lda < a.K || a.ldb < a.N) return GEMM_ERR_INVALID_ARG;
+    if (a.A == nullptr || a.B == nullptr || a.lda < a.a_cols() || a.ldb < a.b_cols())
+        return GEMM_ERR_INVALID_ARG;
     if (a.lda > kMaxLd || a.ldb > kMaxLd) return GEMM_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(a.A) % 2u != 0u || reinterpret_cast<uintptr_t>(a.B) % 2u != 0u)
         return GEMM_ERR_INVALID_ARG;
     uint64_t a_end = 0, b_end = 0;
-    if (!region_end(a.M, a.K, a.lda, 2, &a_end) || !region_end(a.K, a.N, a.ldb, 2, &b_end))
+    if (!region_end(a.a_rows(), a.a_cols(), a.lda, 2, &a_end) ||
+        !region_end(a.b_rows(), a.b_cols(), a.ldb, 2, &b_end))
         return GEMM_ERR_UNSUPPORTED;
     if (overlaps(a.C, c_end, a.A, a_end) || overlaps(a.C, c_end, a.B, b_end))
         return GEMM_ERR_INVALID_ARG;
@@ -239,7 +257,7 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         // Pair tiles (256 x 256 per two SMs) once there is at least a full wave of them;
         // they stage half as much B per flop as one-CTA tiles.
         const int64_t pair_tiles = cdiv(a.M, 2 * dg::kBM) * cdiv(a.N, 256);
-        if (tma && a.M <= 64)
+        if (tma && a.M <= 64 && a.op_a == GEMM_OP_N)
             kernel = GEMM_KERNEL_SKINNY;
         else if (tma && plan->pair_clusters[1] > 0 && pair_tiles >= plan->pair_clusters[1])
             kernel = GEMM_KERNEL_PAIR;
@@ -251,7 +269,8 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
     if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY ||
          kernel == GEMM_KERNEL_PAIR) && !tma)
         return GEMM_ERR_UNSUPPORTED;
-    if (kernel == GEMM_KERNEL_SKINNY && a.M > 64) return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_SKINNY && (a.M > 64 || a.op_a != GEMM_OP_N))
+        return GEMM_ERR_UNSUPPORTED;
     if (kernel == GEMM_KERNEL_PAIR && plan->pair_clusters[0] <= 0) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_SKINNY &&
         kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR)
@@ -464,11 +483,12 @@ gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int32
     return GEMM_OK;
 }
 
-gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
-                         const float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
-                         gemm_dtype_t dtype, gemm_config_t* out) {
+}  // extern "C"
+
+namespace {
+
+gemm_status_t query_impl(gemm_plan_t plan, const Args& a, gemm_config_t* out) {
     if (plan == nullptr || out == nullptr) return GEMM_ERR_INVALID_ARG;
-    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
     gemm_status_t st = check_args(a);
     if (st != GEMM_OK) return st;
     Choice c;
@@ -496,11 +516,8 @@ gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const voi
     return GEMM_OK;
 }
 
-gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
-                       float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
-                       gemm_dtype_t dtype, struct CUstream_st* stream_handle) {
+gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
     if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
-    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
     gemm_status_t st = check_args(a);
     if (st != GEMM_OK) return st;
     Choice c;
@@ -510,63 +527,81 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
 
     DeviceGuard guard(plan->device);
     if (!guard.ok) return GEMM_ERR_CUDA;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     cudaError_t err = cudaSuccess;
+    const int64_t esize = a.c_esize();
 
     if (c.kernel == GEMM_KERNEL_ZERO_FILL) {
-        err = cudaMemset2DAsync(C, static_cast<size_t>(ldc) * 4u, 0, static_cast<size_t>(N) * 4u,
-                                static_cast<size_t>(M), stream);
+        err = cudaMemset2DAsync(const_cast<void*>(a.C), static_cast<size_t>(a.ldc * esize), 0,
+                                static_cast<size_t>(a.N * esize), static_cast<size_t>(a.M),
+                                stream);
     } else {
+        const bool a_mn = a.op_a == GEMM_OP_T;     // A stored K x M: M contiguous
+        const bool b_mn = a.op_b == GEMM_OP_N;     // B stored K x N: N contiguous
         dg::Params p{};
-        p.A = static_cast<const uint16_t*>(A);
-        p.B = static_cast<const uint16_t*>(B);
-        p.C = C;
-        p.lda = lda;
-        p.ldb = ldb;
-        p.ldc = ldc;
-        p.M = static_cast<int32_t>(M);
-        p.N = static_cast<int32_t>(N);
-        p.K = static_cast<int32_t>(K);
+        p.A = static_cast<const uint16_t*>(a.A);
+        p.B = static_cast<const uint16_t*>(a.B);
+        p.C = const_cast<void*>(a.C);
+        p.c_type = a.c_type;
+        p.lda = a.lda;
+        p.ldb = a.ldb;
+        p.ldc = a.ldc;
+        p.M = static_cast<int32_t>(a.M);
+        p.N = static_cast<int32_t>(a.N);
+        p.K = static_cast<int32_t>(a.K);
         p.tiles_m = c.tiles_m;
         p.tiles_n = c.tiles_n;
         p.num_kb = c.num_kb;
         p.group = plan->group;
         p.shares = c.shares;
         p.max_slots = c.max_slots;
-        p.a_vec = tma_ok(A, lda) ? 1 : 0;
-        p.b_vec = tma_ok(B, ldb) ? 1 : 0;
-        p.c_vec = ((reinterpret_cast<uintptr_t>(C) % 16u) == 0u && ldc % 4 == 0) ? 1 : 0;
+        p.a_vec = tma_ok(a.A, a.lda) ? 1 : 0;
+        p.b_vec = tma_ok(a.B, a.ldb) ? 1 : 0;
+        p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16u) == 0u && (a.ldc * esize) % 16 == 0)
+                      ? 1
+                      : 0;
         p.ws = plan->ws;
         p.counters = plan->counters;
         p.status = plan->status;
         p.timeout_ns = plan->timeout_ns;
-        const bool bf16 = dtype == GEMM_BF16;
+        const bool bf16 = a.dtype == GEMM_BF16;
+        // TMA descriptors: a K-major operand is read as boxes {64 k, rows}; an
+        // MN-major one as boxes {64 mn, 64 k}.
+        auto map_a = [&](CUtensorMap* m, uint32_t rows) {
+            return a_mn ? cached_encode_2d(plan, m, a.dtype, a.A, a.M, a.K, a.lda, dg::kSubN,
+                                           dg::kBK)
+                        : cached_encode_2d(plan, m, a.dtype, a.A, a.K, a.M, a.lda, dg::kBK, rows);
+        };
+        auto map_b = [&](CUtensorMap* m, uint32_t rows) {
+            return b_mn ? cached_encode_2d(plan, m, a.dtype, a.B, a.N, a.K, a.ldb, dg::kSubN,
+                                           dg::kBK)
+                        : cached_encode_2d(plan, m, a.dtype, a.B, a.K, a.N, a.ldb, dg::kBK, rows);
+        };
         if (c.kernel == GEMM_KERNEL_TMA) {
             CUtensorMap ma, mb;
-            if (!cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
-                !cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+            if (!map_a(&ma, dg::kBM) || !map_b(&mb, static_cast<uint32_t>(c.bn)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_tma(c.bn, ma, mb, p, dg::idesc_f16(bf16, false, true, dg::kBM, c.bn),
-                                 c.grid, stream);
+            err = dg::launch_tma(c.bn, a_mn, b_mn, ma, mb, p,
+                                 dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, c.bn), c.grid, stream);
         } else if (c.kernel == GEMM_KERNEL_PAIR) {
-            // Each CTA of a pair loads 128 rows of A and 64-column sub-tiles of its half of B.
+            // Each CTA of a pair loads 128 rows of A and its half (bn / 2) of the B tile.
             CUtensorMap ma, mb;
-            if (!cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, dg::kBM) ||
-                !cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK))
+            if (!map_a(&ma, dg::kBM) || !map_b(&mb, static_cast<uint32_t>(c.bn / 2)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_pair(c.bn, ma, mb, p,
-                                  dg::idesc_f16(bf16, false, true, 2 * dg::kBM, c.bn), c.grid,
+            err = dg::launch_pair(c.bn, a_mn, b_mn, ma, mb, p,
+                                  dg::idesc_f16(bf16, a_mn, b_mn, 2 * dg::kBM, c.bn), c.grid,
                                   stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {
-            err = dg::launch_generic(p, dg::idesc_f16(bf16, false, true, dg::kBM, 128), c.grid,
+            err = dg::launch_generic(a_mn, b_mn, p,
+                                     dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, 128), c.grid,
                                      stream);
         } else {
+            // Swap-AB: the B^T tile (128 N rows) is the MMA's A operand, the A tile
+            // (K-major, M <= 64 rows) its B operand.
             CUtensorMap mb, ma;
-            if (!cached_encode_2d(plan, &mb, dtype, B, N, K, ldb, dg::kSubN, dg::kBK) ||
-                !cached_encode_2d(plan, &ma, dtype, A, K, M, lda, dg::kBK, static_cast<uint32_t>(c.ms)))
+            if (!map_b(&mb, 128) || !map_a(&ma, static_cast<uint32_t>(c.ms)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_skinny(c.ms, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, c.ms),
-                                    c.grid, stream);
+            err = dg::launch_skinny(c.ms, b_mn, mb, ma, p,
+                                    dg::idesc_f16(bf16, b_mn, false, 128, c.ms), c.grid, stream);
         }
     }
     if (err != cudaSuccess) {
@@ -589,6 +624,46 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void*
         }
     }
     return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_query(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
+                         const float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                         gemm_dtype_t dtype, gemm_config_t* out) {
+    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    return query_impl(plan, a, out);
+}
+
+gemm_status_t gemm_query_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t op_b, const void* A,
+                            int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                            gemm_out_t c_type, int64_t M, int64_t N, int64_t K,
+                            gemm_dtype_t dtype, gemm_config_t* out) {
+    Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    a.op_a = op_a;
+    a.op_b = op_b;
+    a.c_type = c_type;
+    return query_impl(plan, a, out);
+}
+
+gemm_status_t gemm_run(gemm_plan_t plan, const void* A, int64_t lda, const void* B, int64_t ldb,
+                       float* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                       gemm_dtype_t dtype, struct CUstream_st* stream_handle) {
+    const Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    return run_impl(plan, a, reinterpret_cast<cudaStream_t>(stream_handle));
+}
+
+gemm_status_t gemm_run_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t op_b, const void* A,
+                          int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                          gemm_out_t c_type, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                          struct CUstream_st* stream_handle) {
+    Args a{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    a.op_a = op_a;
+    a.op_b = op_b;
+    a.c_type = c_type;
+    return run_impl(plan, a, reinterpret_cast<cudaStream_t>(stream_handle));
 }
 
 gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st* stream_handle) {

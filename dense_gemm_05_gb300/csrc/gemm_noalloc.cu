@@ -195,6 +195,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.A = static_cast<const uint16_t*>(A);
     p.B = static_cast<const uint16_t*>(B);
     p.C = C;
+    p.c_type = 0;   // fp32 C
     p.lda = lda;
     p.ldb = ldb;
     p.ldc = ldc;
@@ -216,7 +217,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.timeout_ns = 2000000000ull;
     const int grid = shares < s->num_sms ? static_cast<int>(shares) : s->num_sms;
     const bool bf16 = dtype == GEMM_BF16;
-    if (dg::launch_skinny(ms, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, ms), grid,
+    if (dg::launch_skinny(ms, true, mb, ma, p, dg::idesc_f16(bf16, true, false, 128, ms), grid,
                           stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;

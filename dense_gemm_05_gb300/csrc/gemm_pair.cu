@@ -21,6 +21,7 @@
 //   tempty[a] (CTA 0)  256 arrivals: the epilogue threads of both CTAs
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace dg {
 
@@ -37,7 +38,7 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
                      const __grid_constant__ CUtensorMap mapB, const Params p,
@@ -115,16 +116,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a0 =
-                        sdesc_sw128(smem_u32(sA + stage * kAStageBytes), 16u, 1024u);
-                    const uint64_t b0 = sdesc_sw128(smem_u32(sB + stage * Cfg::kBStageBytes),
-                                                    static_cast<uint32_t>(kSubTileBytes), 1024u);
+                    const uint32_t a_base = smem_u32(sA + stage * kAStageBytes);
+                    const uint32_t b_base = smem_u32(sB + stage * Cfg::kBStageBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        tc_mma_f16_pair(d_tmem, a0 + static_cast<uint64_t>((k * 32) >> 4),
-                                        b0 + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc,
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_f16_pair(d_tmem, operand_desc<A_MN>(a_base, k),
+                                        operand_desc<B_MN>(b_base, k), idesc,
                                         (kb | k) != 0 ? 1u : 0u);
-                    }
                     tc_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -168,7 +166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             tc_fence_after();
             const int row = tm * 256 + row_in_tile;
             const int col0 = tn * BN;
-            float* crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+            const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
             const bool row_ok = row < p.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
@@ -181,23 +179,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     tc_fence_before();
                     mbar_arrive_cluster(acc == 0 ? tempty0 : tempty1);
                 }
-                if (row_ok) {
-                    const int ncols = p.N - (col0 + c * 32);
-                    float* dst = crow + c * 32;
-                    if (p.c_vec && ncols >= 32) {
-                        float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(__uint_as_float(v[4 * i]),
-                                                __uint_as_float(v[4 * i + 1]),
-                                                __uint_as_float(v[4 * i + 2]),
-                                                __uint_as_float(v[4 * i + 3]));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (i < ncols) dst[i] = __uint_as_float(v[i]);
-                    }
-                }
+                if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
             }
             if (++acc == 2) {
                 acc = 0;
@@ -224,13 +206,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t fb_local = smem_u32(&full[stage]);
                     const uint32_t fb = mapa_shared(fb_local, 0);   // CTA 0's full[stage]
                     if (leader) mbar_arrive_expect_tx(fb_local, 2u * Cfg::kStageBytes);
-                    tma_load_2d_pair(smem_u32(sA + stage * kAStageBytes), &mapA, fb, kb * kBK,
-                                     a_row);
-#pragma unroll
-                    for (int j = 0; j < Cfg::kBHalf / kSubN; ++j)
-                        tma_load_2d_pair(
-                            smem_u32(sB + stage * Cfg::kBStageBytes + j * kSubTileBytes), &mapB,
-                            fb, b_col + j * kSubN, kb * kBK);
+                    load_operand_pair<A_MN>(smem_u32(sA + stage * kAStageBytes), &mapA, fb, a_row,
+                                            kb * kBK, kBM);
+                    load_operand_pair<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb,
+                                            b_col, kb * kBK, Cfg::kBHalf);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -280,22 +259,41 @@ namespace {
 constexpr int kPairStages256 = 6;
 constexpr int kPairStages128 = 8;
 
-template <int BN, int STAGES>
-cudaError_t set_attrs() {
-    return cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES>,
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+cudaError_t set_attrs_one() {
+    return cudaFuncSetAttribute(gemm_pair_kernel<BN, STAGES, A_MN, B_MN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 PairCfg<BN, STAGES>::kSmemBytes);
 }
 
 template <int BN, int STAGES>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, uint32_t idesc,
-                   int grid, cudaStream_t s) {
-    gemm_pair_kernel<BN, STAGES>
+cudaError_t set_attrs() {
+    cudaError_t e = set_attrs_one<BN, STAGES, false, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, false, false>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, true, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, true, false>();
+    return e;
+}
+
+template <int BN, int STAGES, bool A_MN, bool B_MN>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p, uint32_t idesc,
+                       int grid, cudaStream_t s) {
+    gemm_pair_kernel<BN, STAGES, A_MN, B_MN>
         <<<grid, PairCfg<BN, STAGES>::kThreads, PairCfg<BN, STAGES>::kSmemBytes, s>>>(a, b, p,
                                                                                    idesc);
     return cudaGetLastError();
 }
 
+template <int BN, int STAGES>
+cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
+                   const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true>(a, b, p, idesc, grid, s);
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false>(a, b, p, idesc, grid, s);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true>(a, b, p, idesc, grid, s);
+    return launch_one<BN, STAGES, true, false>(a, b, p, idesc, grid, s);
+}
+
+// All four layout instantiations have the same resources, so one query serves them.
 template <int BN, int STAGES>
 int max_clusters() {
     cudaLaunchConfig_t cfg = {};
@@ -310,7 +308,8 @@ int max_clusters() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, STAGES>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, STAGES, false, true>, &cfg) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -335,10 +334,12 @@ int pair_max_clusters(int bn) {
     return bn == 256 ? max_clusters<256, kPairStages256>() : max_clusters<128, kPairStages128>();
 }
 
-cudaError_t launch_pair(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
-                        uint32_t idesc, int grid, cudaStream_t stream) {
-    if (bn == 256) return launch<256, kPairStages256>(mapA, mapB, p, idesc, grid, stream);
-    return launch<128, kPairStages128>(mapA, mapB, p, idesc, grid, stream);
+cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+                        const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
+                        cudaStream_t stream) {
+    if (bn == 256)
+        return launch<256, kPairStages256>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
+    return launch<128, kPairStages128>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
 }
 
 }  // namespace dg

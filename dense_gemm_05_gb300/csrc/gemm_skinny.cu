@@ -22,6 +22,7 @@
 // 1..4 epilogue, warp 5 TMA producer.  All three walk the same segments.
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace dg {
 
@@ -92,7 +93,7 @@ __device__ __forceinline__ void load_acc(uint32_t taddr, float (&v)[MS]) {
     }
 }
 
-template <int MS, int STAGES>
+template <int MS, int STAGES, bool B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_skinny_kernel(const __grid_constant__ CUtensorMap mapB,
                        const __grid_constant__ CUtensorMap mapA, const Params p,
@@ -167,16 +168,14 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a0 = sdesc_sw128(smem_u32(sBt + stage * Cfg::kBtStageBytes),
-                                                    static_cast<uint32_t>(kSubTileBytes), 1024u);
-                    const uint64_t b0 =
-                        sdesc_sw128(smem_u32(sA + stage * Cfg::kAStageBytes), 16u, 1024u);
+                    // MMA A = the B^T tile (N on the MMA's rows), MMA B = the A tile.
+                    const uint32_t bt_base = smem_u32(sBt + stage * Cfg::kBtStageBytes);
+                    const uint32_t a_base = smem_u32(sA + stage * Cfg::kAStageBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        tc_mma_f16(d_tmem, a0 + static_cast<uint64_t>((k * 16 * 128) >> 4),
-                                   b0 + static_cast<uint64_t>((k * 32) >> 4), idesc,
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_f16(d_tmem, operand_desc<B_MN>(bt_base, k),
+                                   operand_desc<false>(a_base, k), idesc,
                                    (kb != sg.kb0 || k != 0) ? 1u : 0u);
-                    }
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -236,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (n < p.N) {
 #pragma unroll
                     for (int m = 0; m < MS; ++m)
-                        if (m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = v[m];
+                        if (m < p.M) store_c1(p, static_cast<int64_t>(m) * p.ldc + n, v[m]);
                 }
                 continue;
             }
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (n < p.N) {
 #pragma unroll
                     for (int m = 0; m < MS; ++m)
-                        if (m < p.M) p.C[static_cast<int64_t>(m) * p.ldc + n] = s[m];
+                        if (m < p.M) store_c1(p, static_cast<int64_t>(m) * p.ldc + n, s[m]);
                 }
                 if (et == 0) store_relaxed_gpu(&p.counters[sg.tile], 0);
             }
@@ -314,11 +313,8 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        tma_load_2d_hint(
-                            smem_u32(sBt + stage * Cfg::kBtStageBytes + j * kSubTileBytes), &mapB,
-                            fb, sg.tile * 128 + j * kSubN, kb * kBK, pol_stream);
+                    load_operand_hint<B_MN>(smem_u32(sBt + stage * Cfg::kBtStageBytes), &mapB,
+                                            fb, sg.tile * 128, kb * kBK, 128, pol_stream);
                     tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb,
                                      kb * kBK, 0, pol_keep);
                     ++armed;
@@ -366,16 +362,26 @@ constexpr int kStages64 = 8;
 
 template <int MS, int STAGES>
 cudaError_t set_attrs() {
-    return cudaFuncSetAttribute(gemm_skinny_kernel<MS, STAGES>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<MS, STAGES, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SkCfg<MS, STAGES>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm_skinny_kernel<MS, STAGES, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SkCfg<MS, STAGES>::kSmemBytes);
 }
 
 template <int MS, int STAGES>
-cudaError_t launch(const CUtensorMap& b, const CUtensorMap& a, const Params& p, uint32_t idesc,
-                   int grid, cudaStream_t s) {
-    gemm_skinny_kernel<MS, STAGES>
-        <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p, idesc);
+cudaError_t launch(bool b_mn, const CUtensorMap& b, const CUtensorMap& a, const Params& p,
+                   uint32_t idesc, int grid, cudaStream_t s) {
+    if (b_mn)
+        gemm_skinny_kernel<MS, STAGES, true>
+            <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p,
+                                                                                   idesc);
+    else
+        gemm_skinny_kernel<MS, STAGES, false>
+            <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p,
+                                                                                   idesc);
     return cudaGetLastError();
 }
 }  // namespace
@@ -395,11 +401,11 @@ cudaError_t skinny_prepare() {
     return e;
 }
 
-cudaError_t launch_skinny(int ms, const CUtensorMap& mapB, const CUtensorMap& mapA,
+cudaError_t launch_skinny(int ms, bool b_mn, const CUtensorMap& mapB, const CUtensorMap& mapA,
                           const Params& p, uint32_t idesc, int grid, cudaStream_t stream) {
-    if (ms == 16) return launch<16, kStages16>(mapB, mapA, p, idesc, grid, stream);
-    if (ms == 32) return launch<32, kStages32>(mapB, mapA, p, idesc, grid, stream);
-    return launch<64, kStages64>(mapB, mapA, p, idesc, grid, stream);
+    if (ms == 16) return launch<16, kStages16>(b_mn, mapB, mapA, p, idesc, grid, stream);
+    if (ms == 32) return launch<32, kStages32>(b_mn, mapB, mapA, p, idesc, grid, stream);
+    return launch<64, kStages64>(b_mn, mapB, mapA, p, idesc, grid, stream);
 }
 
 }  // namespace dg

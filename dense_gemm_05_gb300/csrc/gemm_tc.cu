@@ -12,9 +12,11 @@
 //   warps 5..8    load/store producer (generic variant, any alignment)
 //
 // Shared memory holds a ring of STAGES {A 128x64, B 64xBN} tiles in the
-// 128-byte-swizzled layout; "full" barriers hand a stage to the MMA issuer,
-// "empty" barriers (tcgen05.commit) hand it back.  Two TMEM accumulators of
-// 128 x BN fp32 let the epilogue drain tile i while the MMAs of tile i+1 run.
+// 128-byte-swizzled layouts of tiles.cuh (A_MN / B_MN: the operand is stored
+// with M / N contiguous, i.e. A transposed, or B in its natural K x N layout);
+// "full" barriers hand a stage to the MMA issuer, "empty" barriers
+// (tcgen05.commit) hand it back.  Two TMEM accumulators of 128 x BN fp32 let
+// the epilogue drain tile i while the MMAs of tile i+1 run.
 //
 // Masking: TMA fills elements outside the global tensor with zeros (the
 // masked load with other=0 of "I Wrote a GPU Matmul Kernel From Scratch in
@@ -22,6 +24,7 @@
 // stores only rows < M and columns < N (the masked store).
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace dg {
 
@@ -67,23 +70,39 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-// 32 consecutive fp32 values of one C row, the first `ncols` of them in range.
-__device__ __forceinline__ void store_row32(float* dst, const uint32_t (&v)[32], int ncols,
-                                            int vec) {
-    if (vec && ncols >= 32) {
-        float4* d4 = reinterpret_cast<float4*>(dst);
+// One operand tile (ROWS M/N rows x 64 K) staged by 128 threads with ordinary
+// loads into the same swizzled layout TMA would produce.  MN_MAJOR: the stored
+// operand has K rows of contiguous M/N elements; otherwise M/N rows of
+// contiguous K elements.  Out-of-range elements are written as zeros.
+template <bool MN_MAJOR, int ROWS>
+__device__ __forceinline__ void load_tile_generic(uint32_t dst, const uint16_t* base, int64_t ld,
+                                                  int mn0, int k0, int mn_total, int k_total,
+                                                  int vec, int pt) {
+    constexpr int kChunks = ROWS * kBK / 8;      // 16-byte chunks in the tile
+    constexpr int kPer = kChunks / 128;
+    constexpr int kRowChunks = MN_MAJOR ? ROWS / 8 : kBK / 8;
+    uint4 v[kPer];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-    } else {
+    for (int i = 0; i < kPer; ++i) {
+        const int q = pt + i * 128;
+        const int r = q / kRowChunks, c = q % kRowChunks;
+        if constexpr (MN_MAJOR) {
+            const int k = k0 + r, mn = mn0 + c * 8;
+            v[i] = load8(base, static_cast<int64_t>(k) * ld + mn, k < k_total, mn_total - mn, vec);
+        } else {
+            const int mn = mn0 + r, k = k0 + c * 8;
+            v[i] = load8(base, static_cast<int64_t>(mn) * ld + k, mn < mn_total, k_total - k, vec);
+        }
+    }
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i < ncols) dst[i] = __uint_as_float(v[i]);
+    for (int i = 0; i < kPer; ++i) {
+        const int q = pt + i * 128;
+        const int r = q / kRowChunks, c = q % kRowChunks;
+        st_shared_v4(dst + chunk_offset<MN_MAJOR>(r, c), v[i]);
     }
 }
 
-template <int BN, int STAGES, bool GENERIC>
+template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB, const Params p,
@@ -156,18 +175,12 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t a0 =
-                        sdesc_sw128(smem_u32(sA + stage * kAStageBytes), 16u, 1024u);
-                    const uint64_t b0 = sdesc_sw128(smem_u32(sB + stage * Cfg::kBStageBytes),
-                                                    static_cast<uint32_t>(kSubTileBytes), 1024u);
+                    const uint32_t a_base = smem_u32(sA + stage * kAStageBytes);
+                    const uint32_t b_base = smem_u32(sB + stage * Cfg::kBStageBytes);
 #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        // K-major A: +32 B per 16 elements inside the swizzle row.
-                        // MN-major B: +16 K-rows of 128 B.
-                        tc_mma_f16(d_tmem, a0 + static_cast<uint64_t>((k * 32) >> 4),
-                                   b0 + static_cast<uint64_t>((k * 16 * 128) >> 4), idesc,
-                                   (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kBK / 16; ++k)
+                        tc_mma_f16(d_tmem, operand_desc<A_MN>(a_base, k),
+                                   operand_desc<B_MN>(b_base, k), idesc, (kb | k) != 0 ? 1u : 0u);
                     tc_commit(smem_u32(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
             tc_fence_after();
             const int row = tm * kBM + row_in_tile;
             const int col0 = tn * BN;
-            float* crow = p.C + static_cast<int64_t>(row) * p.ldc + col0;
+            const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
             const bool row_ok = row < p.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
@@ -221,7 +234,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     tc_fence_before();
                     mbar_arrive(smem_u32(&tempty[acc]));
                 }
-                if (row_ok) store_row32(crow + c * 32, v, p.N - (col0 + c * 32), p.c_vec);
+                if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
             }
             if (++acc == 2) {
                 acc = 0;
@@ -246,12 +259,10 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
-                    tma_load_2d(smem_u32(sA + stage * kAStageBytes), &mapA, fb, kb * kBK,
-                                tm * kBM);
-#pragma unroll
-                    for (int j = 0; j < BN / kSubN; ++j)
-                        tma_load_2d(smem_u32(sB + stage * Cfg::kBStageBytes + j * kSubTileBytes),
-                                    &mapB, fb, tn * BN + j * kSubN, kb * kBK);
+                    load_operand<A_MN>(smem_u32(sA + stage * kAStageBytes), &mapA, fb, tm * kBM,
+                                       kb * kBK, kBM);
+                    load_operand<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb,
+                                       tn * BN, kb * kBK, BN);
                     ++armed;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -283,7 +294,6 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
         const int pt = threadIdx.x - 160;     // 0..127
         int stage = 0;
         uint32_t phase = 0;
-        constexpr int kBChunks = (kBK * BN / 8) / 128;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
             int tm, tn;
             tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
@@ -293,41 +303,10 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     failed = true;
                     break;
                 }
-                const int k0 = kb * kBK;
-                uint4 ra[8];
-                uint4 rb[kBChunks];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = pt + i * 128;
-                    const int r = c >> 3, kc = c & 7;
-                    const int m = tm * kBM + r, k = k0 + kc * 8;
-                    ra[i] = load8(p.A, static_cast<int64_t>(m) * p.lda + k, m < p.M, p.K - k,
-                                  p.a_vec);
-                }
-#pragma unroll
-                for (int i = 0; i < kBChunks; ++i) {
-                    const int c = pt + i * 128;
-                    const int kr = c / (BN / 8), nc = c % (BN / 8);
-                    const int k = k0 + kr, n = tn * BN + nc * 8;
-                    rb[i] = load8(p.B, static_cast<int64_t>(k) * p.ldb + n, k < p.K, p.N - n,
-                                  p.b_vec);
-                }
-                const uint32_t a_dst = smem_u32(sA + stage * kAStageBytes);
-                const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStageBytes);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int c = pt + i * 128;
-                    const int r = c >> 3, kc = c & 7;
-                    st_shared_v4(a_dst + r * 128 + ((kc ^ (r & 7)) << 4), ra[i]);
-                }
-#pragma unroll
-                for (int i = 0; i < kBChunks; ++i) {
-                    const int c = pt + i * 128;
-                    const int kr = c / (BN / 8), nc = c % (BN / 8);
-                    st_shared_v4(b_dst + (nc >> 3) * kSubTileBytes + kr * 128 +
-                                     (((nc & 7) ^ (kr & 7)) << 4),
-                                 rb[i]);
-                }
+                load_tile_generic<A_MN, kBM>(smem_u32(sA + stage * kAStageBytes), p.A, p.lda,
+                                             tm * kBM, kb * kBK, p.M, p.K, p.a_vec, pt);
+                load_tile_generic<B_MN, BN>(smem_u32(sB + stage * Cfg::kBStageBytes), p.B, p.ldb,
+                                            tn * BN, kb * kBK, p.N, p.K, p.b_vec, pt);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full[stage]));
                 if (++stage == STAGES) {
@@ -357,20 +336,39 @@ constexpr int kTmaStages256 = 4;
 constexpr int kTmaStages128 = 6;
 constexpr int kGenericStages = 4;
 
-template <int BN, int STAGES, bool GENERIC>
-cudaError_t set_attrs() {
+template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
+cudaError_t set_attrs_one() {
     using Cfg = TcCfg<BN, STAGES, GENERIC>;
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, GENERIC>,
+    return cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
 }
 
 template <int BN, int STAGES, bool GENERIC>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, uint32_t idesc,
-                   int grid, cudaStream_t s) {
+cudaError_t set_attrs() {
+    cudaError_t e = set_attrs_one<BN, STAGES, GENERIC, false, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, false, false>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, true, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, true, false>();
+    return e;
+}
+
+template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                       uint32_t idesc, int grid, cudaStream_t s) {
     using Cfg = TcCfg<BN, STAGES, GENERIC>;
-    gemm_tc_kernel<BN, STAGES, GENERIC><<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p,
-                                                                                    idesc);
+    gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>
+        <<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p, idesc);
     return cudaGetLastError();
+}
+
+template <int BN, int STAGES, bool GENERIC>
+cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
+                   const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, GENERIC, false, true>(a, b, p, idesc, grid, s);
+    if (!a_mn && !b_mn)
+        return launch_one<BN, STAGES, GENERIC, false, false>(a, b, p, idesc, grid, s);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, GENERIC, true, true>(a, b, p, idesc, grid, s);
+    return launch_one<BN, STAGES, GENERIC, true, false>(a, b, p, idesc, grid, s);
 }
 }  // namespace
 
@@ -387,10 +385,12 @@ cudaError_t tma_prepare() {
     return set_attrs<128, kTmaStages128, false>();
 }
 
-cudaError_t launch_tma(int bn, const CUtensorMap& mapA, const CUtensorMap& mapB, const Params& p,
-                       uint32_t idesc, int grid, cudaStream_t stream) {
-    if (bn == 256) return launch<256, kTmaStages256, false>(mapA, mapB, p, idesc, grid, stream);
-    return launch<128, kTmaStages128, false>(mapA, mapB, p, idesc, grid, stream);
+cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+                       const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
+                       cudaStream_t stream) {
+    if (bn == 256)
+        return launch<256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
+    return launch<128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
 }
 
 int generic_smem_bytes() { return TcCfg<128, kGenericStages, true>::kSmemBytes; }
@@ -399,10 +399,11 @@ int generic_stages() { return kGenericStages; }
 
 cudaError_t generic_prepare() { return set_attrs<128, kGenericStages, true>(); }
 
-cudaError_t launch_generic(const Params& p, uint32_t idesc, int grid, cudaStream_t stream) {
+cudaError_t launch_generic(bool a_mn, bool b_mn, const Params& p, uint32_t idesc, int grid,
+                           cudaStream_t stream) {
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof(dummy));
-    return launch<128, kGenericStages, true>(dummy, dummy, p, idesc, grid, stream);
+    return launch<128, kGenericStages, true>(a_mn, b_mn, dummy, dummy, p, idesc, grid, stream);
 }
 
 }  // namespace dg

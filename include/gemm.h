@@ -63,6 +63,22 @@ typedef enum {
     GEMM_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (debug-sync mode) */
 } gemm_status_t;
 
+/* Storage of an operand for gemm_run_ex (the operation is always C = A @ B):
+ *   A: GEMM_OP_N  A[i, k] at A + i*lda + k   (stored M x K, lda >= K)
+ *      GEMM_OP_T  A[i, k] at A + k*lda + i   (stored K x M, lda >= M)
+ *   B: GEMM_OP_N  B[k, j] at B + k*ldb + j   (stored K x N, ldb >= N)
+ *      GEMM_OP_T  B[k, j] at B + j*ldb + k   (stored N x K, ldb >= K: the
+ *                 [out_features, in_features] layout of a linear layer's weight)
+ * The pages allow any strides (the stride_ak / stride_bk arguments of the
+ * autotuned kernel of Step 5 and of the "Triton 04" teaching kernel); these
+ * are the two unit-stride cases of each operand. */
+typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+/* Element type of C for gemm_run_ex.  16-bit outputs are the fp32 accumulator
+ * rounded to nearest-even once, as the fp16 store of section 4.5 of "Writing
+ * GPU kernels in Triton: Vector Add, Softmax, MatMul" (acc.to(float16)). */
+typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_F16 = 1, GEMM_OUT_BF16 = 2 } gemm_out_t;
+
 /* Which kernel gemm_run selects for a problem (see gemm_query). */
 typedef enum {
     GEMM_KERNEL_NONE = 0,       /* M == 0 or N == 0: nothing is launched */
@@ -114,6 +130,30 @@ GEMM_API gemm_status_t gemm_run(gemm_plan_t plan,
                        float *C, int64_t ldc,
                        int64_t M, int64_t N, int64_t K,
                        gemm_dtype_t dtype, struct CUstream_st *stream);
+
+/*
+ * gemm_run with operand storage and output type chosen by the caller:
+ * C = A @ B with A and B stored as op_a / op_b describe (gemm_op_t), fp32
+ * accumulation, and C[i, j] at C + i*ldc + j of type c_type (gemm_out_t).
+ * gemm_run(...) is gemm_run_ex(GEMM_OP_N, GEMM_OP_N, ..., GEMM_OUT_F32, ...).
+ * C must be aligned to its element size.  Same asynchrony, ownership, size
+ * rules and errors as gemm_run; INVALID_ARG also for an unknown op, and
+ * UNSUPPORTED for an unknown c_type.
+ */
+GEMM_API gemm_status_t gemm_run_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t op_b,
+                                   const void *A, int64_t lda,
+                                   const void *B, int64_t ldb,
+                                   void *C, int64_t ldc, gemm_out_t c_type,
+                                   int64_t M, int64_t N, int64_t K,
+                                   gemm_dtype_t dtype, struct CUstream_st *stream);
+
+/* gemm_query for the arguments of gemm_run_ex. */
+GEMM_API gemm_status_t gemm_query_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t op_b,
+                                     const void *A, int64_t lda,
+                                     const void *B, int64_t ldb,
+                                     const void *C, int64_t ldc, gemm_out_t c_type,
+                                     int64_t M, int64_t N, int64_t K,
+                                     gemm_dtype_t dtype, gemm_config_t *out);
 
 /* Release the plan and its workspace.  NULL-safe.  Waits for nothing: the
  * caller must make sure no gemm_run using the plan is still in flight. */
