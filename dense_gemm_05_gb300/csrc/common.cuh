@@ -30,6 +30,7 @@ struct Params {
     int32_t max_slots;      // skinny: partial-tile slots per output tile in the workspace
     int32_t a_vec, b_vec;   // generic producer: 16-byte vector loads are legal
     int32_t c_vec;          // 16-byte vector stores of C are legal
+    int32_t c_tma;          // the epilogue writes C with TMA stores (mapC is valid)
     float* ws;              // skinny: split-K partial sums
     int* counters;          // skinny: per-tile arrival counters (zero between launches)
     int* status;            // device error word (kDevTimeout on a wait that gave up)
@@ -142,8 +143,8 @@ int tma_smem_bytes(int bn);
 int tma_stages(int bn);
 cudaError_t tma_prepare();
 cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
-                       const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                       cudaStream_t stream);
+                       const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                       uint32_t idesc, int grid, cudaStream_t stream);
 
 // Same pipeline, operands staged by ordinary loads (any alignment). bn = 128.
 int generic_smem_bytes();
@@ -165,8 +166,8 @@ int pair_stages(int bn);
 cudaError_t pair_prepare();
 int pair_max_clusters(int bn);   // co-resident 2-CTA clusters on the current device (0 = unknown)
 cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
-                        const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                        cudaStream_t stream);
+                        const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                        uint32_t idesc, int grid, cudaStream_t stream);
 
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);

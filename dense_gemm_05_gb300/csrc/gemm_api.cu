@@ -75,26 +75,36 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// Row-major [outer, inner] 16-bit matrix with row pitch ld (elements), tiles of
+// Element types of the tensors the library describes to TMA.
+enum Elem : int { kElemF16 = 0, kElemBF16 = 1, kElemF32 = 2 };
+
+Elem elem_of(gemm_dtype_t dt) { return dt == GEMM_BF16 ? kElemBF16 : kElemF16; }
+
+Elem elem_of_out(int c_type) {
+    return c_type == GEMM_OUT_F32 ? kElemF32 : (c_type == GEMM_OUT_BF16 ? kElemBF16 : kElemF16);
+}
+
+// Row-major [outer, inner] matrix with row pitch ld (elements), tiles of
 // box_outer x box_inner elements, 128-byte swizzle, zero fill out of bounds.
-bool encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* ptr, int64_t inner, int64_t outer,
+bool encode_2d(CUtensorMap* map, Elem et, const void* ptr, int64_t inner, int64_t outer,
                int64_t ld, uint32_t box_inner, uint32_t box_outer) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
+    const uint64_t esize = et == kElemF32 ? 4u : 2u;
+    const CUtensorMapDataType t = et == kElemF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : et == kElemBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(map,
-                    dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    2, const_cast<void*>(ptr), dims, strides, box, estr,
+    CUresult r = fn(map, t, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
-bool cached_encode_2d(gemm_plan_s* plan, CUtensorMap* map, gemm_dtype_t dt, const void* ptr,
+bool cached_encode_2d(gemm_plan_s* plan, CUtensorMap* map, Elem dt, const void* ptr,
                       int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
                       uint32_t box_outer) {
     std::lock_guard<std::mutex> lock(plan->cache_mu);
@@ -564,30 +574,42 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
         p.status = plan->status;
         p.timeout_ns = plan->timeout_ns;
         const bool bf16 = a.dtype == GEMM_BF16;
+        const Elem in = elem_of(a.dtype);
         // TMA descriptors: a K-major operand is read as boxes {64 k, rows}; an
         // MN-major one as boxes {64 mn, 64 k}.
         auto map_a = [&](CUtensorMap* m, uint32_t rows) {
-            return a_mn ? cached_encode_2d(plan, m, a.dtype, a.A, a.M, a.K, a.lda, dg::kSubN,
-                                           dg::kBK)
-                        : cached_encode_2d(plan, m, a.dtype, a.A, a.K, a.M, a.lda, dg::kBK, rows);
+            return a_mn ? cached_encode_2d(plan, m, in, a.A, a.M, a.K, a.lda, dg::kSubN, dg::kBK)
+                        : cached_encode_2d(plan, m, in, a.A, a.K, a.M, a.lda, dg::kBK, rows);
         };
         auto map_b = [&](CUtensorMap* m, uint32_t rows) {
-            return b_mn ? cached_encode_2d(plan, m, a.dtype, a.B, a.N, a.K, a.ldb, dg::kSubN,
-                                           dg::kBK)
-                        : cached_encode_2d(plan, m, a.dtype, a.B, a.K, a.N, a.ldb, dg::kBK, rows);
+            return b_mn ? cached_encode_2d(plan, m, in, a.B, a.N, a.K, a.ldb, dg::kSubN, dg::kBK)
+                        : cached_encode_2d(plan, m, in, a.B, a.K, a.N, a.ldb, dg::kBK, rows);
+        };
+        // C written by TMA stores of {128 bytes of columns, 32 rows} boxes when its
+        // base and pitch allow (16-byte multiples); otherwise by ordinary stores.
+        CUtensorMap mc;
+        memset(&mc, 0, sizeof(mc));
+        auto map_c = [&]() {
+            p.c_tma = 0;
+            if (!p.c_vec) return;
+            const uint32_t cols = a.c_type == GEMM_OUT_F32 ? 32u : 64u;
+            if (cached_encode_2d(plan, &mc, elem_of_out(a.c_type), a.C, a.N, a.M, a.ldc, cols, 32u))
+                p.c_tma = 1;
         };
         if (c.kernel == GEMM_KERNEL_TMA) {
             CUtensorMap ma, mb;
             if (!map_a(&ma, dg::kBM) || !map_b(&mb, static_cast<uint32_t>(c.bn)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_tma(c.bn, a_mn, b_mn, ma, mb, p,
+            map_c();
+            err = dg::launch_tma(c.bn, a_mn, b_mn, ma, mb, mc, p,
                                  dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, c.bn), c.grid, stream);
         } else if (c.kernel == GEMM_KERNEL_PAIR) {
             // Each CTA of a pair loads 128 rows of A and its half (bn / 2) of the B tile.
             CUtensorMap ma, mb;
             if (!map_a(&ma, dg::kBM) || !map_b(&mb, static_cast<uint32_t>(c.bn / 2)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_pair(c.bn, a_mn, b_mn, ma, mb, p,
+            map_c();
+            err = dg::launch_pair(c.bn, a_mn, b_mn, ma, mb, mc, p,
                                   dg::idesc_f16(bf16, a_mn, b_mn, 2 * dg::kBM, c.bn), c.grid,
                                   stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {

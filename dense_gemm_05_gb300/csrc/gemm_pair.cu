@@ -33,7 +33,8 @@ struct PairCfg {
     static constexpr int kTmemCols = 2 * BN;                    // two 128 x BN fp32 accumulators
     static constexpr int kThreads = 192;
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 8 * kNumBars + 16;
+    static constexpr int kSmemBytes =
+        1024 + STAGES * kStageBytes + kEpiSmemBytes + 8 * kNumBars + 16;
     static_assert(kBHalf % kSubN == 0, "B half must be whole 64-column sub-tiles");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -41,7 +42,8 @@ struct PairCfg {
 template <int BN, int STAGES, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
-                     const __grid_constant__ CUtensorMap mapB, const Params p,
+                     const __grid_constant__ CUtensorMap mapB,
+                     const __grid_constant__ CUtensorMap mapC, const Params p,
                      const uint32_t idesc) {
     using Cfg = PairCfg<BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
@@ -49,7 +51,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * kAStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBStageBytes);
+    uint8_t* sEpi = sB + STAGES * Cfg::kBStageBytes;      // 4 KiB per epilogue warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiSmemBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -83,6 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (warp == 5 && lane == 0) {
         prefetch_tmap(&mapA);
         prefetch_tmap(&mapB);
+        if (p.c_tma) prefetch_tmap(&mapC);
     }
     tc_fence_before();
     cluster_sync();      // both CTAs' barriers initialised and TMEM allocated
@@ -166,20 +170,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             tc_fence_after();
             const int row = tm * 256 + row_in_tile;
             const int col0 = tn * BN;
-            const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
-            const bool row_ok = row < p.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            const uint32_t tempty_peer0 = acc == 0 ? tempty0 : tempty1;
+            if (p.c_tma) {
+                epilogue_tma<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+                                 row - lane, col0, [&] {
+                                     tc_fence_before();
+                                     mbar_arrive_cluster(tempty_peer0);
+                                 });
+            } else {
+                const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
+                const bool row_ok = row < p.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
-                tmem_ld_wait(v);
-                if (c == BN / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive_cluster(acc == 0 ? tempty0 : tempty1);
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
+                    tmem_ld_wait(v);
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive_cluster(tempty_peer0);
+                    }
+                    if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
                 }
-                if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
             }
             if (++acc == 2) {
                 acc = 0;
@@ -244,6 +257,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         __syncwarp();
     }
 
+    // The TMA stores of C must have completed before the CTA's shared memory goes away.
+    if (warp >= 1 && warp <= 4 && lane == 0 && p.c_tma) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     cluster_sync();      // neither CTA leaves while its peer may still signal it
@@ -276,21 +291,22 @@ cudaError_t set_attrs() {
 }
 
 template <int BN, int STAGES, bool A_MN, bool B_MN>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p, uint32_t idesc,
-                       int grid, cudaStream_t s) {
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                       const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
     gemm_pair_kernel<BN, STAGES, A_MN, B_MN>
-        <<<grid, PairCfg<BN, STAGES>::kThreads, PairCfg<BN, STAGES>::kSmemBytes, s>>>(a, b, p,
+        <<<grid, PairCfg<BN, STAGES>::kThreads, PairCfg<BN, STAGES>::kSmemBytes, s>>>(a, b, c, p,
                                                                                    idesc);
     return cudaGetLastError();
 }
 
 template <int BN, int STAGES>
 cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
-                   const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
-    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true>(a, b, p, idesc, grid, s);
-    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false>(a, b, p, idesc, grid, s);
-    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true>(a, b, p, idesc, grid, s);
-    return launch_one<BN, STAGES, true, false>(a, b, p, idesc, grid, s);
+                   const CUtensorMap& c, const Params& p, uint32_t idesc, int grid,
+                   cudaStream_t s) {
+    if (!a_mn && b_mn) return launch_one<BN, STAGES, false, true>(a, b, c, p, idesc, grid, s);
+    if (!a_mn && !b_mn) return launch_one<BN, STAGES, false, false>(a, b, c, p, idesc, grid, s);
+    if (a_mn && b_mn) return launch_one<BN, STAGES, true, true>(a, b, c, p, idesc, grid, s);
+    return launch_one<BN, STAGES, true, false>(a, b, c, p, idesc, grid, s);
 }
 
 // All four layout instantiations have the same resources, so one query serves them.
@@ -335,11 +351,11 @@ int pair_max_clusters(int bn) {
 }
 
 cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
-                        const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                        uint32_t idesc, int grid, cudaStream_t stream) {
     if (bn == 256)
-        return launch<256, kPairStages256>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
-    return launch<128, kPairStages128>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
+        return launch<256, kPairStages256>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid, stream);
+    return launch<128, kPairStages128>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid, stream);
 }
 
 }  // namespace dg

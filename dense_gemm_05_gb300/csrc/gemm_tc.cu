@@ -36,7 +36,8 @@ struct TcCfg {
     static constexpr int kProducerWarps = GENERIC ? 4 : 1;
     static constexpr int kThreads = 32 * (1 + 4 + kProducerWarps);
     static constexpr int kNumBars = 2 * STAGES + 5;
-    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + 8 * kNumBars + 16;
+    static constexpr int kEpiBytes = GENERIC ? 0 : kEpiSmemBytes;   // TMA-store staging
+    static constexpr int kSmemBytes = 1024 + STAGES * kStageBytes + kEpiBytes + 8 * kNumBars + 16;
     static_assert(BN % kSubN == 0 && BN >= 64 && BN <= 256, "BN");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -62,12 +63,6 @@ __device__ __forceinline__ uint4 load8(const uint16_t* base, int64_t off, bool r
     r.z = e[4] | (e[5] << 16);
     r.w = e[6] | (e[7] << 16);
     return r;
-}
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
 }
 
 // One operand tile (ROWS M/N rows x 64 K) staged by 128 threads with ordinary
@@ -98,14 +93,15 @@ __device__ __forceinline__ void load_tile_generic(uint32_t dst, const uint16_t* 
     for (int i = 0; i < kPer; ++i) {
         const int q = pt + i * 128;
         const int r = q / kRowChunks, c = q % kRowChunks;
-        st_shared_v4(dst + chunk_offset<MN_MAJOR>(r, c), v[i]);
+        st_shared_v4_b32(dst + chunk_offset<MN_MAJOR>(r, c), v[i]);
     }
 }
 
 template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
-                   const __grid_constant__ CUtensorMap mapB, const Params p,
+                   const __grid_constant__ CUtensorMap mapB,
+                   const __grid_constant__ CUtensorMap mapC, const Params p,
                    const uint32_t idesc) {
     using Cfg = TcCfg<BN, STAGES, GENERIC>;
     extern __shared__ uint8_t smem_raw[];
@@ -113,7 +109,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * kAStageBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * Cfg::kBStageBytes);
+    uint8_t* sEpi = sB + STAGES * Cfg::kBStageBytes;      // TMA-store staging (not in GENERIC)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cfg::kEpiBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
@@ -145,6 +142,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
     if (!GENERIC && warp == 5 && lane == 0) {
         prefetch_tmap(&mapA);
         prefetch_tmap(&mapB);
+        if (p.c_tma) prefetch_tmap(&mapC);
     }
     tc_fence_before();
     __syncthreads();
@@ -221,20 +219,29 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
             tc_fence_after();
             const int row = tm * kBM + row_in_tile;
             const int col0 = tn * BN;
-            const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
-            const bool row_ok = row < p.M;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
+            const uint32_t tempty_bar = smem_u32(&tempty[acc]);
+            if (!GENERIC && p.c_tma) {
+                epilogue_tma<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+                                 row - lane, col0, [&] {
+                                     tc_fence_before();
+                                     mbar_arrive(tempty_bar);
+                                 });
+            } else {
+                const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
+                const bool row_ok = row < p.M;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
-                tmem_ld_wait(v);
-                if (c == BN / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(smem_u32(&tempty[acc]));
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
+                    tmem_ld_wait(v);
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(tempty_bar);
+                    }
+                    if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
                 }
-                if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
             }
             if (++acc == 2) {
                 acc = 0;
@@ -321,6 +328,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
         }
     }
 
+    // The TMA stores of C must have completed before the CTA's shared memory goes away.
+    if (!GENERIC && warp >= 1 && warp <= 4 && lane == 0 && p.c_tma) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -353,22 +362,25 @@ cudaError_t set_attrs() {
 }
 
 template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                       uint32_t idesc, int grid, cudaStream_t s) {
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                       const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
     using Cfg = TcCfg<BN, STAGES, GENERIC>;
     gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>
-        <<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, p, idesc);
+        <<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, c, p, idesc);
     return cudaGetLastError();
 }
 
 template <int BN, int STAGES, bool GENERIC>
 cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
-                   const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
-    if (!a_mn && b_mn) return launch_one<BN, STAGES, GENERIC, false, true>(a, b, p, idesc, grid, s);
+                   const CUtensorMap& c, const Params& p, uint32_t idesc, int grid,
+                   cudaStream_t s) {
+    if (!a_mn && b_mn)
+        return launch_one<BN, STAGES, GENERIC, false, true>(a, b, c, p, idesc, grid, s);
     if (!a_mn && !b_mn)
-        return launch_one<BN, STAGES, GENERIC, false, false>(a, b, p, idesc, grid, s);
-    if (a_mn && b_mn) return launch_one<BN, STAGES, GENERIC, true, true>(a, b, p, idesc, grid, s);
-    return launch_one<BN, STAGES, GENERIC, true, false>(a, b, p, idesc, grid, s);
+        return launch_one<BN, STAGES, GENERIC, false, false>(a, b, c, p, idesc, grid, s);
+    if (a_mn && b_mn)
+        return launch_one<BN, STAGES, GENERIC, true, true>(a, b, c, p, idesc, grid, s);
+    return launch_one<BN, STAGES, GENERIC, true, false>(a, b, c, p, idesc, grid, s);
 }
 }  // namespace
 
@@ -386,11 +398,13 @@ cudaError_t tma_prepare() {
 }
 
 cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
-                       const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                       cudaStream_t stream) {
+                       const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                       uint32_t idesc, int grid, cudaStream_t stream) {
     if (bn == 256)
-        return launch<256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
-    return launch<128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, p, idesc, grid, stream);
+        return launch<256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                                 stream);
+    return launch<128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                             stream);
 }
 
 int generic_smem_bytes() { return TcCfg<128, kGenericStages, true>::kSmemBytes; }
@@ -403,7 +417,8 @@ cudaError_t launch_generic(bool a_mn, bool b_mn, const Params& p, uint32_t idesc
                            cudaStream_t stream) {
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof(dummy));
-    return launch<128, kGenericStages, true>(a_mn, b_mn, dummy, dummy, p, idesc, grid, stream);
+    return launch<128, kGenericStages, true>(a_mn, b_mn, dummy, dummy, dummy, p, idesc, grid,
+                                             stream);
 }
 
 }  // namespace dg

@@ -138,6 +138,81 @@ __device__ __forceinline__ void store_c32(const Params& p, int64_t off, const ui
     }
 }
 
+// ---------------------------------------------------------------- TMA-store epilogue
+// One epilogue warp owns 32 accumulator rows.  It writes C in chunks 128 bytes
+// wide (32 fp32 or 64 16-bit columns): the chunk goes to a 4 KiB shared buffer
+// of the warp in the 128-byte-swizzled layout (row r at r * 128, 16-byte piece
+// j at piece j ^ (r % 8), which spreads the warp's rows over all banks), and
+// lane 0 stores it with one TMA box {chunk columns, 32 rows}.  TMA clips the
+// box to the M x N rectangle, so ragged edges need no masking here.
+constexpr int kEpiBufBytes = 4096;             // per epilogue warp
+constexpr int kEpiSmemBytes = 4 * kEpiBufBytes;
+
+// Columns of one chunk for the output type (128 bytes of C).
+__device__ __forceinline__ int epi_chunk_cols(int c_type) { return c_type == kOutF32 ? 32 : 64; }
+
+// lo (and hi, for 16-bit output) hold the chunk's accumulator values for this
+// lane's row: 32 fp32 bit patterns, or 64 values to be rounded to 16 bits.
+__device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorMap* mapC,
+                                                uint32_t buf, int lane, int row0, int col,
+                                                const uint32_t (&lo)[32],
+                                                const uint32_t (&hi)[32]) {
+    if (lane == 0) bulk_wait_group_read0();    // the previous chunk has left the buffer
+    __syncwarp();
+    const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
+    if (p.c_type == kOutF32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4_b32(row + static_cast<uint32_t>((j ^ (lane & 7)) << 4),
+                             make_uint4(lo[4 * j], lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t (&h)[32] = j < 4 ? lo : hi;
+            const int b = (j & 3) * 8;
+            uint4 w;
+            w.x = pack_out(__uint_as_float(h[b]), __uint_as_float(h[b + 1]), p.c_type);
+            w.y = pack_out(__uint_as_float(h[b + 2]), __uint_as_float(h[b + 3]), p.c_type);
+            w.z = pack_out(__uint_as_float(h[b + 4]), __uint_as_float(h[b + 5]), p.c_type);
+            w.w = pack_out(__uint_as_float(h[b + 6]), __uint_as_float(h[b + 7]), p.c_type);
+            st_shared_v4_b32(row + static_cast<uint32_t>((j ^ (lane & 7)) << 4), w);
+        }
+    }
+    fence_proxy_async_smem();                  // generic stores -> visible to the TMA engine
+    __syncwarp();
+    if (lane == 0 && row0 < p.M && col < p.N) {
+        tma_store_2d(mapC, buf, col, row0);
+        bulk_commit_group();
+    }
+}
+
+// The epilogue of one warp's 32 rows x BN columns of an accumulator at TMEM
+// address `taddr` (this warp's lanes), through TMA stores.  `release` is called
+// after the last TMEM load, so the MMA issuer may reuse the accumulator while
+// the final chunks are still being stored.
+template <int BN, typename Release>
+__device__ __forceinline__ void epilogue_tma(const Params& p, const CUtensorMap* mapC,
+                                             uint32_t buf, uint32_t taddr, int lane, int row0,
+                                             int col0, Release release) {
+    const int cw = epi_chunk_cols(p.c_type);
+    const int nchunks = BN / cw;
+#pragma unroll 1
+    for (int ch = 0; ch < nchunks; ++ch) {
+        uint32_t lo[32], hi[32];
+        tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(ch * cw), lo);
+        if (cw == 64) {
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(ch * cw + 32), hi);
+            tmem_ld_wait(hi);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hi[i] = 0u;
+        }
+        tmem_ld_wait(lo);
+        if (ch == nchunks - 1) release();
+        epi_store_chunk(p, mapC, buf, lane, row0, col0 + ch * cw, lo, hi);
+    }
+}
+
 // Store one accumulator value (skinny epilogue, scattered columns).
 __device__ __forceinline__ void store_c1(const Params& p, int64_t off, float x) {
     if (p.c_type == kOutF32)
