@@ -586,12 +586,15 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
                         : cached_encode_2d(plan, m, in, a.B, a.K, a.N, a.ldb, dg::kBK, rows);
         };
         // C written by TMA stores of {128 bytes of columns, 32 rows} boxes when its
-        // base and pitch allow (16-byte multiples); otherwise by ordinary stores.
+        // base, pitch and row length are 16-byte multiples; otherwise by ordinary
+        // stores.  (With a row length that is not, the right edge of C was seen
+        // to be written in whole 16-byte pieces, past column N: the guard-band
+        // tests catch that.)
         CUtensorMap mc;
         memset(&mc, 0, sizeof(mc));
         auto map_c = [&]() {
             p.c_tma = 0;
-            if (!p.c_vec) return;
+            if (!p.c_vec || (a.N * esize) % 16 != 0) return;
             const uint32_t cols = a.c_type == GEMM_OUT_F32 ? 32u : 64u;
             if (cached_encode_2d(plan, &mc, elem_of_out(a.c_type), a.C, a.N, a.M, a.ldc, cols, 32u))
                 p.c_tma = 1;
