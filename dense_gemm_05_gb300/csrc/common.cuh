@@ -26,8 +26,9 @@ struct Params {
     int32_t M, N, K;
     int32_t tiles_m, tiles_n, num_kb;
     int32_t group;          // group-major strip height (0 = row-major)
-    int32_t shares;         // skinny: equal shares of the (tile, K block) iterations
+    int32_t shares;         // skinny / pair: equal stream-K shares of the (tile, K block) iterations
     int32_t max_slots;      // skinny: partial-tile slots per output tile in the workspace
+    int32_t sk_tiles;       // pair: tiles [0, sk_tiles) are split into `shares` stream-K shares
     int32_t a_vec, b_vec;   // generic producer: 16-byte vector loads are legal
     int32_t c_vec;          // 16-byte vector stores of C are legal
     int32_t c_tma;          // the epilogue writes C with TMA stores (mapC is valid)

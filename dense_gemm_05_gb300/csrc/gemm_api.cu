@@ -50,7 +50,8 @@ struct gemm_plan_s {
 
 namespace {
 
-constexpr size_t kWorkspaceBytes = size_t(32) << 20;   // split-K partials
+constexpr size_t kWorkspaceBytes = size_t(64) << 20;   // split-K / stream-K partials
+constexpr int64_t kPairMinShareKb = 16;   // a pair stream-K share streams at least this many K blocks
 constexpr int kMaxCounters = 1 << 16;                   // output tiles that may be split
 constexpr int64_t kMaxDim = INT32_MAX - 1024;   // headroom for tile-edge arithmetic in int32
 
@@ -165,6 +166,7 @@ struct Choice {
     int split = 1;       // SKINNY: most stream-K shares that touch one tile
     int shares = 0;      // SKINNY: stream-K shares
     int max_slots = 0;   // SKINNY: workspace slots per tile
+    int sk_tiles = 0;    // PAIR: tiles in the stream-K phase
     int tiles_m = 0, tiles_n = 0, num_kb = 0;
     int units = 0;
     int grid = 0;
@@ -307,7 +309,38 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
         c->units = static_cast<int>(units);
         const int clusters = plan->pair_clusters[c->bn == 256 ? 1 : 0];
-        c->grid = 2 * (c->units < clusters ? c->units : clusters);
+        const int ncl = c->units < clusters ? c->units : clusters;
+        c->grid = 2 * ncl;
+        // Stream-K phase: when the last wave of tiles leaves at least half of the
+        // clusters idle, that partial wave is cut into one equal K share per
+        // cluster, taken first; the rest are whole tiles.  A wave that is more than
+        // half full costs less idle time than the split's slower streaming and
+        // fix-ups, and with fewer than two full waves the fix-ups have too little
+        // whole-tile work to hide behind (both measured).  If the shares would be
+        // shorter than kPairMinShareKb K blocks, one full wave joins the split
+        // tiles.  Also skipped when the partial tiles would not fit the workspace,
+        // or when forced off (split_k = 1).
+        c->sk_tiles = 0;
+        c->shares = 0;
+        if (plan->force_split != 1 && units % ncl != 0 && 2 * (units % ncl) <= ncl &&
+            units / ncl >= 2) {
+            int64_t sk = units % ncl;
+            if (sk * c->num_kb / ncl < kPairMinShareKb) sk += ncl;
+            const int64_t share_kb = sk * c->num_kb / ncl;
+            const int64_t need = int64_t(ncl) * 2 * 2 * c->bn * 128 * 4;   // [share][slot][rank]
+            if (share_kb >= kPairMinShareKb && need <= static_cast<int64_t>(plan->ws_bytes) &&
+                sk * 2 <= plan->counters_len) {
+                c->sk_tiles = static_cast<int>(sk);
+                c->shares = ncl;
+                const int64_t T = sk * c->num_kb;
+                int most = 1;
+                for (int64_t t = 0; t < sk; ++t)
+                    most = std::max<int>(most, static_cast<int>(
+                                                   dg::share_of((t + 1) * c->num_kb - 1, T, ncl) -
+                                                   dg::share_of(t * c->num_kb, T, ncl) + 1));
+                c->split = most;
+            }
+        }
         return GEMM_OK;
     } else {
         const int64_t tm = cdiv(a.M, dg::kBM);
@@ -564,6 +597,7 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
         p.group = plan->group;
         p.shares = c.shares;
         p.max_slots = c.max_slots;
+        p.sk_tiles = c.sk_tiles;
         p.a_vec = tma_ok(a.A, a.lda) ? 1 : 0;
         p.b_vec = tma_ok(a.B, a.ldb) ? 1 : 0;
         p.c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16u) == 0u && (a.ldc * esize) % 16 == 0)

@@ -39,6 +39,62 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
+// The work of one cluster, in order: first its stream-K share of the tiles
+// [0, sk_tiles) -- one contiguous run of the (tile, K block) iterations of
+// those tiles, cut into per-tile segments -- then the whole tiles
+// sk_tiles + cid, sk_tiles + cid + clusters, ...  Doing the split tiles first
+// lets their fix-ups (run by the epilogue warps) overlap the MMAs of the
+// whole tiles that follow.
+struct PairSeg {
+    int tile;
+    int kb0, kb1;     // K blocks [kb0, kb1) of the tile
+    int share;        // stream-K share, or -1 for a whole data-parallel tile
+};
+
+struct PairWalker {
+    int num_kb, ncl, total, next_dp, share;
+    int64_t t_sk, g, it, end;
+
+    __device__ PairWalker(const Params& p, int cid, int nclusters)
+        : num_kb(p.num_kb), ncl(nclusters), total(p.tiles_m * p.tiles_n), share(cid) {
+        const int sk = p.shares > 0 ? p.sk_tiles : 0;
+        t_sk = int64_t(sk) * num_kb;
+        g = p.shares;
+        if (sk > 0 && cid < g) {
+            it = share_begin(cid, t_sk, g);
+            end = share_begin(cid + 1, t_sk, g);
+        } else {
+            it = end = 0;
+        }
+        next_dp = sk + cid;
+    }
+    __device__ bool next(PairSeg& s) {
+        if (it < end) {
+            s.tile = static_cast<int>(it / num_kb);
+            s.kb0 = static_cast<int>(it - int64_t(s.tile) * num_kb);
+            const int64_t left = end - it;
+            s.kb1 = (num_kb - s.kb0 < left) ? num_kb : s.kb0 + static_cast<int>(left);
+            s.share = share;
+            it += s.kb1 - s.kb0;
+            return true;
+        }
+        if (next_dp < total) {
+            s.tile = next_dp;
+            s.kb0 = 0;
+            s.kb1 = num_kb;
+            s.share = -1;
+            next_dp += ncl;
+            return true;
+        }
+        return false;
+    }
+    // Partial-tile slot of share `sh` for `tile`: 0 if the share begins inside the
+    // tile, 1 if it ends inside it (a share holds at most these two partial tiles).
+    __device__ int slot_of(int64_t sh, int tile) const {
+        return share_begin(sh, t_sk, g) / num_kb == tile ? 0 : 1;
+    }
+};
+
 template <int BN, int STAGES, bool A_MN, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap mapA,
@@ -60,6 +116,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* drain = tempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = abort_flag + 1;   // "this CTA sums a stream-K tile"
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -77,6 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         }
         mbar_init(smem_u32(drain), 1u);
         *abort_flag = 0;
+        *last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -93,7 +151,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total = p.tiles_m * p.tiles_n;
     const int num_kb = p.num_kb;
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(nclusters_x());
@@ -106,7 +163,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = cid; t < total && !failed; t += ncl) {
+            PairWalker walk(p, cid, ncl);
+            PairSeg sg;
+            while (!failed && walk.next(sg)) {
                 if (!mbar_wait_cluster(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag,
                                        p.timeout_ns)) {
                     failed = true;
@@ -114,7 +173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, p.timeout_ns)) {
                         failed = true;
                         break;
@@ -126,7 +185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     for (int k = 0; k < kBK / 16; ++k)
                         tc_mma_f16_pair(d_tmem, operand_desc<A_MN>(a_base, k),
                                         operand_desc<B_MN>(b_base, k), idesc,
-                                        (kb | k) != 0 ? 1u : 0u);
+                                        (kb != sg.kb0 || k != 0) ? 1u : 0u);
                     tc_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -152,17 +211,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else if (warp <= 4) {
         // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;
-        const int row_in_tile = static_cast<int>(rank) * 128 + q * 32 + lane;
+        const int lrow = q * 32 + lane;          // TMEM lane = row of this CTA's half tile
+        const int row_in_tile = static_cast<int>(rank) * 128 + lrow;
+        const int et = threadIdx.x - 32;         // 0..127
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         const uint32_t tempty1 = mapa_shared(smem_u32(&tempty[1]), 0);
+        const uint32_t ebuf = smem_u32(sEpi) + (warp - 1) * kEpiBufBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = cid; t < total; t += ncl) {
+        PairWalker walk(p, cid, ncl);
+        PairSeg sg;
+        while (walk.next(sg)) {
             int tm, tn;
-            tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+            tile_coord32(sg.tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
             const bool ok =
                 mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
-            if (!__all_sync(0xffffffffu, ok)) {
+            // One decision for all 128 epilogue threads: they share named barriers below.
+            if (!named_bar_and(1, 128, ok)) {
                 *abort_flag = 1;
                 if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
                 break;
@@ -173,7 +238,149 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             const uint32_t tempty_peer0 = acc == 0 ? tempty0 : tempty1;
-            if (p.c_tma) {
+            if (sg.kb0 != 0 || sg.kb1 != num_kb) {
+                // ---- a stream-K partial tile.  The shares [first, last] that cover it
+                // each hold a partial sum; C = ((p_first + p_first+1) + ...) + p_last.
+                // Partials live in the workspace as [share][slot][rank][BN/4][128][4]
+                // floats: one float4 per (4 columns, row), so a warp moves 512
+                // contiguous bytes per access.  Work goes 64 columns per round.
+                const int64_t first = share_of(int64_t(sg.tile) * num_kb, walk.t_sk, walk.g);
+                const int64_t last = share_of(int64_t(sg.tile + 1) * num_kb - 1, walk.t_sk, walk.g);
+                const int nparts = static_cast<int>(last - first + 1);
+                int* counter = p.counters + sg.tile * 2 + static_cast<int>(rank);
+                auto part_of = [&](int64_t sh) -> float4* {
+                    return reinterpret_cast<float4*>(
+                        p.ws + ((sh * 2 + walk.slot_of(sh, sg.tile)) * 2 + rank) * (BN * 128));
+                };
+                auto own_round = [&](int c0, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c0), lo);
+                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c0 + 32), hi);
+                    tmem_ld_wait(lo);
+                    if (c0 + 64 == BN) {
+                        tc_fence_before();
+                        mbar_arrive_cluster(tempty_peer0);
+                    }
+                };
+                auto load_round = [&](const float4* src, int c0, float4 (&t)[16]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) t[j] = __ldcg(src + (c0 / 4 + j) * 128 + lrow);
+                };
+                auto store_round = [&](int c0, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
+                    if (p.c_tma) {
+                        if (p.c_type == kOutF32) {
+                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
+                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0 + 32, hi,
+                                            lo);
+                        } else {
+                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
+                        }
+                    } else if (row < p.M) {
+                        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0 + c0;
+                        store_c32(p, off, lo, p.N - (col0 + c0));
+                        store_c32(p, off + 32, hi, p.N - (col0 + c0 + 32));
+                    }
+                };
+                // Sum one 64-column round of the tile in share order.  fold: this
+                // share's own partial comes straight from TMEM (it never published).
+                // Sum one 64-column round of the tile in share order.  fold: this
+                // share's own partial comes straight from TMEM (it never published).
+                auto sum_round = [&](int c0, bool fold, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
+                    float4 s4[16];
+#pragma unroll 1
+                    for (int64_t sh = first; sh <= last; ++sh) {
+                        float4 t[16];
+                        if (fold && sh == sg.share) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t v[32];
+                                tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c0 + 32 * h), v);
+                                tmem_ld_wait(v);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    t[8 * h + j] = make_float4(
+                                        __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                            }
+                            if (c0 + 64 == BN) {
+                                tc_fence_before();
+                                mbar_arrive_cluster(tempty_peer0);
+                            }
+                        } else {
+                            load_round(part_of(sh), c0, t);
+                        }
+                        if (sh == first) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) s4[j] = t[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                s4[j].x += t[j].x;
+                                s4[j].y += t[j].y;
+                                s4[j].z += t[j].z;
+                                s4[j].w += t[j].w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        lo[4 * j] = __float_as_uint(s4[j].x);
+                        lo[4 * j + 1] = __float_as_uint(s4[j].y);
+                        lo[4 * j + 2] = __float_as_uint(s4[j].z);
+                        lo[4 * j + 3] = __float_as_uint(s4[j].w);
+                        hi[4 * j] = __float_as_uint(s4[j + 8].x);
+                        hi[4 * j + 1] = __float_as_uint(s4[j + 8].y);
+                        hi[4 * j + 2] = __float_as_uint(s4[j + 8].z);
+                        hi[4 * j + 3] = __float_as_uint(s4[j + 8].w);
+                    }
+                };
+                // Fold: when every other share of the tile has already published, this
+                // share adds their partials to its accumulator without publishing its
+                // own.  Both ways sum in share order, so the bits are the same.
+                if (et == 0) *last_flag = (load_acquire_gpu(counter) == nparts - 1) ? 2 : 0;
+                named_bar_sync(1, 128);
+                if (*last_flag == 2) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 64) {
+                        uint32_t lo[32], hi[32];
+                        sum_round(c0, true, lo, hi);
+                        store_round(c0, lo, hi);
+                    }
+                    if (et == 0) store_relaxed_gpu(counter, 0);
+                } else {
+                    // Publish this share's partial, then count it in; the share that
+                    // arrives last sums every partial.
+                    float4* mine = part_of(sg.share);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < BN; c0 += 64) {
+                        uint32_t lo[32], hi[32];
+                        own_round(c0, lo, hi);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            __stcg(mine + (c0 / 4 + j) * 128 + lrow,
+                                   make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
+                                               __uint_as_float(lo[4 * j + 2]), __uint_as_float(lo[4 * j + 3])));
+                            __stcg(mine + (c0 / 4 + j + 8) * 128 + lrow,
+                                   make_float4(__uint_as_float(hi[4 * j]), __uint_as_float(hi[4 * j + 1]),
+                                               __uint_as_float(hi[4 * j + 2]), __uint_as_float(hi[4 * j + 3])));
+                        }
+                    }
+                    named_bar_sync(1, 128);
+                    if (et == 0) {
+                        const int old = atomic_add_acq_rel_gpu(counter, 1);
+                        *last_flag = (old == nparts - 1) ? 1 : 0;
+                    }
+                    named_bar_sync(1, 128);
+                    if (*last_flag) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < BN; c0 += 64) {
+                            uint32_t lo[32], hi[32];
+                            sum_round(c0, false, lo, hi);
+                            store_round(c0, lo, hi);
+                        }
+                        if (et == 0) store_relaxed_gpu(counter, 0);
+                    }
+                }
+            } else if (p.c_tma) {
                 epilogue_tma<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
@@ -205,12 +412,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             bool failed = false;
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = cid; t < total && !failed; t += ncl) {
+            PairWalker walk(p, cid, ncl);
+            PairSeg sg;
+            while (!failed && walk.next(sg)) {
                 int tm, tn;
-                tile_coord32(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+                tile_coord32(sg.tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
                 const int a_row = tm * 256 + static_cast<int>(rank) * 128;
                 const int b_col = tn * BN + static_cast<int>(rank) * Cfg::kBHalf;
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag,
                                    p.timeout_ns)) {
                         failed = true;

@@ -106,6 +106,12 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
     return old;
 }
 
+__device__ __forceinline__ int load_acquire_gpu(const int* addr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void store_relaxed_gpu(int* addr, int v) {
     asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }

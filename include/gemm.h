@@ -101,7 +101,8 @@ typedef struct {
     int32_t cluster;      /* CTAs per cluster */
     int32_t group;        /* group-major strip height in tiles (0 = row-major order) */
     int32_t tiles;        /* work units: output tiles, or stream-K shares for SKINNY */
-    int32_t shares;       /* SKINNY: equal contiguous shares of the (tile, K block) iterations */
+    int32_t shares;       /* SKINNY: equal contiguous shares of the (tile, K block) iterations;
+                             PAIR: shares (one per cluster) of the stream-K phase, 0 = none */
 } gemm_config_t;
 
 /*
@@ -188,8 +189,10 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  * gemm_kernel_t of TMA, GENERIC, SKINNY or PAIR; 0 = automatic choice),
  * `split_k` stream-K shares for SKINNY -- the (tile, K block) iterations of
  * all tiles are cut into that many equal contiguous runs, one CTA each
- * (0 = automatic) -- and `block_n` tile columns for
- * TMA/PAIR (128 or 256; 0 = automatic).  For tests and tuning.
+ * (0 = automatic); for PAIR, `split_k` = 1 turns off the stream-K phase that
+ * otherwise splits the last, partial wave of pair tiles (plus one full wave)
+ * by K across all clusters (any other value = automatic) -- and `block_n`
+ * tile columns for TMA/PAIR (128 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
  * arguments (e.g. TMA with a leading dimension that is not a multiple of 8).
  * Errors: INVALID_ARG (null plan, unknown kernel, negative split, bad block_n).

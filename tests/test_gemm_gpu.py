@@ -226,6 +226,85 @@ def test_pair_tile_order_does_not_change_bits(plan, group):
     assert np.array_equal(base, got)
 
 
+# ---------------------------------------------------------------- pair stream-K phase
+
+def pair_sk_expected(cfg, M, N, K):
+    """Stream-K shares the pair kernel should use, from the grid the plan reports:
+    one per cluster when the last wave of tiles is at most half full and at least
+    two full waves precede it; the split covers that partial wave, plus one full
+    wave when the shares would otherwise be shorter than 16 K blocks."""
+    ncl = cfg["grid"] // 2
+    units = -(-M // 256) * -(-N // cfg["block_n"])
+    num_kb = -(-K // 64)
+    rem = units % ncl
+    if rem == 0 or 2 * rem > ncl or units // ncl < 2:
+        return 0
+    sk = rem if rem * num_kb // ncl >= 16 else rem + ncl
+    return ncl if sk * num_kb // ncl >= 16 else 0
+
+
+def query_pair(plan, A, B, M, N, K, block_n, split=0):
+    dev = torch.device("cuda:0")
+    c = torch.empty(M, N, dtype=torch.float32, device=dev)
+    plan.force(g.GEMM_KERNEL_PAIR, split, block_n)
+    try:
+        return plan.query(A.to(dev), B.to(dev), c, M, N, K)
+    finally:
+        plan.force(0, 0, 0)
+
+
+# (M, K, N, dtype, block_n), with 76 clusters: 160 tiles of 256 columns over
+# K = 1024 (8 + 76 split tiles, two shares per split tile); 176 tiles of 128
+# columns over K = 4096 (the 24 tiles of the partial wave, each split over 4-5
+# shares); 190 tiles of 256 columns over K = 2048 (38 split tiles, 2-3 shares
+# each).
+SK_EXACT = [(2048, 1024, 5120, "bf16", 256), (2048, 4096, 2816, "f16", 128),
+            (2560, 2048, 4864, "bf16", 256)]
+
+
+@pytest.mark.parametrize("M,K,N,dtype,block_n", SK_EXACT)
+def test_pair_stream_k_integer_exact(plan, M, K, N, dtype, block_n):
+    A, B = int_inputs(M, K, N, dtype, seed=M + K + N + 1)
+    cfg = query_pair(plan, A, B, M, N, K, block_n)
+    expected = pair_sk_expected(cfg, M, N, K)
+    assert cfg["shares"] == expected, cfg
+    if expected == 0:
+        pytest.skip(f"{cfg['grid'] // 2} clusters leave no partial wave for this shape")
+    assert cfg["split_k"] >= 2, cfg
+    got = run(plan, A, B, M, N, K, ldc=N + 8, kernel=g.GEMM_KERNEL_PAIR, block_n=block_n)
+    assert_guards(got, M, N)
+    ref = oracle.gemm(A, B)
+    assert np.array_equal(got[:M, :N], ref), f"max diff {np.abs(got[:M, :N] - ref).max()}"
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+def test_pair_stream_k_ragged(plan, block_n):
+    """Ragged M, N and K in the split tiles: 10 x 17 (or 33) tiles, K = 1000."""
+    M, K, N = 2500, 1000, 4100
+    lda, ldb = 1000, 4104
+    A, B = workloads.custom(M, K, N, "bf16", seed=31 + block_n, dist="normal", lda=lda, ldb=ldb)
+    cfg = query_pair(plan, A, B, M, N, K, block_n)
+    assert cfg["shares"] == pair_sk_expected(cfg, M, N, K), cfg
+    got = run(plan, A, B, M, N, K, ldc=N + 5, kernel=g.GEMM_KERNEL_PAIR, block_n=block_n)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"pair stream-K {M}x{N}x{K} bn={block_n}")
+
+
+def test_pair_stream_k_deterministic_and_ablation(plan):
+    """Fixed-order fix-up: repeated runs agree bit for bit; split_k = 1 turns the
+    phase off and still matches the oracle."""
+    M, K, N = 2048, 2048, 5120
+    A, B = workloads.custom(M, K, N, "bf16", seed=44, dist="normal")
+    assert query_pair(plan, A, B, M, N, K, 256)["shares"] > 0
+    assert query_pair(plan, A, B, M, N, K, 256, split=1)["shares"] == 0
+    got1 = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_PAIR, block_n=256)
+    got2 = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_PAIR, block_n=256)
+    assert np.array_equal(got1, got2), "stream-K result changed between runs"
+    off = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_PAIR, split=1, block_n=256)
+    assert_close(got1[:M, :N], A, B, M, N, K, "pair stream-K on")
+    assert_close(off[:M, :N], A, B, M, N, K, "pair stream-K off")
+
+
 # ---------------------------------------------------------------- exactness
 
 def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):

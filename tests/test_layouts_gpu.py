@@ -136,6 +136,25 @@ def test_integer_exact_every_layout_and_output(plan, out, op_a, op_b):
         assert np.array_equal(got[:M, :N], ref), f"kernel {kernel}"
 
 
+@pytest.mark.parametrize("out", [g.GEMM_OUT_F32, g.GEMM_OUT_F16, g.GEMM_OUT_BF16])
+@pytest.mark.parametrize("op_a,op_b", [(N_, N_), (T_, T_)])
+@pytest.mark.parametrize("M,K,N", [(2048, 1024, 5120), (2560, 2048, 4864)])
+def test_pair_stream_k_layouts_and_outputs(plan, out, op_a, op_b, M, K, N):
+    """Pair tiles with a stream-K phase (160 tiles of 256 columns, two shares per
+    split tile; 190 tiles, 2-3 shares per split tile): the fix-up
+    writes every output type and reads every operand layout.  Integer inputs:
+    the fp32 sums stay below 2^24 and are exact, so each output is the oracle's
+    value rounded once (to nearest even) to the output type."""
+    gen = torch.Generator().manual_seed(91)
+    A = torch.randint(-4, 5, (M, K), generator=gen).to(torch.bfloat16)
+    B = torch.randint(-4, 5, (K, N), generator=gen).to(torch.bfloat16)
+    got = run_ex(plan, stored(A, op_a), stored(B, op_b), op_a, op_b, M, N, K, out,
+                 kernel=g.GEMM_KERNEL_PAIR, expect=g.GEMM_KERNEL_PAIR)
+    assert np.all(got[M:] == SENTINEL)
+    ref = torch.from_numpy(oracle.gemm(A, B)).float().to(TORCH_OUT[out]).double().numpy()
+    assert np.array_equal(got[:M, :N], ref)
+
+
 def test_matmul_accepts_transposed_views(plan):
     """Plan.matmul on torch views: x @ w.t() with w stored [out, in] (a linear layer)."""
     M, K, N = 256, 512, 384
