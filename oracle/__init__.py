@@ -12,6 +12,9 @@ Contents
     kernels in Triton: Vector Add, Softmax, MatMul").
   * ``schedule``: the tile-grid, mask and program-order arithmetic that the
     pages print (pure Python).
+  * ``softmax``: row-wise softmax in binary64 (numpy), the five steps of
+    section 2.3 of "Writing GPU kernels in Triton: Vector Add, Softmax, MatMul";
+    pinned by ``tests/test_softmax_oracle.py``.
 
 Pinned by ``tests/test_oracle.py`` against the pages' worked examples, closed
 forms (identity, zero, small-integer products), bit-pattern decoding by numpy

@@ -105,3 +105,54 @@ def custom(M: int, K: int, N: int, dtype: str, seed: int, dist: str = "uniform",
     """Ad-hoc shape with the same recipe (used by the ragged sweeps and edge cases)."""
     w = Workload(f"custom{M}x{K}x{N}", M, K, N, dtype, dist, dist, scale, scale, seed)
     return make_inputs(w, lda=lda, ldb=ldb)
+
+
+# ---------------------------------------------------------------- row-wise softmax
+#
+# Recipe: one CPU ``torch.Generator`` seeded with the workload's seed draws the
+# M x N float32 matrix with ``torch.randn`` (the distribution of the softmax
+# chapter's demo input, whose scores stand in for QK^T / sqrt(d) rows), times
+# ``scale``.  A padded leading dimension is filled with NaN beyond column N.
+
+@dataclasses.dataclass(frozen=True)
+class RowsWorkload:
+    name: str
+    M: int
+    N: int
+    scale: float
+    seed: int
+    note: str = ""
+
+    @property
+    def bytes_alg(self) -> int:
+        """One read of X and one write of Y, 4 B per element each."""
+        return 8 * self.M * self.N
+
+
+SOFTMAX_WORKLOADS: dict[str, RowsWorkload] = {
+    w.name: w
+    for w in [
+        RowsWorkload("softmax128x1000_f32", 128, 1000, 1.0, 20,
+                     "the softmax chapter's demo shape: 128 rows of 1000, N(0,1)"),
+        RowsWorkload("softmax65536x1000_f32", 65536, 1000, 1.0, 21,
+                     "65536 rows of the demo's length: 262 MB in, 262 MB out (> L2)"),
+        RowsWorkload("softmax4096x32768_f32", 4096, 32768, 1.0, 22,
+                     "long rows (tens of thousands of elements): 537 MB in, 537 MB out"),
+    ]
+}
+
+
+def make_rows(w: RowsWorkload | str, *, ld: int | None = None) -> torch.Tensor:
+    """CPU float32 tensor stored as (M, ld) with the workload's values in the first N columns."""
+    if isinstance(w, str):
+        w = SOFTMAX_WORKLOADS[w]
+    g = torch.Generator().manual_seed(w.seed)
+    x = torch.randn(w.M, w.N, generator=g, dtype=torch.float32)
+    if w.scale != 1.0:
+        x = x * torch.tensor(w.scale, dtype=torch.float32)
+    return _place(x, ld, torch.float32)
+
+
+def custom_rows(M: int, N: int, seed: int, scale: float = 1.0, ld: int | None = None) -> torch.Tensor:
+    """Ad-hoc softmax input with the same recipe."""
+    return make_rows(RowsWorkload(f"rows{M}x{N}", M, N, scale, seed), ld=ld)
