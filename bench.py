@@ -428,6 +428,38 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
                    "shares": cfg["shares"], "host_us_per_call": host_us,
                    "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                    "bytes_alg": w.bytes_alg}
+    del a, bs, c
+    out.update(softmax_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
+    return out
+
+
+def softmax_secondary(torch, g, workloads, dev, stream, peaks, peak_src) -> dict:
+    """Row-wise softmax (the next-ranked row of the hot-path table): HBM-bound, one
+    read and one write of fp32 per element.  Inputs and outputs exceed L2 (no
+    flush needed); events around every launch, median of 30."""
+    out = {}
+    for name in ("softmax65536x1000_f32", "softmax4096x32768_f32"):
+        w = workloads.SOFTMAX_WORKLOADS[name]
+        x = workloads.make_rows(w).to(dev)
+        y = torch.empty_like(x)
+        cfg = g.softmax_rows_query(x.data_ptr(), w.N, y.data_ptr(), w.N, w.M, w.N)
+        call = lambda: g.softmax(x, out=y, stream=stream)  # noqa: E731
+        time_launches(torch, None, [call] * 5, stream)
+        ms = sorted(time_launches(torch, None, [call] * 30, stream))
+        t = ms[len(ms) // 2] / 1e3
+        gbs = w.bytes_alg / t / 1e9
+        with torch.cuda.stream(stream):
+            ref_call = lambda: torch.softmax(x, dim=1)  # noqa: E731
+            time_launches(torch, None, [ref_call] * 3, stream)
+            tms = sorted(time_launches(torch, None, [ref_call] * 15, stream))
+        out[name] = {"gbs": gbs, "pct_of_hbm_peak": 100 * gbs / peaks["hbm_gbs"],
+                     "median_us": t * 1e6, "bytes_alg": w.bytes_alg,
+                     "l2": f"X and Y {w.bytes_alg / 2e6:.0f} MB each (> L2), no flush",
+                     "kernel": f"softmax {cfg['path_name']} path, {cfg['threads_per_row']} threads "
+                               f"per row, grid {cfg['grid']}" + (", staged" if cfg["staged"] else ""),
+                     "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
+                     "torch_softmax_gbs": w.bytes_alg / (tms[len(tms) // 2] / 1e3) / 1e9}
+        del x, y
     return out
 
 
@@ -496,9 +528,20 @@ def run_case(args) -> None:
     import dense_gemm_05_gb300 as g
     import workloads
     g.build()
+    dev = torch.device("cuda:0")
+    if args.case in workloads.SOFTMAX_WORKLOADS:
+        w = workloads.SOFTMAX_WORKLOADS[args.case]
+        x = workloads.make_rows(w).to(dev)
+        y = torch.empty_like(x)
+        cfg = g.softmax_rows_query(x.data_ptr(), w.N, y.data_ptr(), w.N, w.M, w.N)
+        torch.cuda.synchronize()
+        for _ in range(args.launches):
+            g.softmax(x, out=y)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": w.name, "launches": args.launches, "softmax": cfg}), flush=True)
+        return
     w = workloads.WORKLOADS[args.case]
     A, B = workloads.make_inputs(w)
-    dev = torch.device("cuda:0")
     a, b = A.to(dev), B.to(dev)
     c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
     plan = g.Plan(0)
@@ -521,7 +564,7 @@ def main() -> None:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    help="profiling: run only this workload's GEMM --launches times")
+                    help="profiling: run only this workload's GEMM (or softmax) --launches times")
     ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
     if args.case:

@@ -10,7 +10,8 @@ binding functions raises.
              GEMM_BF16, torch.cuda.current_stream().cuda_stream)
     gemm_plan_destroy(plan)
 
-``matmul(a, b)`` wraps the same calls for 2-D torch tensors.
+``matmul(a, b)`` wraps the same calls for 2-D torch tensors; ``softmax(x)``
+wraps the row-wise softmax of ``include/softmax.h``.
 """
 from __future__ import annotations
 
@@ -49,7 +50,14 @@ KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 
 #: Every function the header declares (checked by the tests against the library's exports).
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
-                 "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex")
+                 "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
+                 "softmax_rows", "softmax_rows_query")
+
+SOFTMAX_PATH_NONE = 0
+SOFTMAX_PATH_WARP = 1
+SOFTMAX_PATH_CTA = 2
+SOFTMAX_PATH_STREAM = 3
+SOFTMAX_PATH_NAMES = {0: "none", 1: "warp", 2: "cta", 3: "stream"}
 
 #: Limits of gemm_run_noalloc (mirrors of the header's macros).
 GEMM_NOALLOC_MAX_M = 64
@@ -71,6 +79,17 @@ class GemmConfig(ctypes.Structure):
     def as_dict(self) -> dict:
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}
         d["kernel_name"] = KERNEL_NAMES.get(d["kernel"], "?")
+        return d
+
+
+class SoftmaxConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("path", "threads_per_row", "elems_per_thread", "vec", "rows_per_cta", "block",
+                 "grid", "staged", "slots")]
+
+    def as_dict(self) -> dict:
+        d = {n: int(getattr(self, n)) for n, _ in self._fields_}
+        d["path_name"] = SOFTMAX_PATH_NAMES.get(d["path"], "?")
         return d
 
 
@@ -118,6 +137,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_query_ex.argtypes = [vp, i32, i32, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64,
                                     i32, ctypes.POINTER(GemmConfig)]
         L.gemm_query_ex.restype = i32
+        L.softmax_rows.argtypes = [vp, i64, vp, i64, i64, i64, vp]
+        L.softmax_rows.restype = i32
+        L.softmax_rows_query.argtypes = [vp, i64, vp, i64, i64, i64, ctypes.POINTER(SoftmaxConfig)]
+        L.softmax_rows_query.restype = i32
         _lib = L
         return L
 
@@ -198,6 +221,19 @@ def gemm_run_noalloc(A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M: in
     """Small-M C = A @ B on the current device with no plan and no allocation (for
     callers that cannot allocate device memory); returns the gemm_status_t code."""
     return int(lib().gemm_run_noalloc(A, lda, B, ldb, C, ldc, M, N, K, dtype, stream))
+
+
+def softmax_rows(X: int, ldx: int, Y: int, ldy: int, M: int, N: int, stream: int = 0) -> int:
+    """Y = row-wise softmax of X (fp32, raw pointers as ints) on `stream`; returns the status."""
+    return int(lib().softmax_rows(X, ldx, Y, ldy, M, N, stream))
+
+
+def softmax_rows_query(X: int, ldx: int, Y: int, ldy: int, M: int, N: int) -> dict:
+    cfg = SoftmaxConfig()
+    st = lib().softmax_rows_query(X, ldx, Y, ldy, M, N, ctypes.byref(cfg))
+    if st != GEMM_OK:
+        raise GemmError(st, "softmax_rows_query")
+    return cfg.as_dict()
 
 
 # ------------------------------------------------------------------ torch convenience
@@ -336,3 +372,29 @@ def matmul(a, b, out_dtype=None):
     if dev not in _default_plans:
         _default_plans[dev] = Plan(dev)
     return _default_plans[dev].matmul(a, b, out_dtype)
+
+
+def _rows_view(t, what):
+    import torch
+    if t.dtype != torch.float32:
+        raise TypeError(f"{what} must be float32, got {t.dtype}")
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError(f"{what} must be 2-D with unit inner stride (row-major)")
+    return max(t.stride(0), t.size(1)) if t.size(0) > 1 else max(t.size(1), 1)
+
+
+def softmax(x, out=None, stream=None):
+    """Row-wise softmax of a 2-D float32 CUDA tensor (each row on its own); `out`
+    may be `x` itself (in place).  Raises GemmError on failure."""
+    import torch
+    ldx = _rows_view(x, "x")
+    if out is None:
+        out = torch.empty_like(x, memory_format=torch.contiguous_format)
+    if tuple(out.shape) != tuple(x.shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, x {tuple(x.shape)}")
+    ldy = _rows_view(out, "out")
+    s = (torch.cuda.current_stream(x.device) if stream is None else stream).cuda_stream
+    st = softmax_rows(x.data_ptr(), ldx, out.data_ptr(), ldy, x.size(0), x.size(1), s)
+    if st != GEMM_OK:
+        raise GemmError(st, "softmax_rows")
+    return out

@@ -23,7 +23,8 @@ def declared_functions():
     for fn in os.listdir(os.path.join(ROOT, "include")):
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
-            names += [n for n in re.findall(r"GEMM_API\s+[\w\s\*]*?\b(\w+)\s*\(", text) if n.startswith("gemm_")]
+            names += [n for n in re.findall(r"GEMM_API\s+[\w\s\*]*?\b(\w+)\s*\(", text)
+                      if not n.startswith("__")]
     return names
 
 
@@ -77,3 +78,22 @@ def test_plan_create_without_a_usable_gpu_fails_cleanly():
     h = ctypes.c_void_p()
     st = g.lib().gemm_plan_create(ctypes.byref(h), 0)
     assert st in (g.GEMM_ERR_CUDA, g.GEMM_ERR_INVALID_ARG) and not h.value
+
+
+def test_softmax_argument_checks_need_no_gpu():
+    """Argument errors and empty shapes are decided before any CUDA call."""
+    sr = g.softmax_rows
+    assert sr(0, 1, 0, 1, -1, 4) == g.GEMM_ERR_INVALID_ARG          # negative M
+    assert sr(0, 1, 0, 1, 4, -1) == g.GEMM_ERR_INVALID_ARG          # negative N
+    assert sr(0, 8, 0, 8, 0, 8) == g.GEMM_OK                        # M == 0: no-op
+    assert sr(0, 8, 0, 8, 8, 0) == g.GEMM_OK                        # N == 0: no-op
+    assert sr(0, 8, 4096, 8, 2, 8) == g.GEMM_ERR_INVALID_ARG        # null X
+    assert sr(4096, 7, 65536, 8, 2, 8) == g.GEMM_ERR_INVALID_ARG    # ldx < N
+    assert sr(4096, 8, 65536, 7, 2, 8) == g.GEMM_ERR_INVALID_ARG    # ldy < N
+    assert sr(4098, 8, 65536, 8, 2, 8) == g.GEMM_ERR_INVALID_ARG    # X not 4-byte aligned
+    assert sr(4096, 8, 4096 + 16, 8, 2, 8) == g.GEMM_ERR_INVALID_ARG  # partial overlap
+    assert sr(4096, 8, 4096, 16, 2, 8) == g.GEMM_ERR_INVALID_ARG    # same start, other pitch
+    assert sr(4096, 1 << 31, 1 << 40, 1 << 31, 2, 1 << 31) == g.GEMM_ERR_UNSUPPORTED  # N > 2^31-1
+    with pytest.raises(g.GemmError):
+        g.softmax_rows_query(0, 1, 0, 1, -1, 1)
+    assert g.softmax_rows_query(0, 1, 0, 1, 0, 5)["path_name"] == "none"
