@@ -15,6 +15,10 @@ Contents
   * ``softmax``: row-wise softmax in binary64 (numpy), the five steps of
     section 2.3 of "Writing GPU kernels in Triton: Vector Add, Softmax, MatMul";
     pinned by ``tests/test_softmax_oracle.py``.
+  * ``attention``: attention forward O = softmax(Q K^T / sqrt(d) [+ causal
+    mask]) V in binary64 (numpy), the result the Flash Attention section of
+    "How to hand-write Triton kernels for matmul and Flash Attention" reaches;
+    pinned by ``tests/test_attention_oracle.py``.
 
 Pinned by ``tests/test_oracle.py`` against the pages' worked examples, closed
 forms (identity, zero, small-integer products), bit-pattern decoding by numpy

@@ -156,3 +156,65 @@ def make_rows(w: RowsWorkload | str, *, ld: int | None = None) -> torch.Tensor:
 def custom_rows(M: int, N: int, seed: int, scale: float = 1.0, ld: int | None = None) -> torch.Tensor:
     """Ad-hoc softmax input with the same recipe."""
     return make_rows(RowsWorkload(f"rows{M}x{N}", M, N, scale, seed), ld=ld)
+
+
+# ---------------------------------------------------------------- attention forward
+#
+# Recipe: one CPU ``torch.Generator`` per workload draws Q, then K, then V, each
+# [BH, seq, d] float32 ``torch.randn`` (unit-variance rows, so Q K^T / sqrt(d)
+# has unit-variance scores), rounded to fp16/bf16 to nearest-even.  BH
+# independent heads (e.g. batch 2 x 8 heads for BH = 16) share the layout
+# [BH, seq, d], row-major, d contiguous.
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    BH: int
+    seq: int
+    d: int
+    dtype: str
+    causal: bool
+    seed: int
+    note: str = ""
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+
+    @property
+    def flops(self) -> int:
+        """2 flops per multiply-add of Q K^T and of P V, over the (query, key)
+        pairs the mask keeps: seq^2 pairs, or seq (seq + 1) / 2 when causal."""
+        pairs = self.seq * (self.seq + 1) // 2 if self.causal else self.seq * self.seq
+        return 4 * self.BH * pairs * self.d
+
+
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {
+    w.name: w
+    for w in [
+        AttnWorkload("attn_bh2_s256_d64_f16_causal", 2, 256, 64, "f16", True, 30,
+                     "small causal case: 2 heads of 256 x 64"),
+        AttnWorkload("attn_bh2_s1000_d64_bf16", 2, 1000, 64, "bf16", False, 31,
+                     "ragged sequence (1000 = 7 x 128 + 104), no mask"),
+        AttnWorkload("attn_bh16_s8192_d64_bf16_causal", 16, 8192, 64, "bf16", True, 32,
+                     "the section's sequence length 8192 and head dimension 64, causal, 16 heads"),
+        AttnWorkload("attn_bh16_s8192_d64_bf16", 16, 8192, 64, "bf16", False, 33,
+                     "the same without the mask"),
+    ]
+}
+
+
+def make_qkv(w: AttnWorkload | str) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """CPU tensors Q, K, V of shape [BH, seq, d] in the workload's dtype."""
+    if isinstance(w, str):
+        w = ATTN_WORKLOADS[w]
+    g = torch.Generator().manual_seed(w.seed)
+    out = []
+    for _ in range(3):
+        out.append(torch.randn(w.BH, w.seq, w.d, generator=g, dtype=torch.float32).to(w.torch_dtype))
+    return out[0], out[1], out[2]
+
+
+def custom_qkv(BH: int, seq: int, d: int, dtype: str, seed: int, causal: bool = False):
+    """Ad-hoc attention input with the same recipe."""
+    return make_qkv(AttnWorkload(f"attn{BH}x{seq}x{d}", BH, seq, d, dtype, causal, seed))
