@@ -51,7 +51,7 @@ KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
-                 "softmax_rows", "softmax_rows_query")
+                 "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query")
 
 SOFTMAX_PATH_NONE = 0
 SOFTMAX_PATH_WARP = 1
@@ -91,6 +91,14 @@ class SoftmaxConfig(ctypes.Structure):
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}
         d["path_name"] = SOFTMAX_PATH_NAMES.get(d["path"], "?")
         return d
+
+
+class AttentionConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("block_q", "block_kv", "head_dim", "stages", "grid_x", "grid_y", "causal")]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
 
 
 _lock = threading.Lock()
@@ -141,6 +149,12 @@ def lib() -> ctypes.CDLL:
         L.softmax_rows.restype = i32
         L.softmax_rows_query.argtypes = [vp, i64, vp, i64, i64, i64, ctypes.POINTER(SoftmaxConfig)]
         L.softmax_rows_query.restype = i32
+        L.attention_fwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32,
+                                    i32, vp]
+        L.attention_fwd.restype = i32
+        L.attention_fwd_query.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32,
+                                          i32, i32, ctypes.POINTER(AttentionConfig)]
+        L.attention_fwd_query.restype = i32
         _lib = L
         return L
 
@@ -233,6 +247,25 @@ def softmax_rows_query(X: int, ldx: int, Y: int, ldy: int, M: int, N: int) -> di
     st = lib().softmax_rows_query(X, ldx, Y, ldy, M, N, ctypes.byref(cfg))
     if st != GEMM_OK:
         raise GemmError(st, "softmax_rows_query")
+    return cfg.as_dict()
+
+
+def attention_fwd(Q: int, K: int, V: int, O: int, BH: int, seq: int, d: int, ld: int, hs: int,
+                  ldo: int, hso: int, causal: int, dtype: int, out_type: int,
+                  stream: int = 0) -> int:
+    """O = softmax(Q K^T / sqrt(d) [causal]) V per head (raw pointers); returns the status."""
+    return int(lib().attention_fwd(Q, K, V, O, BH, seq, d, ld, hs, ldo, hso, causal, dtype,
+                                   out_type, stream))
+
+
+def attention_fwd_query(Q: int, K: int, V: int, O: int, BH: int, seq: int, d: int, ld: int,
+                        hs: int, ldo: int, hso: int, causal: int, dtype: int,
+                        out_type: int) -> dict:
+    cfg = AttentionConfig()
+    st = lib().attention_fwd_query(Q, K, V, O, BH, seq, d, ld, hs, ldo, hso, causal, dtype,
+                                   out_type, ctypes.byref(cfg))
+    if st != GEMM_OK:
+        raise GemmError(st, "attention_fwd_query")
     return cfg.as_dict()
 
 
@@ -397,4 +430,36 @@ def softmax(x, out=None, stream=None):
     st = softmax_rows(x.data_ptr(), ldx, out.data_ptr(), ldy, x.size(0), x.size(1), s)
     if st != GEMM_OK:
         raise GemmError(st, "softmax_rows")
+    return out
+
+
+def _heads_view(t, what):
+    """(ld, head_stride) of a [BH, seq, d] view with unit stride along d."""
+    if t.dim() != 3 or (t.size(2) > 1 and t.stride(2) != 1):
+        raise ValueError(f"{what} must be [BH, seq, d] with unit stride along d")
+    return t.stride(1), t.stride(0)
+
+
+def attention(q, k, v, causal: bool = False, out=None, out_dtype=None, stream=None):
+    """O = softmax(q k^T / sqrt(d)) v for [BH, seq, d] fp16/bf16 CUDA tensors (q, k, v
+    with the same strides); with `causal`, key j counts for query i only if j <= i.
+    O is fp32 unless `out_dtype` (or `out`) says otherwise."""
+    import torch
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must have the same dtype")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"shapes differ: {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    lds = {_heads_view(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"))}
+    if len(lds) != 1:
+        raise ValueError("q, k and v must share one layout (strides)")
+    ld, hs = lds.pop()
+    BH, seq, d = q.shape
+    if out is None:
+        out = torch.empty((BH, seq, d), dtype=out_dtype or torch.float32, device=q.device)
+    ldo, hso = _heads_view(out, "out")
+    s = (torch.cuda.current_stream(q.device) if stream is None else stream).cuda_stream
+    st = attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), BH, seq, d, ld,
+                       hs, ldo, hso, int(bool(causal)), _dtype_code(q), _out_code(out), s)
+    if st != GEMM_OK:
+        raise GemmError(st, "attention_fwd")
     return out

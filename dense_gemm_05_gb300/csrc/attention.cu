@@ -1,0 +1,623 @@
+// attention.cu -- attention forward on GB300 (sm_103a): the C ABI declared in
+// include/attention.h.
+//
+// The loop of section "Flash Attention in Triton and online softmax" of "How
+// to hand-write Triton kernels for matmul and Flash Attention": one CTA per
+// block of 128 queries of one head walks the key/value blocks (128 keys each)
+// and keeps, per query row, a running maximum m, a running sum l and an
+// accumulator O that are rescaled by alpha = exp(m_old - m_new) whenever m
+// grows; O / l is written once at the end.  Causal: key j takes part in row i
+// only if j <= i, so query block t needs key blocks 0..t, and only block t is
+// masked element by element.
+//
+// GB300 mapping (one CTA per SM: 512 TMEM columns, ~180 KiB of shared memory):
+//   warp 0      TMA producer: the Q tile once, then K and V tiles into a
+//               3-stage ring (3-D tensor maps over [BH, seq, d]).
+//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T (M 128, N 128, K 64)
+//               into one of two TMEM score buffers, one block ahead of the
+//               softmax; then O += P_j V_j (M 128, N 64, K 128) once P_j is in
+//               shared memory.
+//   warps 2..5  softmax, one thread per query row (= TMEM lane): read S_j from
+//               TMEM, mask, row max, p = 2^(s*c - m*c) with c = log2(e)/sqrt(d),
+//               row sum, P_j rounded to the input type into shared memory in
+//               the operand layout of the second MMA, and the rescale of O in
+//               TMEM (load, multiply by alpha, store) after the previous P V
+//               has finished.  At the end O / l goes to global memory.
+// Every mbarrier wait is bounded; a role that gives up raises the CTA's abort
+// flag and records the failure in a device status word.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/attention.h"
+#include "ptx.cuh"
+#include "tiles.cuh"
+
+namespace {
+
+__device__ int g_attn_status;
+
+constexpr int kBQ = 128;                  // queries per CTA
+constexpr int kBKV = 128;                 // keys per block
+constexpr int kD = 64;                    // head dimension
+constexpr int kStages = 3;                // K/V ring depth
+constexpr int kQBytes = kBQ * kD * 2;     // 16 KiB: 128 rows of 128 B (K-major operand)
+constexpr int kKBytes = kBKV * kD * 2;    // 16 KiB: K-major operand, N = keys
+constexpr int kVBytes = kBKV * kD * 2;    // 16 KiB: two 8 KiB MN-major halves of 64 keys
+constexpr int kPBytes = kBQ * kBKV * 2;   // 32 KiB: two 16 KiB K-major atoms of 64 keys
+constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 2;
+constexpr int kSmemBytes =
+    1024 + kQBytes + kStages * (kKBytes + kVBytes) + 2 * kPBytes + 8 * kNumBars + 16;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256,320)
+constexpr uint32_t kTmemO = 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+struct AttnParams {
+    void* O;
+    int64_t ldo, hso;
+    int32_t out_type;      // gemm_out_t
+    int32_t o_vec;         // 16-byte stores of O rows are legal
+    int32_t seq;
+    int32_t causal;
+    int32_t ntiles;        // query blocks per head
+    float c;               // log2(e) / sqrt(d)
+    uint64_t timeout_ns;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attention_fwd_kernel(const __grid_constant__ CUtensorMap mapQ,
+                         const __grid_constant__ CUtensorMap mapK,
+                         const __grid_constant__ CUtensorMap mapV, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sK = sQ + kQBytes;
+    uint8_t* sV = sK + kStages * kKBytes;
+    uint8_t* sP = sV + kStages * kVBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
+    uint64_t* q_full = bars;
+    uint64_t* k_full = q_full + 1;
+    uint64_t* v_full = k_full + kStages;
+    uint64_t* kv_empty = v_full + kStages;
+    uint64_t* s_full = kv_empty + kStages;
+    uint64_t* s_empty = s_full + 2;
+    uint64_t* p_full = s_empty + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* drain = pv_done + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int h = blockIdx.y;
+    const int qt = p.causal ? (p.ntiles - 1 - static_cast<int>(blockIdx.x))
+                            : static_cast<int>(blockIdx.x);   // heavy causal blocks first
+    const int q0 = qt * kBQ;
+    const int nkv = p.causal ? qt + 1 : (p.seq + kBKV - 1) / kBKV;
+
+    if (threadIdx.x == 0) {
+        dg::mbar_init(dg::smem_u32(q_full), 1u);
+        for (int s = 0; s < kStages; ++s) {
+            dg::mbar_init(dg::smem_u32(&k_full[s]), 1u);
+            dg::mbar_init(dg::smem_u32(&v_full[s]), 1u);
+            dg::mbar_init(dg::smem_u32(&kv_empty[s]), 1u);
+        }
+        for (int b = 0; b < 2; ++b) {
+            dg::mbar_init(dg::smem_u32(&s_full[b]), 1u);
+            dg::mbar_init(dg::smem_u32(&s_empty[b]), 128u);
+            dg::mbar_init(dg::smem_u32(&p_full[b]), 128u);
+        }
+        dg::mbar_init(dg::smem_u32(pv_done), 1u);
+        dg::mbar_init(dg::smem_u32(drain), 1u);
+        *abort_flag = 0;
+        dg::fence_mbar_init();
+    }
+    if (warp == 1) {
+        dg::tmem_alloc(dg::smem_u32(tmem_slot), kTmemCols);
+        dg::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        dg::prefetch_tmap(&mapQ);
+        dg::prefetch_tmap(&mapK);
+        dg::prefetch_tmap(&mapV);
+    }
+    dg::tc_fence_before();
+    __syncthreads();
+    dg::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicExch(&g_attn_status, 1);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t qb = dg::smem_u32(q_full);
+            dg::mbar_arrive_expect_tx(qb, kQBytes);
+            dg::tma_load_3d(dg::smem_u32(sQ), &mapQ, qb, 0, q0, h);
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j % kStages;
+                const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
+                if (!dg::mbar_wait(dg::smem_u32(&kv_empty[st]), ph ^ 1u, abort_flag,
+                                   p.timeout_ns)) {
+                    fail();
+                    break;
+                }
+                const uint32_t kb = dg::smem_u32(&k_full[st]);
+                dg::mbar_arrive_expect_tx(kb, kKBytes);
+                dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes), &mapK, kb, 0, j * kBKV, h);
+                const uint32_t vb = dg::smem_u32(&v_full[st]);
+                dg::mbar_arrive_expect_tx(vb, kVBytes);
+                const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
+                dg::tma_load_3d(vdst, &mapV, vb, 0, j * kBKV, h);
+                dg::tma_load_3d(vdst + kVBytes / 2, &mapV, vb, 0, j * kBKV + kBKV / 2, h);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = dg::idesc_f16(BF16, false, false, kBQ, kBKV);
+            constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
+            const uint32_t q_addr = dg::smem_u32(sQ);
+            bool ok = dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
+            auto issue_s = [&](int jj) -> bool {
+                const int st = jj % kStages;
+                const int b = jj & 1;
+                if (!dg::mbar_wait(dg::smem_u32(&s_empty[b]),
+                                   (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, abort_flag,
+                                   p.timeout_ns))
+                    return false;
+                if (!dg::mbar_wait(dg::smem_u32(&k_full[st]),
+                                   static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
+                                   p.timeout_ns))
+                    return false;
+                dg::tc_fence_after();
+                const uint32_t k_addr = dg::smem_u32(sK + st * kKBytes);
+#pragma unroll
+                for (int k16 = 0; k16 < kD / 16; ++k16)
+                    dg::tc_mma_f16(tmem_base + static_cast<uint32_t>(b * kBKV),
+                                   dg::operand_desc<false>(q_addr, k16),
+                                   dg::operand_desc<false>(k_addr, k16), idesc_s,
+                                   k16 > 0 ? 1u : 0u);
+                dg::tc_commit(dg::smem_u32(&s_full[b]));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < nkv; ++j) {
+                if (j + 1 < nkv && !issue_s(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                const int b = j & 1;
+                const int st = j % kStages;
+                if (!dg::mbar_wait(dg::smem_u32(&p_full[b]), static_cast<uint32_t>(j >> 1) & 1u,
+                                   abort_flag, p.timeout_ns) ||
+                    !dg::mbar_wait(dg::smem_u32(&v_full[st]),
+                                   static_cast<uint32_t>(j / kStages) & 1u, abort_flag,
+                                   p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                dg::tc_fence_after();
+                const uint32_t p_addr = dg::smem_u32(sP + b * kPBytes);
+                const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
+#pragma unroll
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        dg::tc_mma_f16(
+                            tmem_base + kTmemO,
+                            dg::operand_desc<false>(p_addr + half * (kPBytes / 2), k16),
+                            dg::operand_desc<true>(v_addr + half * (kVBytes / 2), k16), idesc_pv,
+                            (j > 0 || half > 0 || k16 > 0) ? 1u : 0u);
+                dg::tc_commit(dg::smem_u32(&kv_empty[st]));
+                dg::tc_commit(dg::smem_u32(pv_done));
+            }
+            if (!ok) fail();
+            // Every MMA issued must have completed (and signalled its barriers)
+            // before the CTA's shared memory and TMEM go away.
+            const volatile int never = 0;
+            dg::tc_commit(dg::smem_u32(drain));
+            dg::mbar_wait(dg::smem_u32(drain), 0u, &never, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;            // query row in the tile == TMEM lane
+        const int qrow = q0 + r;
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int ptype = BF16 ? dg::kOutBF16 : dg::kOutF16;
+        float m = -INFINITY, l = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int b = j & 1;
+            const bool got = dg::mbar_wait(dg::smem_u32(&s_full[b]),
+                                           static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
+                                           p.timeout_ns);
+            if (!__all_sync(0xffffffffu, got)) {   // tcgen05.ld is warp-collective
+                ok = false;
+                break;
+            }
+            dg::tc_fence_after();
+            // S_j row: all four 32-column loads in flight before one wait; the
+            // score buffer is handed back as soon as the values are in registers.
+            const uint32_t s_addr = lane_addr + static_cast<uint32_t>(b * kBKV);
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            dg::tmem_ld_32x32b_x32(s_addr, v0);
+            dg::tmem_ld_32x32b_x32(s_addr + 32u, v1);
+            dg::tmem_ld_32x32b_x32(s_addr + 64u, v2);
+            dg::tmem_ld_32x32b_x32(s_addr + 96u, v3);
+            dg::tmem_ld_wait(v0);
+            dg::tmem_ld_wait(v1);
+            dg::tmem_ld_wait(v2);
+            dg::tmem_ld_wait(v3);
+            dg::tc_fence_before();
+            dg::mbar_arrive(dg::smem_u32(&s_empty[b]));     // S buffer b may be refilled
+            float x[kBKV];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                x[i] = __uint_as_float(v0[i]);
+                x[32 + i] = __uint_as_float(v1[i]);
+                x[64 + i] = __uint_as_float(v2[i]);
+                x[96 + i] = __uint_as_float(v3[i]);
+            }
+            // Mask (only the diagonal block, and the block holding key seq-1):
+            // keys at or beyond seq, and (causal) keys after this query.
+            const int kv0 = j * kBKV;
+            if ((p.causal && j == qt) || kv0 + kBKV > p.seq) {
+                const int lim = min(p.seq, p.causal ? qrow + 1 : p.seq) - kv0;   // keys [kv0, kv0+lim) stay
+#pragma unroll
+                for (int i = 0; i < kBKV; ++i)
+                    if (i >= lim) x[i] = -INFINITY;
+            }
+            // Row maximum (four independent chains)
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < kBKV; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
+            const float mb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float m_new = fmaxf(m, mb);
+            const float mc = m_new * p.c;
+            const float alpha = dg::ex2_approx(m * p.c - mc);   // 0 on the first block
+            float sums[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            const uint32_t pbuf = dg::smem_u32(sP + b * kPBytes);
+#pragma unroll
+            for (int c8 = 0; c8 < kBKV / 8; ++c8) {            // 8-key chunks 0..15
+                float pv[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    pv[t] = dg::ex2_approx(fmaf(x[c8 * 8 + t], p.c, -mc));
+                    sums[t & 3] += pv[t];
+                }
+                uint4 w;
+                w.x = dg::pack_out(pv[0], pv[1], ptype);
+                w.y = dg::pack_out(pv[2], pv[3], ptype);
+                w.z = dg::pack_out(pv[4], pv[5], ptype);
+                w.w = dg::pack_out(pv[6], pv[7], ptype);
+                dg::st_shared_v4_b32(pbuf + static_cast<uint32_t>((c8 >> 3) * (kPBytes / 2)) +
+                                         dg::chunk_offset<false>(r, c8 & 7),
+                                     w);
+            }
+            const float rs = (sums[0] + sums[1]) + (sums[2] + sums[3]);
+            l = l * alpha + rs;
+            dg::fence_proxy_async_smem();     // P_j -> visible to the tensor cores
+            if (j > 0) {
+                // O holds the sum up to block j-1 once P_{j-1} V_{j-1} is done;
+                // rescale it to the new maximum before P_j V_j is added.
+                const bool done = dg::mbar_wait(dg::smem_u32(pv_done),
+                                                static_cast<uint32_t>(j - 1) & 1u, abort_flag,
+                                                p.timeout_ns);
+                if (!__all_sync(0xffffffffu, done)) {
+                    ok = false;
+                    break;
+                }
+                dg::tc_fence_after();
+                if (!__all_sync(0xffffffffu, alpha == 1.0f)) {
+#pragma unroll
+                    for (int ch = 0; ch < kD / 32; ++ch) {
+                        uint32_t v[32];
+                        const uint32_t ta = lane_addr + kTmemO + static_cast<uint32_t>(ch * 32);
+                        dg::tmem_ld_32x32b_x32(ta, v);
+                        dg::tmem_ld_wait(v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        dg::tmem_st_32x32b_x32(ta, v);
+                    }
+                    dg::tmem_st_wait();
+                }
+            }
+            dg::tc_fence_before();
+            dg::mbar_arrive(dg::smem_u32(&p_full[b]));
+            m = m_new;
+        }
+        if (ok) {
+            const bool done = dg::mbar_wait(dg::smem_u32(pv_done),
+                                            static_cast<uint32_t>(nkv - 1) & 1u, abort_flag,
+                                            p.timeout_ns);
+            ok = __all_sync(0xffffffffu, done);
+        }
+        if (!ok) {
+            fail();
+        } else {
+            dg::tc_fence_after();
+            const float inv = 1.0f / l;
+            uint32_t o[kD];
+#pragma unroll
+            for (int ch = 0; ch < kD / 32; ++ch) {
+                uint32_t v[32];
+                dg::tmem_ld_32x32b_x32(lane_addr + kTmemO + static_cast<uint32_t>(ch * 32), v);
+                dg::tmem_ld_wait(v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[ch * 32 + i] = __float_as_uint(__uint_as_float(v[i]) * inv);
+            }
+            if (qrow < p.seq) {
+                const int64_t off = int64_t(h) * p.hso + int64_t(qrow) * p.ldo;
+                if (p.out_type == dg::kOutF32) {
+                    float* dst = static_cast<float*>(p.O) + off;
+                    if (p.o_vec) {
+#pragma unroll
+                        for (int i = 0; i < kD / 4; ++i)
+                            reinterpret_cast<float4*>(dst)[i] = make_float4(
+                                __uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kD; ++i) dst[i] = __uint_as_float(o[i]);
+                    }
+                } else {
+                    uint16_t* dst = static_cast<uint16_t*>(p.O) + off;
+                    if (p.o_vec) {
+#pragma unroll
+                        for (int i = 0; i < kD / 8; ++i) {
+                            uint4 w;
+                            w.x = dg::pack_out(__uint_as_float(o[8 * i]), __uint_as_float(o[8 * i + 1]), p.out_type);
+                            w.y = dg::pack_out(__uint_as_float(o[8 * i + 2]), __uint_as_float(o[8 * i + 3]), p.out_type);
+                            w.z = dg::pack_out(__uint_as_float(o[8 * i + 4]), __uint_as_float(o[8 * i + 5]), p.out_type);
+                            w.w = dg::pack_out(__uint_as_float(o[8 * i + 6]), __uint_as_float(o[8 * i + 7]), p.out_type);
+                            reinterpret_cast<uint4*>(dst)[i] = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kD; ++i)
+                            dst[i] = static_cast<uint16_t>(
+                                dg::pack_out(__uint_as_float(o[i]), 0.0f, p.out_type) & 0xFFFFu);
+                    }
+                }
+            }
+        }
+    }
+
+    if (*abort_flag && threadIdx.x == 0) {
+        // Copies already issued may still land in this CTA's shared memory:
+        // give them a bounded 2 ms before the CTA leaves.
+        const uint64_t t0 = dg::global_timer_ns();
+        while (dg::global_timer_ns() - t0 < 2000000ull) {
+        }
+    }
+    dg::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        dg::tc_fence_after();
+        dg::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000,
+                                             cudaEnableDefault, &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+        else
+            (void)cudaGetLastError();
+    });
+    return fn;
+}
+
+// [BH, seq, d] view with row pitch ld and head pitch hs (elements); boxes of
+// 64 d x `rows` rows x 1 head, 128-byte swizzle, zero fill beyond seq.
+bool encode_qkv(CUtensorMap* map, bool bf16, const void* ptr, int64_t BH, int64_t seq, int64_t ld,
+                int64_t hs, uint32_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(seq),
+                          static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(hs) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceFacts {
+    bool known = false;
+    bool sm103 = false;
+};
+
+std::mutex g_mu;
+DeviceFacts g_dev[64];
+bool g_attr_set[2] = {false, false};
+
+bool device_ok(bool* sm103) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceFacts& f = g_dev[dev];
+    if (!f.known) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        f.sm103 = major == 10 && minor == 3;
+        f.known = true;
+    }
+    *sm103 = f.sm103;
+    return true;
+}
+
+// Bytes [begin, end) spanned by a [BH, seq, width] strided view.
+void span(const void* ptr, int64_t BH, int64_t seq, int64_t width, int64_t ld, int64_t hs,
+          int64_t esize, uintptr_t* b, uintptr_t* e) {
+    *b = reinterpret_cast<uintptr_t>(ptr);
+    *e = *b + static_cast<uintptr_t>(((BH - 1) * hs + (seq - 1) * ld + width) * esize);
+}
+
+gemm_status_t check(const void* Q, const void* K, const void* V, const void* O, int64_t BH,
+                    int64_t seq, int64_t d, int64_t ld, int64_t hs, int64_t ldo, int64_t hso,
+                    gemm_dtype_t dtype, int32_t out_type) {
+    if (BH < 0 || seq < 0 || d < 0 || ld < 0 || hs < 0 || ldo < 0 || hso < 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_F16 && dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
+    if (out_type != GEMM_OUT_F32 && out_type != GEMM_OUT_F16 && out_type != GEMM_OUT_BF16)
+        return GEMM_ERR_UNSUPPORTED;
+    if (BH == 0 || seq == 0) return GEMM_OK;
+    if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (ld < d || ldo < d) return GEMM_ERR_INVALID_ARG;
+    const int64_t osz = out_type == GEMM_OUT_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+         reinterpret_cast<uintptr_t>(V)) % 16u != 0u ||
+        reinterpret_cast<uintptr_t>(O) % static_cast<uintptr_t>(osz) != 0u)
+        return GEMM_ERR_INVALID_ARG;
+    if (d != kD) return GEMM_ERR_UNSUPPORTED;
+    if (ld % 8 != 0 || hs % 8 != 0 || BH > 65535 || seq > INT32_MAX ||
+        ld > (int64_t(1) << 36) || hs > (int64_t(1) << 36) || ldo > (int64_t(1) << 36) ||
+        hso > (int64_t(1) << 36))
+        return GEMM_ERR_UNSUPPORTED;
+    uintptr_t ob, oe;
+    span(O, BH, seq, d, ldo, hso, osz, &ob, &oe);
+    for (const void* t : {Q, K, V}) {
+        uintptr_t tb, te;
+        span(t, BH, seq, d, ld, hs, 2, &tb, &te);
+        if (ob < te && tb < oe) return GEMM_ERR_INVALID_ARG;
+    }
+    return GEMM_OK;
+}
+
+bool debug_sync() {
+    static const bool on = [] {
+        const char* e = std::getenv("GEMM_DEBUG_SYNC");
+        return e != nullptr && e[0] == '1';
+    }();
+    return on;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t attention_fwd_query(const void* Q, const void* K, const void* V, const void* O,
+                                  int64_t BH, int64_t seq, int64_t d, int64_t ld,
+                                  int64_t head_stride, int64_t ldo, int64_t head_stride_o,
+                                  int32_t causal, gemm_dtype_t dtype, int32_t out_type,
+                                  attention_config_t* out) {
+    if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+    const gemm_status_t st =
+        check(Q, K, V, O, BH, seq, d, ld, head_stride, ldo, head_stride_o, dtype, out_type);
+    if (st != GEMM_OK) return st;
+    *out = attention_config_t{};
+    out->block_q = kBQ;
+    out->block_kv = kBKV;
+    out->head_dim = static_cast<int32_t>(d);
+    out->stages = kStages;
+    out->grid_x = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
+    out->grid_y = static_cast<int32_t>(BH);
+    out->causal = causal ? 1 : 0;
+    return GEMM_OK;
+}
+
+gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O, int64_t BH,
+                            int64_t seq, int64_t d, int64_t ld, int64_t head_stride, int64_t ldo,
+                            int64_t head_stride_o, int32_t causal, gemm_dtype_t dtype,
+                            int32_t out_type, struct CUstream_st* stream) {
+    const gemm_status_t st =
+        check(Q, K, V, O, BH, seq, d, ld, head_stride, ldo, head_stride_o, dtype, out_type);
+    if (st != GEMM_OK || BH == 0 || seq == 0) return st;
+    bool sm103 = false;
+    if (!device_ok(&sm103)) return GEMM_ERR_CUDA;
+    if (!sm103) return GEMM_ERR_UNSUPPORTED;
+    const bool bf16 = dtype == GEMM_BF16;
+    CUtensorMap mq, mk, mv;
+    if (!encode_qkv(&mq, bf16, Q, BH, seq, ld, head_stride, kBQ) ||
+        !encode_qkv(&mk, bf16, K, BH, seq, ld, head_stride, kBKV) ||
+        !encode_qkv(&mv, bf16, V, BH, seq, ld, head_stride, kBKV / 2))
+        return GEMM_ERR_CUDA;
+    auto kernel = bf16 ? attention_fwd_kernel<true> : attention_fwd_kernel<false>;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_attr_set[bf16 ? 1 : 0]) {
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kSmemBytes) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            g_attr_set[bf16 ? 1 : 0] = true;
+        }
+    }
+    AttnParams p{};
+    p.O = O;
+    p.ldo = ldo;
+    p.hso = head_stride_o;
+    p.out_type = out_type;
+    const int64_t ovec = out_type == GEMM_OUT_F32 ? 4 : 8;
+    p.o_vec = (reinterpret_cast<uintptr_t>(O) % 16u == 0u && ldo % ovec == 0 &&
+               head_stride_o % ovec == 0)
+                  ? 1
+                  : 0;
+    p.seq = static_cast<int32_t>(seq);
+    p.causal = causal ? 1 : 0;
+    p.ntiles = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
+    p.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+    p.timeout_ns = kTimeoutNs;
+    const dim3 grid(static_cast<unsigned>(p.ntiles), static_cast<unsigned>(BH));
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        int status = 0;
+        if (cudaMemcpyFromSymbol(&status, g_attn_status, sizeof(int)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (status != 0) {
+            const int zero = 0;
+            (void)cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
+            return GEMM_ERR_TIMEOUT;
+        }
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

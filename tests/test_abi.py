@@ -97,3 +97,26 @@ def test_softmax_argument_checks_need_no_gpu():
     with pytest.raises(g.GemmError):
         g.softmax_rows_query(0, 1, 0, 1, -1, 1)
     assert g.softmax_rows_query(0, 1, 0, 1, 0, 5)["path_name"] == "none"
+
+
+def test_attention_argument_checks_need_no_gpu():
+    """Argument errors and empty shapes are decided before any CUDA call."""
+    af = g.attention_fwd
+    a, b, c, o = 1 << 20, 2 << 20, 3 << 20, 4 << 20            # distinct, aligned, unused
+    F16, BF16 = g.GEMM_F16, g.GEMM_BF16
+    F32 = g.GEMM_OUT_F32
+    assert af(a, b, c, o, 0, 128, 64, 64, 8192, 64, 8192, 1, BF16, F32, 0) == g.GEMM_OK       # BH 0
+    assert af(a, b, c, o, 2, 0, 64, 64, 8192, 64, 8192, 1, BF16, F32, 0) == g.GEMM_OK        # seq 0
+    assert af(a, b, c, o, -1, 8, 64, 64, 512, 64, 512, 0, BF16, F32, 0) == g.GEMM_ERR_INVALID_ARG
+    assert af(0, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, BF16, F32, 0) == g.GEMM_ERR_INVALID_ARG
+    assert af(a, b, c, o, 2, 8, 64, 32, 512, 64, 512, 0, BF16, F32, 0) == g.GEMM_ERR_INVALID_ARG  # ld < d
+    assert af(a + 8, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, F16, F32, 0) == g.GEMM_ERR_INVALID_ARG  # align
+    assert af(a, b, c, o, 2, 8, 128, 128, 1024, 128, 1024, 0, F16, F32, 0) == g.GEMM_ERR_UNSUPPORTED  # d
+    assert af(a, b, c, o, 2, 8, 64, 68, 544, 64, 512, 0, F16, F32, 0) == g.GEMM_ERR_UNSUPPORTED   # ld % 8
+    assert af(a, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, 7, F32, 0) == g.GEMM_ERR_UNSUPPORTED     # dtype
+    assert af(a, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, F16, 9, 0) == g.GEMM_ERR_UNSUPPORTED     # out
+    assert af(a, b, c, b + 256, 2, 8, 64, 64, 512, 64, 512, 0, F16, F32, 0) == g.GEMM_ERR_INVALID_ARG  # O on K
+    with pytest.raises(g.GemmError):
+        g.attention_fwd_query(a, b, c, o, -1, 8, 64, 64, 512, 64, 512, 0, F16, F32)
+    cfg = g.attention_fwd_query(a, b, c, o, 3, 1000, 64, 64, 64000, 64, 64000, 1, BF16, F32)
+    assert cfg["grid_x"] == 8 and cfg["grid_y"] == 3 and cfg["block_q"] == 128 and cfg["causal"] == 1

@@ -1,0 +1,178 @@
+"""GPU parity of the attention forward pass (through the C ABI) against the binary64 oracle.
+
+Tolerance, derived from the kernel's arithmetic (u_t = 2^-8 for bf16 inputs,
+2^-11 for fp16; u = 2^-24):
+  * the weights P are rounded to the input type before P V while the row sum
+    l adds the unrounded fp32 values: each weight p/l is off by at most u_t
+    relatively;
+  * a score s = q.k is an fp32 sum of d exact products: |ds| <= d u sum|q||k|;
+    scaled by 1/sqrt(d) it moves every weight of its row by a factor
+    exp(+-|ds|/sqrt(d)), i.e. 2 eps relatively with eps = max_j d u sum|q||k_j| / sqrt(d);
+  * ex2.approx (relative 2^-22 per value), the fp32 row sum, the fp32 MMA
+    sums of P V and the rescales add far less than 2^-12 relatively;
+so |O - O*| <= (2 u_t + 2 eps + 2^-12) sum_j P*_j |V_j| (+ u_out |O*| for a
+16-bit O, the one output rounding) + 1e-7.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dense_gemm_05_gb300 as g
+import workloads
+from oracle import attention as oa
+
+pytestmark = pytest.mark.gpu
+
+U_IN = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+U_OUT = {torch.float32: 0.0, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.build()
+
+
+def dtype_name(t):
+    return "bf16" if t.dtype == torch.bfloat16 else "f16"
+
+
+def assert_attn_close(got, Q, K, V, causal, head, rows, out_dtype, what):
+    """got: float64 numpy [len(rows), d] for head `head`."""
+    rows = np.asarray(rows, dtype=np.int64)
+    ref = oa.attention_rows(Q, K, V, causal, head, rows)
+    wabs = oa.weight_abs_v(Q, K, V, causal, head, rows)
+    q = Q[head].double().numpy()[rows]
+    k = K[head].double().numpy()
+    d = q.shape[1]
+    qk = np.abs(q) @ np.abs(k).T
+    if causal:
+        qk = np.where(rows[:, None] >= np.arange(k.shape[0])[None, :], qk, 0.0)
+    eps = d * 2.0 ** -24 * qk.max(axis=1, keepdims=True) / math.sqrt(d)
+    tol = (2 * U_IN[dtype_name(Q)] + 2 * eps + 2.0 ** -12) * wabs + U_OUT[out_dtype] * np.abs(ref) + 1e-7
+    err = np.abs(got - ref)
+    ok = err <= tol
+    if not ok.all():
+        i, c = np.argwhere(~ok)[0]
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} off; first row {rows[i]} col {c}: "
+                             f"gpu {got[i, c]!r} oracle {ref[i, c]!r} tol {tol[i, c]!r}")
+
+
+def run(Q, K, V, causal, out_dtype=torch.float32, layout="heads"):
+    """Q, K, V: CPU [BH, seq, d].  layout 'heads' = contiguous [BH, seq, d];
+    'interleaved' = stored [seq, BH, d]; 'padded' = rows padded to 72 elements."""
+    dev = torch.device("cuda:0")
+    BH, seq, d = Q.shape
+    if layout == "heads":
+        q, k, v = (t.to(dev) for t in (Q, K, V))
+    elif layout == "interleaved":
+        q, k, v = (t.transpose(0, 1).contiguous().to(dev).transpose(0, 1) for t in (Q, K, V))
+    else:
+        def pad(t):
+            buf = torch.full((BH, seq, 72), float("nan"), dtype=t.dtype)
+            buf[:, :, :d] = t
+            return buf.to(dev)[:, :, :d]
+        q, k, v = pad(Q), pad(K), pad(V)
+    out = torch.full((BH, seq, d), float("nan"), dtype=out_dtype, device=dev)
+    g.attention(q, k, v, causal=causal, out=out)
+    torch.cuda.synchronize()
+    return out.float().cpu().double().numpy()
+
+
+@pytest.mark.parametrize("name", ["attn_bh2_s256_d64_f16_causal", "attn_bh2_s1000_d64_bf16"])
+def test_small_workloads_full(name):
+    w = workloads.ATTN_WORKLOADS[name]
+    Q, K, V = workloads.make_qkv(w)
+    got = run(Q, K, V, w.causal)
+    for h in range(w.BH):
+        assert_attn_close(got[h], Q, K, V, w.causal, h, np.arange(w.seq), torch.float32, f"{name} head {h}")
+
+
+SEQS = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 300, 513]
+
+
+@pytest.mark.parametrize("seq", SEQS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_lengths(seq, causal):
+    dt = "bf16" if seq % 2 else "f16"
+    Q, K, V = workloads.custom_qkv(3, seq, 64, dt, seed=seq * 3 + causal)
+    got = run(Q, K, V, causal)
+    assert np.all(np.isfinite(got))
+    for h in range(3):
+        assert_attn_close(got[h], Q, K, V, causal, h, np.arange(seq), torch.float32,
+                          f"seq {seq} causal {causal} head {h}")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("layout", ["heads", "interleaved", "padded"])
+def test_layouts_and_output_types(out_dtype, layout):
+    Q, K, V = workloads.custom_qkv(4, 333, 64, "bf16", seed=7)
+    got = run(Q, K, V, True, out_dtype=out_dtype, layout=layout)
+    for h in range(4):
+        assert_attn_close(got[h], Q, K, V, True, h, np.arange(333), out_dtype, f"{layout} {out_dtype} head {h}")
+
+
+def test_fp32_output_layouts():
+    Q, K, V = workloads.custom_qkv(3, 200, 64, "f16", seed=8)
+    for layout in ("interleaved", "padded"):
+        got = run(Q, K, V, False, layout=layout)
+        for h in range(3):
+            assert_attn_close(got[h], Q, K, V, False, h, np.arange(200), torch.float32, f"{layout} head {h}")
+
+
+def test_closed_forms_on_gpu():
+    """Constant V rows give O = that row; identical keys give (prefix) means of V."""
+    Q, K, V = workloads.custom_qkv(2, 300, 64, "bf16", seed=9)
+    Vc = torch.ones_like(V) * torch.linspace(-2, 2, 64).to(torch.bfloat16)
+    got = run(Q, K, Vc, True)
+    assert np.allclose(got, Vc.double().numpy(), rtol=2 ** -7, atol=1e-6)
+    Ks = K[:, :1].expand(-1, 300, -1).contiguous()
+    got = run(Q, Ks, V, True)
+    prefix = np.cumsum(V.double().numpy(), axis=1) / np.arange(1, 301)[None, :, None]
+    wabs = np.cumsum(np.abs(V.double().numpy()), axis=1) / np.arange(1, 301)[None, :, None]
+    assert np.all(np.abs(got - prefix) <= (2 * 2 ** -8 + 2 ** -12) * wabs + 1e-6)
+
+
+def test_repeatable_bits():
+    Q, K, V = workloads.custom_qkv(2, 700, 64, "bf16", seed=10)
+    a = run(Q, K, V, True)
+    b = run(Q, K, V, True)
+    assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16"])
+def test_full_size_sampled(name):
+    """The measured workloads, launched as bench.py launches them: sampled rows of
+    three heads (first and last rows of the sequence included) against the oracle;
+    every output finite."""
+    w = workloads.ATTN_WORKLOADS[name]
+    Q, K, V = workloads.make_qkv(w)
+    dev = torch.device("cuda:0")
+    q, k, v = Q.to(dev), K.to(dev), V.to(dev)
+    out = g.attention(q, k, v, causal=w.causal)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    rng = np.random.default_rng(w.seed)
+    for h in (0, w.BH // 2, w.BH - 1):
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, w.seq - 1], rng.integers(0, w.seq, 48)]))
+        got = out[h, torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        assert_attn_close(got, Q, K, V, w.causal, h, rows, torch.float32, f"{name} head {h}")
+
+
+def test_device_errors():
+    dev = torch.device("cuda:0")
+    q = torch.randn(2, 64, 64, device=dev).to(torch.bfloat16)
+    o = torch.empty(2, 64, 64, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    st = g.attention_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), q.data_ptr(), 2, 64, 64, 64,
+                         4096, 64, 4096, 0, g.GEMM_BF16, g.GEMM_OUT_BF16, s)
+    assert st == g.GEMM_ERR_INVALID_ARG                       # O overlaps Q
+    st = g.attention_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), 2, 64, 64, 64,
+                         4096, 64, 4096, 0, g.GEMM_BF16, g.GEMM_OUT_F32, s)
+    assert st == g.GEMM_OK                                    # Q = K = V is fine
+    with pytest.raises(TypeError):
+        g.attention(q, q.half(), q)
+    torch.cuda.synchronize()
