@@ -430,6 +430,40 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
                    "bytes_alg": w.bytes_alg}
     del a, bs, c
     out.update(softmax_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
+    out.update(attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
+    return out
+
+
+def attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src) -> dict:
+    """Attention forward (a ranked next row of the hot-path table): seq 8192, d 64,
+    16 heads, bf16, causal and not.  Tensor-core work, but bounded in practice by
+    the exponentials of the softmax (one per score).  Events around every launch,
+    median of 20; torch's scaled_dot_product_attention on the same tensors for
+    context."""
+    out = {}
+    for name in ("attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16"):
+        w = workloads.ATTN_WORKLOADS[name]
+        Q, K, V = workloads.make_qkv(w)
+        q, k, v = Q.to(dev), K.to(dev), V.to(dev)
+        o = torch.empty(w.BH, w.seq, w.d, dtype=torch.float32, device=dev)
+        call = lambda: g.attention(q, k, v, causal=w.causal, out=o, stream=stream)  # noqa: E731
+        time_launches(torch, None, [call] * 3, stream)
+        ms = sorted(time_launches(torch, None, [call] * 20, stream))
+        t = ms[len(ms) // 2] / 1e3
+        tf = w.flops / t / 1e12
+        with torch.cuda.stream(stream):
+            q4, k4, v4 = q.unsqueeze(0), k.unsqueeze(0), v.unsqueeze(0)
+            ref = lambda: torch.nn.functional.scaled_dot_product_attention(  # noqa: E731
+                q4, k4, v4, is_causal=w.causal)
+            time_launches(torch, None, [ref] * 3, stream)
+            tms = sorted(time_launches(torch, None, [ref] * 10, stream))
+        out[name] = {"tflops": tf, "pct_of_peak": 100 * tf / peaks["bf16_tflops"],
+                     "median_us": t * 1e6, "flops": w.flops,
+                     "flops_counted": "4 * BH * d * (query, key) pairs kept by the mask",
+                     "kernel": "attention_fwd_kernel: 2 query tiles of 128 per CTA, 128-key blocks",
+                     "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
+                     "torch_sdpa_tflops": w.flops / (tms[len(tms) // 2] / 1e3) / 1e12}
+        del q, k, v, o
     return out
 
 
@@ -529,6 +563,16 @@ def run_case(args) -> None:
     import workloads
     g.build()
     dev = torch.device("cuda:0")
+    if args.case in workloads.ATTN_WORKLOADS:
+        w = workloads.ATTN_WORKLOADS[args.case]
+        q, k, v = (t.to(dev) for t in workloads.make_qkv(w))
+        o = torch.empty(w.BH, w.seq, w.d, dtype=torch.float32, device=dev)
+        torch.cuda.synchronize()
+        for _ in range(args.launches):
+            g.attention(q, k, v, causal=w.causal, out=o)
+        torch.cuda.synchronize()
+        print(json.dumps({"case": w.name, "launches": args.launches}), flush=True)
+        return
     if args.case in workloads.SOFTMAX_WORKLOADS:
         w = workloads.SOFTMAX_WORKLOADS[args.case]
         x = workloads.make_rows(w).to(dev)

@@ -2,27 +2,33 @@
 // include/attention.h.
 //
 // The loop of section "Flash Attention in Triton and online softmax" of "How
-// to hand-write Triton kernels for matmul and Flash Attention": one CTA per
-// block of 128 queries of one head walks the key/value blocks (128 keys each)
+// to hand-write Triton kernels for matmul and Flash Attention": each block of
+// 128 queries of one head walks the key/value blocks (128 keys each)
 // and keeps, per query row, a running maximum m, a running sum l and an
 // accumulator O that are rescaled by alpha = exp(m_old - m_new) whenever m
 // grows; O / l is written once at the end.  Causal: key j takes part in row i
 // only if j <= i, so query block t needs key blocks 0..t, and only block t is
 // masked element by element.
 //
-// GB300 mapping (one CTA per SM: 512 TMEM columns, ~180 KiB of shared memory):
-//   warp 0      TMA producer: the Q tile once, then K and V tiles into a
+// GB300 mapping: one CTA per SM holds two query tiles of one head (A, B)
+// that share every K/V block (512 TMEM columns, ~190 KiB of shared memory):
+//   warp 0      TMA producer: both Q tiles once, then K and V blocks into a
 //               3-stage ring (3-D tensor maps over [BH, seq, d]).
-//   warp 1      TMEM owner and MMA issuer: S_j = Q K_j^T (M 128, N 128, K 64)
-//               into one of two TMEM score buffers, one block ahead of the
-//               softmax; then O += P_j V_j (M 128, N 64, K 128) once P_j is in
-//               shared memory.
-//   warps 2..5  softmax, one thread per query row (= TMEM lane): read S_j from
-//               TMEM, mask, row max, p = 2^(s*c - m*c) with c = log2(e)/sqrt(d),
-//               row sum, P_j rounded to the input type into shared memory in
-//               the operand layout of the second MMA, and the rescale of O in
-//               TMEM (load, multiply by alpha, store) after the previous P V
-//               has finished.  At the end O / l goes to global memory.
+//   warps 1, 2  one MMA issuer per tile (warp 1 also owns TMEM):
+//               S_t(j+1) = Q_t K^T (M 128, N 128, K 64) into the tile's TMEM
+//               score buffer as soon as the tile's softmax has read S_t(j),
+//               then O_t += P_t(j) V_j (M 128, N 64, K 128) once P_t(j) is in
+//               shared memory; a K/V stage is refilled when every tile that
+//               used it has committed its release.
+//   warps 3..10 two softmax warpgroups, one per tile, one thread per query
+//               row (= TMEM lane): read S_t(j) from TMEM, mask, row max,
+//               p = 2^(s*c - m*c) with c = log2(e)/sqrt(d), row sum, P_t(j)
+//               rounded to the input type into shared memory in the operand
+//               layout of the second MMA, and the rescale of O_t in TMEM
+//               (load, multiply by alpha, store) after P_t(j-1) V_{j-1} has
+//               finished.  At the end O_t / l goes to global memory.  The two
+//               warpgroups interleave on the SM's exponential units and issue
+//               slots while the tensor cores work on the other tile.
 // Every mbarrier wait is bounded; a role that gives up raises the CTA's abort
 // flag and records the failure in a device status word.
 #include <cmath>
@@ -41,20 +47,21 @@ namespace {
 
 __device__ int g_attn_status;
 
-constexpr int kBQ = 128;                  // queries per CTA
+constexpr int kBQ = 128;                  // queries per tile (TMEM lanes)
+constexpr int kTiles = 2;                 // query tiles per CTA, sharing every K/V block
 constexpr int kBKV = 128;                 // keys per block
 constexpr int kD = 64;                    // head dimension
 constexpr int kStages = 3;                // K/V ring depth
-constexpr int kQBytes = kBQ * kD * 2;     // 16 KiB: 128 rows of 128 B (K-major operand)
+constexpr int kQBytes = kBQ * kD * 2;     // 16 KiB per tile: 128 rows of 128 B (K-major operand)
 constexpr int kKBytes = kBKV * kD * 2;    // 16 KiB: K-major operand, N = keys
 constexpr int kVBytes = kBKV * kD * 2;    // 16 KiB: two 8 KiB MN-major halves of 64 keys
-constexpr int kPBytes = kBQ * kBKV * 2;   // 32 KiB: two 16 KiB K-major atoms of 64 keys
-constexpr int kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 2;
-constexpr int kSmemBytes =
-    1024 + kQBytes + kStages * (kKBytes + kVBytes) + 2 * kPBytes + 8 * kNumBars + 16;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;       // S0 [0,128), S1 [128,256), O [256,320)
-constexpr uint32_t kTmemO = 256;
+constexpr int kPBytes = kBQ * kBKV * 2;   // 32 KiB per tile: two 16 KiB K-major atoms of 64 keys
+constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + 5 * kTiles;
+constexpr int kSmemBytes = 1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) +
+                           kTiles * kPBytes + 8 * kNumBars + 16;
+constexpr int kThreads = 32 * (1 + kTiles + 4 * kTiles);   // producer, an MMA warp and a
+                                                           // softmax warpgroup per tile
+constexpr uint32_t kTmemCols = 512;       // S_t at 128 t, O_t at 256 + 64 t
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -66,7 +73,8 @@ struct AttnParams {
     int32_t o_vec;         // 16-byte stores of O rows are legal
     int32_t seq;
     int32_t causal;
-    int32_t ntiles;        // query blocks per head
+    int32_t ntiles;        // query tiles per head
+    int32_t npairs;        // CTAs per head (tiles 2c and 2c+1)
     float c;               // log2(e) / sqrt(d)
     uint64_t timeout_ns;
 };
@@ -79,45 +87,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = sQ + kQBytes;
+    uint8_t* sQ = smem;                                  // tile t at t * kQBytes
+    uint8_t* sK = sQ + kTiles * kQBytes;
     uint8_t* sV = sK + kStages * kKBytes;
-    uint8_t* sP = sV + kStages * kVBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
+    uint8_t* sP = sV + kStages * kVBytes;                // tile t at t * kPBytes
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTiles * kPBytes);
     uint64_t* q_full = bars;
     uint64_t* k_full = q_full + 1;
     uint64_t* v_full = k_full + kStages;
-    uint64_t* kv_empty = v_full + kStages;
-    uint64_t* s_full = kv_empty + kStages;
-    uint64_t* s_empty = s_full + 2;
-    uint64_t* p_full = s_empty + 2;
-    uint64_t* pv_done = p_full + 2;
-    uint64_t* drain = pv_done + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* kv_empty = v_full + kStages;               // [tile][stage]
+    uint64_t* s_full = kv_empty + kTiles * kStages;      // [tile]
+    uint64_t* s_empty = s_full + kTiles;
+    uint64_t* p_full = s_empty + kTiles;
+    uint64_t* pv_done = p_full + kTiles;
+    uint64_t* drain = pv_done + kTiles;                  // [tile]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kTiles);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int h = blockIdx.y;
-    const int qt = p.causal ? (p.ntiles - 1 - static_cast<int>(blockIdx.x))
-                            : static_cast<int>(blockIdx.x);   // heavy causal blocks first
-    const int q0 = qt * kBQ;
-    const int nkv = p.causal ? qt + 1 : (p.seq + kBKV - 1) / kBKV;
+    const int pair = p.causal ? (p.npairs - 1 - static_cast<int>(blockIdx.x))
+                              : static_cast<int>(blockIdx.x);   // heavy causal pairs first
+    // Key blocks each tile needs (0 for a tile beyond the sequence).
+    int nkv[kTiles];
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) {
+        const int qt = pair * kTiles + t;
+        nkv[t] = qt >= p.ntiles ? 0 : (p.causal ? qt + 1 : (p.seq + kBKV - 1) / kBKV);
+    }
+    const int nkv_max = nkv[kTiles - 1] > nkv[0] ? nkv[kTiles - 1] : nkv[0];
 
     if (threadIdx.x == 0) {
         dg::mbar_init(dg::smem_u32(q_full), 1u);
         for (int s = 0; s < kStages; ++s) {
             dg::mbar_init(dg::smem_u32(&k_full[s]), 1u);
             dg::mbar_init(dg::smem_u32(&v_full[s]), 1u);
-            dg::mbar_init(dg::smem_u32(&kv_empty[s]), 1u);
         }
-        for (int b = 0; b < 2; ++b) {
-            dg::mbar_init(dg::smem_u32(&s_full[b]), 1u);
-            dg::mbar_init(dg::smem_u32(&s_empty[b]), 128u);
-            dg::mbar_init(dg::smem_u32(&p_full[b]), 128u);
+        for (int s = 0; s < kTiles * kStages; ++s) dg::mbar_init(dg::smem_u32(&kv_empty[s]), 1u);
+        for (int t = 0; t < kTiles; ++t) {
+            dg::mbar_init(dg::smem_u32(&s_full[t]), 1u);
+            dg::mbar_init(dg::smem_u32(&s_empty[t]), 128u);
+            dg::mbar_init(dg::smem_u32(&p_full[t]), 128u);
+            dg::mbar_init(dg::smem_u32(&pv_done[t]), 1u);
         }
-        dg::mbar_init(dg::smem_u32(pv_done), 1u);
-        dg::mbar_init(dg::smem_u32(drain), 1u);
+        for (int t = 0; t < kTiles; ++t) dg::mbar_init(dg::smem_u32(&drain[t]), 1u);
         *abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -144,13 +158,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint32_t qb = dg::smem_u32(q_full);
-            dg::mbar_arrive_expect_tx(qb, kQBytes);
-            dg::tma_load_3d(dg::smem_u32(sQ), &mapQ, qb, 0, q0, h);
-            for (int j = 0; j < nkv; ++j) {
+            dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
+            for (int t = 0; t < kTiles; ++t)
+                dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes), &mapQ, qb, 0,
+                                (pair * kTiles + t) * kBQ, h);
+            bool ok = true;
+            for (int j = 0; ok && j < nkv_max; ++j) {
                 const int st = j % kStages;
                 const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
-                if (!dg::mbar_wait(dg::smem_u32(&kv_empty[st]), ph ^ 1u, abort_flag,
-                                   p.timeout_ns)) {
+                // The stage held block j - kStages: every tile that used it must be done.
+                for (int t = 0; t < kTiles; ++t)
+                    if (j >= kStages && j - kStages < nkv[t] &&
+                        !dg::mbar_wait(dg::smem_u32(&kv_empty[t * kStages + st]), ph ^ 1u,
+                                       abort_flag, p.timeout_ns))
+                        ok = false;
+                if (!ok) {
                     fail();
                     break;
                 }
@@ -165,96 +187,101 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp <= kTiles) {
+        // ------------------------------------------------------------ MMA issuers
+        // One warp per query tile, so that neither tile's pace holds up the
+        // other: S_t(j+1) as soon as the tile's softmax has read S_t(j) out of
+        // TMEM and K_{j+1} has landed, then P_t(j) V_j once P_t(j) is in
+        // shared memory; each softmax warpgroup finds its next scores ready
+        // when it finishes a block.
+        const int t = warp - 1;
         if (lane == 0) {
             constexpr uint32_t idesc_s = dg::idesc_f16(BF16, false, false, kBQ, kBKV);
             constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
-            const uint32_t q_addr = dg::smem_u32(sQ);
-            bool ok = dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
+            const int n = nkv[t];
+            const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
+            const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t * kBKV);
+            const uint32_t o_tmem = tmem_base + 256u + static_cast<uint32_t>(t * kD);
+            bool ok = n == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
             auto issue_s = [&](int jj) -> bool {
-                const int st = jj % kStages;
-                const int b = jj & 1;
-                if (!dg::mbar_wait(dg::smem_u32(&s_empty[b]),
-                                   (static_cast<uint32_t>(jj >> 1) & 1u) ^ 1u, abort_flag,
-                                   p.timeout_ns))
-                    return false;
-                if (!dg::mbar_wait(dg::smem_u32(&k_full[st]),
+                // K_jj landed, and the tile's score buffer was read (jj-th use).
+                if (!dg::mbar_wait(dg::smem_u32(&k_full[jj % kStages]),
                                    static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
-                                   p.timeout_ns))
+                                   p.timeout_ns) ||
+                    !dg::mbar_wait(dg::smem_u32(&s_empty[t]), (static_cast<uint32_t>(jj) & 1u) ^ 1u,
+                                   abort_flag, p.timeout_ns))
                     return false;
                 dg::tc_fence_after();
-                const uint32_t k_addr = dg::smem_u32(sK + st * kKBytes);
+                const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
 #pragma unroll
                 for (int k16 = 0; k16 < kD / 16; ++k16)
-                    dg::tc_mma_f16(tmem_base + static_cast<uint32_t>(b * kBKV),
-                                   dg::operand_desc<false>(q_addr, k16),
+                    dg::tc_mma_f16(s_tmem, dg::operand_desc<false>(q_addr, k16),
                                    dg::operand_desc<false>(k_addr, k16), idesc_s,
                                    k16 > 0 ? 1u : 0u);
-                dg::tc_commit(dg::smem_u32(&s_full[b]));
+                dg::tc_commit(dg::smem_u32(&s_full[t]));
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < nkv; ++j) {
-                if (j + 1 < nkv && !issue_s(j + 1)) {
+            if (ok && n > 0) ok = issue_s(0);
+            for (int j = 0; ok && j < n; ++j) {
+                const int st = j % kStages;
+                if (j + 1 < n && !issue_s(j + 1)) {
                     ok = false;
                     break;
                 }
-                const int b = j & 1;
-                const int st = j % kStages;
-                if (!dg::mbar_wait(dg::smem_u32(&p_full[b]), static_cast<uint32_t>(j >> 1) & 1u,
+                if (!dg::mbar_wait(dg::smem_u32(&v_full[st]), static_cast<uint32_t>(j / kStages) & 1u,
                                    abort_flag, p.timeout_ns) ||
-                    !dg::mbar_wait(dg::smem_u32(&v_full[st]),
-                                   static_cast<uint32_t>(j / kStages) & 1u, abort_flag,
-                                   p.timeout_ns)) {
+                    !dg::mbar_wait(dg::smem_u32(&p_full[t]), static_cast<uint32_t>(j) & 1u,
+                                   abort_flag, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 dg::tc_fence_after();
-                const uint32_t p_addr = dg::smem_u32(sP + b * kPBytes);
+                const uint32_t p_addr = dg::smem_u32(sP + t * kPBytes);
                 const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
 #pragma unroll
                 for (int half = 0; half < 2; ++half)
 #pragma unroll
                     for (int k16 = 0; k16 < 4; ++k16)
-                        dg::tc_mma_f16(
-                            tmem_base + kTmemO,
-                            dg::operand_desc<false>(p_addr + half * (kPBytes / 2), k16),
-                            dg::operand_desc<true>(v_addr + half * (kVBytes / 2), k16), idesc_pv,
-                            (j > 0 || half > 0 || k16 > 0) ? 1u : 0u);
-                dg::tc_commit(dg::smem_u32(&kv_empty[st]));
-                dg::tc_commit(dg::smem_u32(pv_done));
+                        dg::tc_mma_f16(o_tmem,
+                                       dg::operand_desc<false>(p_addr + half * (kPBytes / 2), k16),
+                                       dg::operand_desc<true>(v_addr + half * (kVBytes / 2), k16),
+                                       idesc_pv, (j > 0 || half > 0 || k16 > 0) ? 1u : 0u);
+                dg::tc_commit(dg::smem_u32(&pv_done[t]));
+                dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
             }
             if (!ok) fail();
-            // Every MMA issued must have completed (and signalled its barriers)
-            // before the CTA's shared memory and TMEM go away.
+            // Every MMA this thread issued must have completed (and signalled its
+            // barriers) before the CTA's shared memory and TMEM go away.
             const volatile int never = 0;
-            dg::tc_commit(dg::smem_u32(drain));
-            dg::mbar_wait(dg::smem_u32(drain), 0u, &never, 100000000ull);
+            dg::tc_commit(dg::smem_u32(&drain[t]));
+            dg::mbar_wait(dg::smem_u32(&drain[t]), 0u, &never, 100000000ull);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
+        const int t = (warp - 1 - kTiles) >> 2;         // query tile of this warpgroup
         const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;            // query row in the tile == TMEM lane
-        const int qrow = q0 + r;
+        const int r = quarter * 32 + lane;              // query row in the tile == TMEM lane
+        const int qrow = (pair * kTiles + t) * kBQ + r;
+        const int qt = pair * kTiles + t;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t s_addr = lane_addr + static_cast<uint32_t>(t * kBKV);
+        const uint32_t o_addr = lane_addr + 256u + static_cast<uint32_t>(t * kD);
+        const uint32_t pbuf = dg::smem_u32(sP + t * kPBytes);
         const int ptype = BF16 ? dg::kOutBF16 : dg::kOutF16;
+        const int n = nkv[t];
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1;
-            const bool got = dg::mbar_wait(dg::smem_u32(&s_full[b]),
-                                           static_cast<uint32_t>(j >> 1) & 1u, abort_flag,
-                                           p.timeout_ns);
+        for (int j = 0; j < n; ++j) {
+            const bool got = dg::mbar_wait(dg::smem_u32(&s_full[t]), static_cast<uint32_t>(j) & 1u,
+                                           abort_flag, p.timeout_ns);
             if (!__all_sync(0xffffffffu, got)) {   // tcgen05.ld is warp-collective
                 ok = false;
                 break;
             }
             dg::tc_fence_after();
-            // S_j row: all four 32-column loads in flight before one wait; the
+            // S_t(j) row: all four 32-column loads in flight before one wait; the
             // score buffer is handed back as soon as the values are in registers.
-            const uint32_t s_addr = lane_addr + static_cast<uint32_t>(b * kBKV);
             uint32_t v0[32], v1[32], v2[32], v3[32];
             dg::tmem_ld_32x32b_x32(s_addr, v0);
             dg::tmem_ld_32x32b_x32(s_addr + 32u, v1);
@@ -265,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dg::tmem_ld_wait(v2);
             dg::tmem_ld_wait(v3);
             dg::tc_fence_before();
-            dg::mbar_arrive(dg::smem_u32(&s_empty[b]));     // S buffer b may be refilled
+            dg::mbar_arrive(dg::smem_u32(&s_empty[t]));     // the MMA may write S_t(j+1)
             float x[kBKV];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -292,31 +319,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mc = m_new * p.c;
             const float alpha = dg::ex2_approx(m * p.c - mc);   // 0 on the first block
             float sums[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t pbuf = dg::smem_u32(sP + b * kPBytes);
 #pragma unroll
-            for (int c8 = 0; c8 < kBKV / 8; ++c8) {            // 8-key chunks 0..15
-                float pv[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    pv[t] = dg::ex2_approx(fmaf(x[c8 * 8 + t], p.c, -mc));
-                    sums[t & 3] += pv[t];
-                }
-                uint4 w;
-                w.x = dg::pack_out(pv[0], pv[1], ptype);
-                w.y = dg::pack_out(pv[2], pv[3], ptype);
-                w.z = dg::pack_out(pv[4], pv[5], ptype);
-                w.w = dg::pack_out(pv[6], pv[7], ptype);
-                dg::st_shared_v4_b32(pbuf + static_cast<uint32_t>((c8 >> 3) * (kPBytes / 2)) +
-                                         dg::chunk_offset<false>(r, c8 & 7),
-                                     w);
+            for (int i = 0; i < kBKV; ++i) {
+                x[i] = dg::ex2_approx(fmaf(x[i], p.c, -mc));
+                sums[i & 3] += x[i];
             }
-            const float rs = (sums[0] + sums[1]) + (sums[2] + sums[3]);
-            l = l * alpha + rs;
-            dg::fence_proxy_async_smem();     // P_j -> visible to the tensor cores
+            l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
             if (j > 0) {
-                // O holds the sum up to block j-1 once P_{j-1} V_{j-1} is done;
-                // rescale it to the new maximum before P_j V_j is added.
-                const bool done = dg::mbar_wait(dg::smem_u32(pv_done),
+                // P_t(j-1) V_{j-1} must be done: it read the P buffer about to be
+                // rewritten, and O_t must hold its sum before the rescale.
+                const bool done = dg::mbar_wait(dg::smem_u32(&pv_done[t]),
                                                 static_cast<uint32_t>(j - 1) & 1u, abort_flag,
                                                 p.timeout_ns);
                 if (!__all_sync(0xffffffffu, done)) {
@@ -324,41 +336,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 dg::tc_fence_after();
-                if (!__all_sync(0xffffffffu, alpha == 1.0f)) {
+            }
 #pragma unroll
-                    for (int ch = 0; ch < kD / 32; ++ch) {
-                        uint32_t v[32];
-                        const uint32_t ta = lane_addr + kTmemO + static_cast<uint32_t>(ch * 32);
-                        dg::tmem_ld_32x32b_x32(ta, v);
-                        dg::tmem_ld_wait(v);
+            for (int c8 = 0; c8 < kBKV / 8; ++c8) {            // 8-key chunks 0..15
+                uint4 w;
+                w.x = dg::pack_out(x[8 * c8], x[8 * c8 + 1], ptype);
+                w.y = dg::pack_out(x[8 * c8 + 2], x[8 * c8 + 3], ptype);
+                w.z = dg::pack_out(x[8 * c8 + 4], x[8 * c8 + 5], ptype);
+                w.w = dg::pack_out(x[8 * c8 + 6], x[8 * c8 + 7], ptype);
+                dg::st_shared_v4_b32(pbuf + static_cast<uint32_t>((c8 >> 3) * (kPBytes / 2)) +
+                                         dg::chunk_offset<false>(r, c8 & 7),
+                                     w);
+            }
+            dg::fence_proxy_async_smem();     // P_t(j) -> visible to the tensor cores
+            if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
+                // Rescale O_t to the new maximum before P_t(j) V_j is added.
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        dg::tmem_st_32x32b_x32(ta, v);
-                    }
-                    dg::tmem_st_wait();
+                for (int ch = 0; ch < kD / 32; ++ch) {
+                    uint32_t v[32];
+                    const uint32_t ta = o_addr + static_cast<uint32_t>(ch * 32);
+                    dg::tmem_ld_32x32b_x32(ta, v);
+                    dg::tmem_ld_wait(v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    dg::tmem_st_32x32b_x32(ta, v);
                 }
+                dg::tmem_st_wait();
             }
             dg::tc_fence_before();
-            dg::mbar_arrive(dg::smem_u32(&p_full[b]));
+            dg::mbar_arrive(dg::smem_u32(&p_full[t]));
             m = m_new;
         }
-        if (ok) {
-            const bool done = dg::mbar_wait(dg::smem_u32(pv_done),
-                                            static_cast<uint32_t>(nkv - 1) & 1u, abort_flag,
+        if (ok && n > 0) {
+            const bool done = dg::mbar_wait(dg::smem_u32(&pv_done[t]),
+                                            static_cast<uint32_t>(n - 1) & 1u, abort_flag,
                                             p.timeout_ns);
             ok = __all_sync(0xffffffffu, done);
         }
         if (!ok) {
             fail();
-        } else {
+        } else if (n > 0) {
             dg::tc_fence_after();
             const float inv = 1.0f / l;
             uint32_t o[kD];
 #pragma unroll
             for (int ch = 0; ch < kD / 32; ++ch) {
                 uint32_t v[32];
-                dg::tmem_ld_32x32b_x32(lane_addr + kTmemO + static_cast<uint32_t>(ch * 32), v);
+                dg::tmem_ld_32x32b_x32(o_addr + static_cast<uint32_t>(ch * 32), v);
                 dg::tmem_ld_wait(v);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[ch * 32 + i] = __float_as_uint(__uint_as_float(v[i]) * inv);
@@ -550,7 +575,7 @@ gemm_status_t attention_fwd_query(const void* Q, const void* K, const void* V, c
     out->block_kv = kBKV;
     out->head_dim = static_cast<int32_t>(d);
     out->stages = kStages;
-    out->grid_x = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
+    out->grid_x = static_cast<int32_t>(((seq + kBQ - 1) / kBQ + kTiles - 1) / kTiles);
     out->grid_y = static_cast<int32_t>(BH);
     out->causal = causal ? 1 : 0;
     return GEMM_OK;
@@ -597,9 +622,10 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
     p.seq = static_cast<int32_t>(seq);
     p.causal = causal ? 1 : 0;
     p.ntiles = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
+    p.npairs = (p.ntiles + kTiles - 1) / kTiles;
     p.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.timeout_ns = kTimeoutNs;
-    const dim3 grid(static_cast<unsigned>(p.ntiles), static_cast<unsigned>(BH));
+    const dim3 grid(static_cast<unsigned>(p.npairs), static_cast<unsigned>(BH));
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
