@@ -11,20 +11,21 @@
 // masked element by element.
 //
 // GB300 mapping: one CTA per SM holds two query tiles of one head (A, B)
-// that share every K/V block (512 TMEM columns, ~190 KiB of shared memory):
+// that share every K/V block (512 TMEM columns, ~130 KiB of shared memory):
 //   warp 0      TMA producer: both Q tiles once, then K and V blocks into a
 //               3-stage ring (3-D tensor maps over [BH, seq, d]).
 //   warps 1, 2  one MMA issuer per tile (warp 1 also owns TMEM):
 //               S_t(j+1) = Q_t K^T (M 128, N 128, K 64) into the tile's TMEM
 //               score buffer as soon as the tile's softmax has read S_t(j),
-//               then O_t += P_t(j) V_j (M 128, N 64, K 128) once P_t(j) is in
-//               shared memory; a K/V stage is refilled when every tile that
-//               used it has committed its release.
+//               then O_t += P_t(j) V_j (M 128, N 64, K 128) with P_t(j) read
+//               from TMEM once the softmax has stored it there; a K/V stage
+//               is refilled when every tile that used it has committed its
+//               release.
 //   warps 3..10 two softmax warpgroups, one per tile, one thread per query
 //               row (= TMEM lane): read S_t(j) from TMEM, mask, row max,
 //               p = 2^(s*c - m*c) with c = log2(e)/sqrt(d), row sum, P_t(j)
-//               rounded to the input type into shared memory in the operand
-//               layout of the second MMA, and the rescale of O_t in TMEM
+//               rounded to the input type into TMEM (the A operand of the
+//               second MMA), and the rescale of O_t in TMEM
 //               (load, multiply by alpha, store) after P_t(j-1) V_{j-1} has
 //               finished.  At the end O_t / l goes to global memory.  The two
 //               warpgroups interleave on the SM's exponential units and issue
@@ -55,13 +56,15 @@ constexpr int kStages = 3;                // K/V ring depth
 constexpr int kQBytes = kBQ * kD * 2;     // 16 KiB per tile: 128 rows of 128 B (K-major operand)
 constexpr int kKBytes = kBKV * kD * 2;    // 16 KiB: K-major operand, N = keys
 constexpr int kVBytes = kBKV * kD * 2;    // 16 KiB: two 8 KiB MN-major halves of 64 keys
-constexpr int kPBytes = kBQ * kBKV * 2;   // 32 KiB per tile: two 16 KiB K-major atoms of 64 keys
 constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + 5 * kTiles;
-constexpr int kSmemBytes = 1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) +
-                           kTiles * kPBytes + 8 * kNumBars + 16;
+constexpr int kSmemBytes =
+    1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
 constexpr int kThreads = 32 * (1 + kTiles + 4 * kTiles);   // producer, an MMA warp and a
                                                            // softmax warpgroup per tile
-constexpr uint32_t kTmemCols = 512;       // S_t at 128 t, O_t at 256 + 64 t
+constexpr uint32_t kTmemCols = 512;       // per tile t at 256 t: S (128 columns of fp32),
+constexpr uint32_t kTmemP = 128;          //   P (64 columns, two 16-bit values each),
+constexpr uint32_t kTmemO = 192;          //   O (64 columns of fp32)
+constexpr uint32_t kTmemTile = 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 static_assert(kSmemBytes <= 232448, "shared memory");
@@ -90,8 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sQ = smem;                                  // tile t at t * kQBytes
     uint8_t* sK = sQ + kTiles * kQBytes;
     uint8_t* sV = sK + kStages * kKBytes;
-    uint8_t* sP = sV + kStages * kVBytes;                // tile t at t * kPBytes
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kTiles * kPBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kStages * kVBytes);
     uint64_t* q_full = bars;
     uint64_t* k_full = q_full + 1;
     uint64_t* v_full = k_full + kStages;
@@ -200,8 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
             const int n = nkv[t];
             const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
-            const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t * kBKV);
-            const uint32_t o_tmem = tmem_base + 256u + static_cast<uint32_t>(t * kD);
+            const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile;
+            const uint32_t p_tmem = s_tmem + kTmemP;
+            const uint32_t o_tmem = s_tmem + kTmemO;
             bool ok = n == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
             auto issue_s = [&](int jj) -> bool {
                 // K_jj landed, and the tile's score buffer was read (jj-th use).
@@ -236,16 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 dg::tc_fence_after();
-                const uint32_t p_addr = dg::smem_u32(sP + t * kPBytes);
                 const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
+                // P_t(j) from TMEM (8 columns = 16 keys per MMA), V_j from shared memory.
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
-#pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16)
-                        dg::tc_mma_f16(o_tmem,
-                                       dg::operand_desc<false>(p_addr + half * (kPBytes / 2), k16),
-                                       dg::operand_desc<true>(v_addr + half * (kVBytes / 2), k16),
-                                       idesc_pv, (j > 0 || half > 0 || k16 > 0) ? 1u : 0u);
+                for (int k16 = 0; k16 < kBKV / 16; ++k16)
+                    dg::tc_mma_f16_ts(o_tmem, p_tmem + static_cast<uint32_t>(k16 * 8),
+                                      dg::operand_desc<true>(v_addr + (k16 >> 2) * (kVBytes / 2),
+                                                             k16 & 3),
+                                      idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);
                 dg::tc_commit(dg::smem_u32(&pv_done[t]));
                 dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
             }
@@ -265,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = (pair * kTiles + t) * kBQ + r;
         const int qt = pair * kTiles + t;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t s_addr = lane_addr + static_cast<uint32_t>(t * kBKV);
-        const uint32_t o_addr = lane_addr + 256u + static_cast<uint32_t>(t * kD);
-        const uint32_t pbuf = dg::smem_u32(sP + t * kPBytes);
+        const uint32_t s_addr = lane_addr + static_cast<uint32_t>(t) * kTmemTile;
+        const uint32_t p_addr = s_addr + kTmemP;
+        const uint32_t o_addr = s_addr + kTmemO;
         const int ptype = BF16 ? dg::kOutBF16 : dg::kOutF16;
         const int n = nkv[t];
         float m = -INFINITY, l = 0.0f;
@@ -318,11 +319,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_new = fmaxf(m, mb);
             const float mc = m_new * p.c;
             const float alpha = dg::ex2_approx(m * p.c - mc);   // 0 on the first block
+            // p = 2^(s*c - m*c), summed in fp32 and packed two per 32-bit word
+            // (rounded to the input type) as they are made.
             float sums[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            uint32_t pw[kBKV / 2];
 #pragma unroll
-            for (int i = 0; i < kBKV; ++i) {
-                x[i] = dg::ex2_approx(fmaf(x[i], p.c, -mc));
-                sums[i & 3] += x[i];
+            for (int i = 0; i < kBKV / 2; ++i) {
+                const float a = dg::ex2_approx(fmaf(x[2 * i], p.c, -mc));
+                const float bb = dg::ex2_approx(fmaf(x[2 * i + 1], p.c, -mc));
+                sums[(2 * i) & 3] += a;
+                sums[(2 * i + 1) & 3] += bb;
+                pw[i] = dg::pack_out(a, bb, ptype);
             }
             l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
             if (j > 0) {
@@ -337,18 +344,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 dg::tc_fence_after();
             }
+            // P_t(j) into TMEM: this row's 128 weights, two per 32-bit column
+            // (the A operand of the P V MMA).
+            {
+                uint32_t w0[32], w1[32];
 #pragma unroll
-            for (int c8 = 0; c8 < kBKV / 8; ++c8) {            // 8-key chunks 0..15
-                uint4 w;
-                w.x = dg::pack_out(x[8 * c8], x[8 * c8 + 1], ptype);
-                w.y = dg::pack_out(x[8 * c8 + 2], x[8 * c8 + 3], ptype);
-                w.z = dg::pack_out(x[8 * c8 + 4], x[8 * c8 + 5], ptype);
-                w.w = dg::pack_out(x[8 * c8 + 6], x[8 * c8 + 7], ptype);
-                dg::st_shared_v4_b32(pbuf + static_cast<uint32_t>((c8 >> 3) * (kPBytes / 2)) +
-                                         dg::chunk_offset<false>(r, c8 & 7),
-                                     w);
+                for (int i = 0; i < 32; ++i) {
+                    w0[i] = pw[i];
+                    w1[i] = pw[32 + i];
+                }
+                dg::tmem_st_32x32b_x32(p_addr, w0);
+                dg::tmem_st_32x32b_x32(p_addr + 32u, w1);
             }
-            dg::fence_proxy_async_smem();     // P_t(j) -> visible to the tensor cores
+            dg::tmem_st_wait();
             if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
                 // Rescale O_t to the new maximum before P_t(j) V_j is added.
 #pragma unroll
