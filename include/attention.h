@@ -52,7 +52,7 @@ typedef struct {
     int32_t block_kv;     /* keys per step of the online softmax */
     int32_t head_dim;
     int32_t stages;       /* K/V shared-memory ring depth */
-    int32_t grid_x;       /* query blocks per head */
+    int32_t grid_x;       /* CTAs per head (each holds two query blocks) */
     int32_t grid_y;       /* heads */
     int32_t causal;
 } attention_config_t;

@@ -119,4 +119,5 @@ def test_attention_argument_checks_need_no_gpu():
     with pytest.raises(g.GemmError):
         g.attention_fwd_query(a, b, c, o, -1, 8, 64, 64, 512, 64, 512, 0, F16, F32)
     cfg = g.attention_fwd_query(a, b, c, o, 3, 1000, 64, 64, 64000, 64, 64000, 1, BF16, F32)
-    assert cfg["grid_x"] == 8 and cfg["grid_y"] == 3 and cfg["block_q"] == 128 and cfg["causal"] == 1
+    # 8 query blocks of 128 per head, two per CTA
+    assert cfg["grid_x"] == 4 and cfg["grid_y"] == 3 and cfg["block_q"] == 128 and cfg["causal"] == 1
