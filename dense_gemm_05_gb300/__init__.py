@@ -74,7 +74,7 @@ class GemmError(RuntimeError):
 class GemmConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("kernel", "block_m", "block_n", "block_k", "stages", "split_k", "grid",
-                 "cluster", "group", "tiles", "shares")]
+                 "cluster", "group", "tiles", "shares", "staged")]
 
     def as_dict(self) -> dict:
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}

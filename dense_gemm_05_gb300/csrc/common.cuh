@@ -170,6 +170,11 @@ cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
                         const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
                         uint32_t idesc, int grid, cudaStream_t stream);
 
+// Copy a rows x cols 16-bit matrix (pitch lds) into dst with pitch ldd (a multiple
+// of 8 elements, dst 16-byte aligned), zero-filling columns [cols, ldd).
+cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
+                              int64_t rows, int64_t cols, int num_sms, cudaStream_t stream);
+
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);
 

@@ -39,6 +39,8 @@ struct gemm_plan_s {
     int* counters = nullptr;      // split-K per-tile arrival counters (kept at zero)
     int counters_len = 0;
     int* status = nullptr;        // device error word
+    uint16_t* stage = nullptr;    // copies of operands whose rows are not 16-byte aligned
+    size_t stage_bytes = 0;
     int group = 8;
     int force_kernel = 0;
     int force_split = 0;
@@ -52,6 +54,7 @@ namespace {
 
 constexpr size_t kWorkspaceBytes = size_t(64) << 20;   // split-K / stream-K partials
 constexpr int64_t kPairMinShareKb = 16;   // a pair stream-K share streams at least this many K blocks
+constexpr size_t kStageBytes = size_t(32) << 20;       // staging copies of misaligned operands
 constexpr int kMaxCounters = 1 << 16;                   // output tiles that may be split
 constexpr int64_t kMaxDim = INT32_MAX - 1024;   // headroom for tile-edge arithmetic in int32
 
@@ -250,6 +253,48 @@ bool choose_shares(const gemm_plan_s* plan, Choice* c, int64_t shares) {
         most = std::max<int>(most, static_cast<int>(last - first + 1));
     }
     c->split = most;
+    return true;
+}
+
+// Operands whose base or row pitch is not a multiple of 16 bytes cannot be read
+// by TMA.  When they fit in the plan's staging buffer they are copied there
+// first, rows padded to a multiple of 8 elements, and the TMA kernels read the
+// copies; otherwise (or with the generic kernel forced) the generic kernel
+// reads them in place.  `out` gets the arguments the GEMM kernel will see.
+struct Staging {
+    bool a = false, b = false;
+    int64_t lda = 0, ldb = 0;
+    size_t off_b = 0;
+};
+
+bool plan_staging(const gemm_plan_s* plan, const Args& a, Staging* st, Args* out) {
+    *out = a;
+    *st = Staging{};
+    if (plan->force_kernel == GEMM_KERNEL_GENERIC || plan->stage == nullptr || a.M == 0 ||
+        a.N == 0 || a.K == 0)
+        return false;
+    const bool a_bad = !tma_ok(a.A, a.lda);
+    const bool b_bad = !tma_ok(a.B, a.ldb);
+    if (!a_bad && !b_bad) return false;
+    const int64_t lda2 = (a.a_cols() + 7) / 8 * 8;
+    const int64_t ldb2 = (a.b_cols() + 7) / 8 * 8;
+    const uint64_t bytes_a = a_bad ? static_cast<uint64_t>(a.a_rows()) * lda2 * 2 : 0;
+    const uint64_t off_b = (bytes_a + 255) / 256 * 256;
+    const uint64_t bytes_b = b_bad ? static_cast<uint64_t>(a.b_rows()) * ldb2 * 2 : 0;
+    if (off_b + bytes_b > plan->stage_bytes) return false;
+    st->a = a_bad;
+    st->b = b_bad;
+    st->lda = lda2;
+    st->ldb = ldb2;
+    st->off_b = static_cast<size_t>(off_b);
+    if (a_bad) {
+        out->A = plan->stage;
+        out->lda = lda2;
+    }
+    if (b_bad) {
+        out->B = reinterpret_cast<const uint8_t*>(plan->stage) + off_b;
+        out->ldb = ldb2;
+    }
     return true;
 }
 
@@ -465,15 +510,18 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     }
     if (cudaMalloc(&p->ws, kWorkspaceBytes) != cudaSuccess ||
         cudaMalloc(&p->counters, sizeof(int) * kMaxCounters) != cudaSuccess ||
-        cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+        cudaMalloc(&p->status, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&p->stage, kStageBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         cudaFree(p->ws);
         cudaFree(p->counters);
         cudaFree(p->status);
+        cudaFree(p->stage);
         delete p;
         return GEMM_ERR_OOM;
     }
     p->ws_bytes = kWorkspaceBytes;
+    p->stage_bytes = kStageBytes;
     p->counters_len = kMaxCounters;
     if (cudaMemset(p->counters, 0, sizeof(int) * kMaxCounters) != cudaSuccess ||
         cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
@@ -494,6 +542,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     cudaFree(plan->ws);
     cudaFree(plan->counters);
     cudaFree(plan->status);
+    cudaFree(plan->stage);
     delete plan;
     return GEMM_OK;
 }
@@ -530,10 +579,13 @@ gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int32
 
 namespace {
 
-gemm_status_t query_impl(gemm_plan_t plan, const Args& a, gemm_config_t* out) {
+gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out) {
     if (plan == nullptr || out == nullptr) return GEMM_ERR_INVALID_ARG;
-    gemm_status_t st = check_args(a);
+    gemm_status_t st = check_args(a_in);
     if (st != GEMM_OK) return st;
+    Args a;
+    Staging sg;
+    plan_staging(plan, a_in, &sg, &a);
     Choice c;
     st = choose(plan, a, &c);
     if (st != GEMM_OK) return st;
@@ -555,14 +607,18 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a, gemm_config_t* out) {
                     : 0;
     cfg.tiles = c.units;
     cfg.shares = c.shares;
+    cfg.staged = (sg.a ? 1 : 0) | (sg.b ? 2 : 0);
     *out = cfg;
     return GEMM_OK;
 }
 
-gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
+gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) {
     if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
-    gemm_status_t st = check_args(a);
+    gemm_status_t st = check_args(a_in);
     if (st != GEMM_OK) return st;
+    Args a;
+    Staging sg;
+    const bool staged = plan_staging(plan, a_in, &sg, &a);
     Choice c;
     st = choose(plan, a, &c);
     if (st != GEMM_OK) return st;
@@ -571,6 +627,22 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a, cudaStream_t stream) {
     DeviceGuard guard(plan->device);
     if (!guard.ok) return GEMM_ERR_CUDA;
     cudaError_t err = cudaSuccess;
+    if (staged) {
+        if (sg.a)
+            err = dg::launch_stage_rows(static_cast<const uint16_t*>(a_in.A), a_in.lda,
+                                        const_cast<uint16_t*>(static_cast<const uint16_t*>(a.A)),
+                                        a.lda, a_in.a_rows(), a_in.a_cols(), plan->num_sms,
+                                        stream);
+        if (err == cudaSuccess && sg.b)
+            err = dg::launch_stage_rows(static_cast<const uint16_t*>(a_in.B), a_in.ldb,
+                                        const_cast<uint16_t*>(static_cast<const uint16_t*>(a.B)),
+                                        a.ldb, a_in.b_rows(), a_in.b_cols(), plan->num_sms,
+                                        stream);
+        if (err != cudaSuccess) {
+            (void)cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
     const int64_t esize = a.c_esize();
 
     if (c.kernel == GEMM_KERNEL_ZERO_FILL) {

@@ -266,18 +266,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     for (int j = 0; j < 16; ++j) t[j] = __ldcg(src + (c0 / 4 + j) * 128 + lrow);
                 };
                 auto store_round = [&](int c0, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
-                    if (p.c_tma) {
-                        if (p.c_type == kOutF32) {
-                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
-                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0 + 32, hi,
-                                            lo);
-                        } else {
-                            epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
-                        }
-                    } else if (row < p.M) {
-                        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0 + c0;
-                        store_c32(p, off, lo, p.N - (col0 + c0));
-                        store_c32(p, off + 32, hi, p.N - (col0 + c0 + 32));
+                    if (p.c_type == kOutF32) {
+                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
+                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0 + 32, hi, lo);
+                    } else {
+                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
                     }
                 };
                 // Sum one 64-column round of the tile in share order.  fold: this
@@ -380,26 +373,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         if (et == 0) store_relaxed_gpu(counter, 0);
                     }
                 }
-            } else if (p.c_tma) {
-                epilogue_tma<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+            } else {
+                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
                                      mbar_arrive_cluster(tempty_peer0);
                                  });
-            } else {
-                const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
-                const bool row_ok = row < p.M;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(c * 32), v);
-                    tmem_ld_wait(v);
-                    if (c == BN / 32 - 1) {
-                        tc_fence_before();
-                        mbar_arrive_cluster(tempty_peer0);
-                    }
-                    if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
-                }
             }
             if (++acc == 2) {
                 acc = 0;

@@ -222,8 +222,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             const uint32_t tempty_bar = smem_u32(&tempty[acc]);
-            if (!GENERIC && p.c_tma) {
-                epilogue_tma<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+            if (!GENERIC) {
+                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
                                      mbar_arrive(tempty_bar);

@@ -74,6 +74,12 @@ __device__ __forceinline__ void st_shared_v4_b32(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -138,13 +138,16 @@ __device__ __forceinline__ void store_c32(const Params& p, int64_t off, const ui
     }
 }
 
-// ---------------------------------------------------------------- TMA-store epilogue
+// ---------------------------------------------------------------- staged epilogue
 // One epilogue warp owns 32 accumulator rows.  It writes C in chunks 128 bytes
 // wide (32 fp32 or 64 16-bit columns): the chunk goes to a 4 KiB shared buffer
 // of the warp in the 128-byte-swizzled layout (row r at r * 128, 16-byte piece
-// j at piece j ^ (r % 8), which spreads the warp's rows over all banks), and
-// lane 0 stores it with one TMA box {chunk columns, 32 rows}.  TMA clips the
-// box to the M x N rectangle, so ragged edges need no masking here.
+// j at piece j ^ (r % 8), which spreads the warp's rows over all banks).  With
+// c_tma, lane 0 stores it with one TMA box {chunk columns, 32 rows}, which the
+// hardware clips to the M x N rectangle.  Otherwise (a C that TMA cannot
+// address) the warp writes it back row by row, each row as 128 contiguous
+// bytes across the lanes, masked at M and N -- coalesced, where storing each
+// lane's own row directly would touch 32 rows per instruction.
 constexpr int kEpiBufBytes = 4096;             // per epilogue warp
 constexpr int kEpiSmemBytes = 4 * kEpiBufBytes;
 
@@ -157,7 +160,7 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
                                                 uint32_t buf, int lane, int row0, int col,
                                                 const uint32_t (&lo)[32],
                                                 const uint32_t (&hi)[32]) {
-    if (lane == 0) bulk_wait_group_read0();    // the previous chunk has left the buffer
+    if (p.c_tma && lane == 0) bulk_wait_group_read0();   // the previous chunk has left the buffer
     __syncwarp();
     const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
     if (p.c_type == kOutF32) {
@@ -178,20 +181,44 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
             st_shared_v4_b32(row + static_cast<uint32_t>((j ^ (lane & 7)) << 4), w);
         }
     }
-    fence_proxy_async_smem();                  // generic stores -> visible to the TMA engine
+    if (p.c_tma) {
+        fence_proxy_async_smem();              // generic stores -> visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && row0 < p.M && col < p.N) {
+            tma_store_2d(mapC, buf, col, row0);
+            bulk_commit_group();
+        }
+        return;
+    }
     __syncwarp();
-    if (lane == 0 && row0 < p.M && col < p.N) {
-        tma_store_2d(mapC, buf, col, row0);
-        bulk_commit_group();
+    // Lane l reads 32-bit word l of each 128-byte row (in 16-byte piece l / 4).
+    const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll 4
+    for (int rr = 0; rr < 32; ++rr) {
+        const int r = row0 + rr;
+        if (r >= p.M) break;
+        const uint32_t w = ld_shared_b32(buf + static_cast<uint32_t>(rr * 128) +
+                                         ((static_cast<uint32_t>((lane >> 2) ^ (rr & 7))) << 4) +
+                                         word);
+        const int64_t off = static_cast<int64_t>(r) * p.ldc;
+        if (p.c_type == kOutF32) {
+            const int c = col + lane;
+            if (c < p.N) static_cast<float*>(p.C)[off + c] = __uint_as_float(w);
+        } else {
+            const int c = col + 2 * lane;
+            uint16_t* dst = static_cast<uint16_t*>(p.C) + off;
+            if (c < p.N) dst[c] = static_cast<uint16_t>(w & 0xFFFFu);
+            if (c + 1 < p.N) dst[c + 1] = static_cast<uint16_t>(w >> 16);
+        }
     }
 }
 
 // The epilogue of one warp's 32 rows x BN columns of an accumulator at TMEM
-// address `taddr` (this warp's lanes), through TMA stores.  `release` is called
+// address `taddr` (this warp's lanes), through the staged chunks above.  `release` is called
 // after the last TMEM load, so the MMA issuer may reuse the accumulator while
 // the final chunks are still being stored.
 template <int BN, typename Release>
-__device__ __forceinline__ void epilogue_tma(const Params& p, const CUtensorMap* mapC,
+__device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorMap* mapC,
                                              uint32_t buf, uint32_t taddr, int lane, int row0,
                                              int col0, Release release) {
     const int cw = epi_chunk_cols(p.c_type);

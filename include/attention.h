@@ -48,7 +48,7 @@ extern "C" {
 #endif
 
 typedef struct {
-    int32_t block_q;      /* queries per CTA (TMEM lanes) */
+    int32_t block_q;      /* queries per block (TMEM lanes); a CTA holds two blocks */
     int32_t block_kv;     /* keys per step of the online softmax */
     int32_t head_dim;
     int32_t stages;       /* K/V shared-memory ring depth */

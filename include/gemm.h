@@ -103,12 +103,15 @@ typedef struct {
     int32_t tiles;        /* work units: output tiles, or stream-K shares for SKINNY */
     int32_t shares;       /* SKINNY: equal contiguous shares of the (tile, K block) iterations;
                              PAIR: shares (one per cluster) of the stream-K phase, 0 = none */
+    int32_t staged;       /* operands copied to 16-byte-aligned rows first: 1 = A, 2 = B, 3 = both */
 } gemm_config_t;
 
 /*
  * Create a plan on CUDA device `device` (that device becomes current for the
  * call).  Checks that the device is compute capability 10.3, queries the SM
- * count, sets kernel attributes and allocates the plan's workspace.
+ * count, sets kernel attributes and allocates the plan's workspace (64 MiB of
+ * split-K / stream-K partials, tile counters, a status word) and its 32 MiB
+ * staging buffer.
  * Errors: INVALID_ARG (out == NULL), UNSUPPORTED (not sm_103), CUDA, OOM.
  * On error *out is set to NULL.
  */
@@ -121,6 +124,12 @@ GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t *out, int device);
  * The region written, rows [0, M) x columns [0, N) of C, must not overlap the
  * regions read from A or B.
  * M == 0 or N == 0: no-op.  K == 0: C[0:M, 0:N] = 0.
+ * An operand whose base or row pitch is not a multiple of 16 bytes (e.g. an
+ * odd ld) is first copied by a kernel into the plan's 32 MiB staging buffer
+ * with rows padded to 16 bytes, when it fits (both together when both are),
+ * and the tensor-memory-access kernels read the copy; larger ones are read in
+ * place by the generic kernel.  Consecutive calls on one plan reuse the buffer
+ * in stream order.
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA (launch failure), TIMEOUT (only in
  * debug-sync mode).  Nothing is launched when an error is returned, except
  * for CUDA/TIMEOUT, which report a failure of the launched work itself.
@@ -194,7 +203,9 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  * by K across all clusters (any other value = automatic) -- and `block_n`
  * tile columns for TMA/PAIR (128 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
- * arguments (e.g. TMA with a leading dimension that is not a multiple of 8).
+ * arguments (e.g. SKINNY with M > 64, or TMA with an operand that is neither
+ * 16-byte aligned nor small enough for the staging buffer).  Forcing GENERIC
+ * also turns staging off (misaligned operands are read in place).
  * Errors: INVALID_ARG (null plan, unknown kernel, negative split, bad block_n).
  */
 GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,

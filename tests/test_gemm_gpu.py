@@ -91,12 +91,26 @@ def test_workload_256_f16_full(plan):
 
 
 def test_workload_ragged_f16_full(plan):
-    """M=1023 K=1000 N=1029: ldb = 1029 halves is not a 16-byte pitch -> generic producer."""
+    """M=1023 K=1000 N=1029: ldb = 1029 halves is not a 16-byte pitch -> B is staged
+    into 16-byte rows and the TMA kernel reads the copy."""
     w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
     A, B = workloads.make_inputs(w)
-    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_GENERIC)
+    dev = torch.device("cuda:0")
+    cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
+    assert cfg["kernel"] == g.GEMM_KERNEL_TMA and cfg["staged"] == 2, cfg
+    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_TMA)
     assert_guards(got, w.M, w.N)
     assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+
+
+def test_workload_ragged_f16_generic_in_place(plan):
+    """The same workload with the generic kernel forced: B read in place."""
+    w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
+    A, B = workloads.make_inputs(w)
+    got = run(plan, A, B, w.M, w.N, w.K, kernel=g.GEMM_KERNEL_GENERIC,
+              expect=g.GEMM_KERNEL_GENERIC)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " generic")
 
 
 def test_workload_ragged_f16_padded_pitch_uses_tma(plan):
@@ -378,6 +392,55 @@ def test_ragged_sweep(plan, M, N, K):
     assert_close(got[:M, :N], A, B, M, N, K, f"{M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (129, 257, 130), (17, 15, 63), (255, 128, 1000)])
+def test_ragged_sweep_generic_in_place(plan, M, N, K):
+    A, B = workloads.custom(M, K, N, "f16", seed=M + N + K)
+    got = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_GENERIC, expect=g.GEMM_KERNEL_GENERIC)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"generic {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,staged", [
+    (300, 520, 1001, 1001, 520, 1),      # A rows of 1001 halves
+    (300, 517, 1000, 1000, 517, 2),      # B rows of 517 halves
+    (1000, 1300, 777, 779, 1301, 3),     # both, with padding beyond K and N
+    (40, 3000, 1003, 1003, 3000, 1),     # skinny M with A staged
+])
+def test_staged_operands(plan, M, N, K, lda, ldb, staged):
+    A, B = workloads.custom(M, K, N, "bf16", seed=lda + ldb, dist="normal", lda=lda, ldb=ldb)
+    dev = torch.device("cuda:0")
+    cfg = plan.query(A.to(dev), B.to(dev), torch.empty(M, N, device=dev), M, N, K)
+    assert cfg["staged"] == staged and cfg["kernel"] != g.GEMM_KERNEL_GENERIC, cfg
+    got = run(plan, A, B, M, N, K, ldc=N + 1)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, f"staged {M}x{N}x{K}")
+
+
+def test_staged_misaligned_base_and_integer_exact(plan):
+    """A starting one element past a 16-byte boundary is staged; small integers stay exact."""
+    M, K, N = 500, 640, 384
+    A, B = int_inputs(M, K, N, "f16", seed=5)
+    dev = torch.device("cuda:0")
+    abuf = torch.zeros(M * K + 8, dtype=torch.float16, device=dev)
+    a = abuf[1:1 + M * K].view(M, K)
+    a.copy_(A.to(dev))
+    b = B.to(dev)
+    c = torch.full((M, N), SENTINEL, dtype=torch.float32, device=dev)
+    cfg = plan.query(a, b, c)
+    assert cfg["staged"] == 1, cfg
+    plan.run(a, b, c)
+    torch.cuda.synchronize()
+    assert np.array_equal(c.cpu().double().numpy(), oracle.gemm(A, B))
+
+
+def test_too_large_to_stage_uses_generic(plan):
+    M, K, N = 200, 4096, 4100
+    A, B = workloads.custom(M, K, N, "bf16", seed=3, dist="normal", ldb=4101)
+    got = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_GENERIC)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, "unstaged generic")
+
+
 @pytest.mark.parametrize("M,N,K", [(129, 257, 130), (17, 128, 63), (255, 15, 1000)])
 def test_ragged_sweep_padded_pitches_tma(plan, M, N, K):
     lda, ldb = -(-K // 8) * 8 + 8, -(-N // 8) * 8 + 8
@@ -448,9 +511,12 @@ def test_argument_errors(plan):
     assert g.gemm_run(h, A, 64, A, 64, A, 64, 32, 32, 64, g.GEMM_BF16, s) == E      # C overlaps A
     assert g.gemm_run(h, A, 64, A, 64, C, 64, 64, 64, 64, 7, s) == U                # dtype
     assert g.gemm_run(h, A, 64, A, 64, C, 64, 1 << 31, 64, 64, g.GEMM_BF16, s) == U
-    plan.force(g.GEMM_KERNEL_TMA, 0)
+    a2 = torch.ones(128, 64, dtype=torch.bfloat16, device=dev)
+    c2 = torch.empty(128, 64, dtype=torch.float32, device=dev)
+    plan.force(g.GEMM_KERNEL_SKINNY, 0)
     try:
-        assert g.gemm_run(h, A, 63, A, 64, C, 64, 64, 64, 63, g.GEMM_BF16, s) == U  # TMA pitch
+        assert g.gemm_run(h, a2.data_ptr(), 64, a2.data_ptr(), 64, c2.data_ptr(), 64, 65, 64, 64,
+                          g.GEMM_BF16, s) == U                                      # skinny M > 64
     finally:
         plan.force(0, 0)
     torch.cuda.synchronize()
@@ -465,7 +531,10 @@ def test_kernel_selection(plan):
         return plan.query(a, b, c, M, N, K)
     assert q(8192, 8192, 8192)["kernel"] == g.GEMM_KERNEL_PAIR
     assert q(8192, 8192, 8192)["block_n"] == 256
-    assert q(1023, 1000, 1029)["kernel"] == g.GEMM_KERNEL_GENERIC
+    r = q(1023, 1000, 1029)                     # odd ldb: B staged, then TMA
+    assert r["kernel"] == g.GEMM_KERNEL_TMA and r["staged"] == 2, r
+    r = q(200, 4096, 4100, ldb=4101)            # a 33.6 MB B does not fit the staging buffer
+    assert r["kernel"] == g.GEMM_KERNEL_GENERIC and r["staged"] == 0, r
     s = q(16, 4096, 14336)
     assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["block_m"] == 16
     # 112 tiles of 128 columns already saturate HBM: one share per tile, no split.
