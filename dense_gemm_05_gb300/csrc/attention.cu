@@ -311,27 +311,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kBKV; ++i)
                     if (i >= lim) x[i] = -INFINITY;
             }
-            // Row maximum (four independent chains)
+            // Row maximum (four independent chains of three-input max)
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kBKV; ++i) mx[i & 3] = fmaxf(mx[i & 3], x[i]);
+            for (int i = 0; i < kBKV; i += 2) mx[(i >> 1) & 3] = dg::fmax3(mx[(i >> 1) & 3], x[i], x[i + 1]);
             const float mb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m, mb);
             const float mc = m_new * p.c;
             const float alpha = dg::ex2_approx(m * p.c - mc);   // 0 on the first block
-            // p = 2^(s*c - m*c), summed in fp32 and packed two per 32-bit word
-            // (rounded to the input type) as they are made.
-            float sums[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            // p = 2^(s*c - m*c), two scores per packed fp32 multiply-add and add,
+            // summed in fp32 and packed two per 32-bit word (rounded to the input
+            // type) as they are made.
+            const float2 c2 = make_float2(p.c, p.c);
+            const float2 mc2 = make_float2(-mc, -mc);
+            float2 sums[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
             uint32_t pw[kBKV / 2];
 #pragma unroll
             for (int i = 0; i < kBKV / 2; ++i) {
-                const float a = dg::ex2_approx(fmaf(x[2 * i], p.c, -mc));
-                const float bb = dg::ex2_approx(fmaf(x[2 * i + 1], p.c, -mc));
-                sums[(2 * i) & 3] += a;
-                sums[(2 * i + 1) & 3] += bb;
-                pw[i] = dg::pack_out(a, bb, ptype);
+                const float2 t2 = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), c2, mc2);
+                const float2 e2 = make_float2(dg::ex2_approx(t2.x), dg::ex2_approx(t2.y));
+                sums[i & 1] = __fadd2_rn(sums[i & 1], e2);
+                pw[i] = dg::pack_out(e2.x, e2.y, ptype);
             }
-            l = l * alpha + ((sums[0] + sums[1]) + (sums[2] + sums[3]));
+            l = l * alpha + ((sums[0].x + sums[1].x) + (sums[0].y + sums[1].y));
             if (j > 0) {
                 // P_t(j-1) V_{j-1} must be done: it read the P buffer about to be
                 // rewritten, and O_t must hold its sum before the rescale.

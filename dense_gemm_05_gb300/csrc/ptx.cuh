@@ -303,6 +303,13 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // 2^x by the PTX approximate instruction (ex2.approx.ftz.f32; subnormal
 // results flush to zero).
 __device__ __forceinline__ float ex2_approx(float x) {
