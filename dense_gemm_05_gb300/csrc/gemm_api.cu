@@ -55,6 +55,22 @@ namespace {
 constexpr size_t kWorkspaceBytes = size_t(64) << 20;   // split-K / stream-K partials
 constexpr int64_t kPairMinShareKb = 16;   // a pair stream-K share streams at least this many K blocks
 constexpr size_t kStageBytes = size_t(32) << 20;       // staging copies of misaligned operands
+constexpr int kPairMinSkKb = 32;          // K blocks per tile below which no pair stream-K phase
+
+// Kernel choice: flop/s each SM sustains on one tile of each kind, measured on
+// GB300 with one wave of tiles (bf16, K = 8192): pair tiles 256 x 256 (two
+// SMs), one-CTA tiles 128 x 256 and 128 x 128.  A one-CTA 128 x 128 tile loads
+// twice the bytes per flop of a pair tile's half, which is why it is slowest.
+constexpr double kRatePairPerSm = 10.6e12;
+constexpr double kRateTma256PerSm = 9.1e12;
+constexpr double kRateTma128PerSm = 6.6e12;
+
+// Seconds for `tiles` equal tiles of `tile_flops` each on `slots` units that
+// each run one tile at `rate` flop/s: whole waves times one tile's time.
+double est_seconds(int64_t tiles, int64_t slots, double tile_flops, double rate) {
+    const int64_t waves = (tiles + slots - 1) / slots;
+    return static_cast<double>(waves) * tile_flops / rate;
+}
 constexpr int kMaxCounters = 1 << 16;                   // output tiles that may be split
 constexpr int64_t kMaxDim = INT32_MAX - 1024;   // headroom for tile-edge arithmetic in int32
 
@@ -310,18 +326,33 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
     }
     const bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
     int kernel = plan->force_kernel;
+    int auto_bn = 0;
     if (kernel == 0) {
-        // Pair tiles (256 x 256 per two SMs) once there is at least a full wave of them;
-        // they stage half as much B per flop as one-CTA tiles.
-        const int64_t pair_tiles = cdiv(a.M, 2 * dg::kBM) * cdiv(a.N, 256);
-        if (tma && a.M <= 64 && a.op_a == GEMM_OP_N)
+        if (tma && a.M <= 64 && a.op_a == GEMM_OP_N) {
             kernel = GEMM_KERNEL_SKINNY;
-        else if (tma && plan->pair_clusters[1] > 0 && pair_tiles >= plan->pair_clusters[1])
-            kernel = GEMM_KERNEL_PAIR;
-        else if (tma)
-            kernel = GEMM_KERNEL_TMA;
-        else
+        } else if (tma) {
+            // The cheapest of pair tiles 256 x 256, one-CTA tiles 128 x 256 and
+            // 128 x 128 under est_seconds (waves x time of one tile).
+            const double k = static_cast<double>(a.K);
+            const int64_t pair_slots = plan->pair_clusters[1];
+            const double t_pair =
+                pair_slots > 0 ? est_seconds(cdiv(a.M, 256) * cdiv(a.N, 256), pair_slots,
+                                             2.0 * 256 * 256 * k, 2.0 * kRatePairPerSm)
+                               : 1e30;
+            const double t_tma256 = est_seconds(cdiv(a.M, 128) * cdiv(a.N, 256), plan->num_sms,
+                                                2.0 * 128 * 256 * k, kRateTma256PerSm);
+            const double t_tma128 = est_seconds(cdiv(a.M, 128) * cdiv(a.N, 128), plan->num_sms,
+                                                2.0 * 128 * 128 * k, kRateTma128PerSm);
+            if (t_pair <= t_tma256 && t_pair <= t_tma128) {
+                kernel = GEMM_KERNEL_PAIR;
+                auto_bn = 256;
+            } else {
+                kernel = GEMM_KERNEL_TMA;
+                auto_bn = t_tma256 < t_tma128 ? 256 : 128;
+            }
+        } else {
             kernel = GEMM_KERNEL_GENERIC;
+        }
     }
     if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY ||
          kernel == GEMM_KERNEL_PAIR) && !tma)
@@ -346,7 +377,8 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         const int64_t tm = cdiv(a.M, 2 * dg::kBM);
         const int64_t t256 = tm * cdiv(a.N, 256);
         c->bn = plan->force_bn ? plan->force_bn
-                               : ((t256 >= int64_t(plan->pair_clusters[1])) ? 256 : 128);
+                               : (auto_bn ? auto_bn
+                                          : ((t256 >= int64_t(plan->pair_clusters[1])) ? 256 : 128));
         c->stages = dg::pair_stages(c->bn);
         c->tiles_m = static_cast<int>(tm);
         c->tiles_n = static_cast<int>(cdiv(a.N, c->bn));
@@ -354,6 +386,28 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (units > INT32_MAX) return GEMM_ERR_UNSUPPORTED;
         c->units = static_cast<int>(units);
         const int clusters = plan->pair_clusters[c->bn == 256 ? 1 : 0];
+        c->sk_tiles = 0;
+        c->shares = 0;
+        // Whole-problem stream-K: every tile's K loop is split over all the
+        // clusters (split_k = 2 forces it), so that a problem with fewer pair
+        // tiles than clusters still occupies every SM.
+        if (plan->force_split == 2) {
+            const int64_t T = units * c->num_kb;
+            const int64_t need = int64_t(clusters) * 2 * 2 * c->bn * 128 * 4;
+            if (T / clusters >= kPairMinShareKb && need <= static_cast<int64_t>(plan->ws_bytes) &&
+                units * 2 <= plan->counters_len) {
+                c->grid = 2 * clusters;
+                c->sk_tiles = c->units;
+                c->shares = clusters;
+                int most = 1;
+                for (int64_t t = 0; t < units; ++t)
+                    most = std::max<int>(most, static_cast<int>(
+                                                   dg::share_of((t + 1) * c->num_kb - 1, T, clusters) -
+                                                   dg::share_of(t * c->num_kb, T, clusters) + 1));
+                c->split = most;
+                return GEMM_OK;
+            }
+        }
         const int ncl = c->units < clusters ? c->units : clusters;
         c->grid = 2 * ncl;
         // Stream-K phase: when the last wave of tiles leaves at least half of the
@@ -364,11 +418,11 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         // whole-tile work to hide behind (both measured).  If the shares would be
         // shorter than kPairMinShareKb K blocks, one full wave joins the split
         // tiles.  Also skipped when the partial tiles would not fit the workspace,
-        // or when forced off (split_k = 1).
-        c->sk_tiles = 0;
-        c->shares = 0;
+        // with fewer than kPairMinSkKb K blocks per tile (the fix-ups then cost
+        // more than the idle time they save; measured at K = 1024), or when
+        // forced off (split_k = 1).
         if (plan->force_split != 1 && units % ncl != 0 && 2 * (units % ncl) <= ncl &&
-            units / ncl >= 2) {
+            units / ncl >= 2 && c->num_kb >= kPairMinSkKb) {
             int64_t sk = units % ncl;
             if (sk * c->num_kb / ncl < kPairMinShareKb) sk += ncl;
             const int64_t share_kb = sk * c->num_kb / ncl;
@@ -392,7 +446,8 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (kernel == GEMM_KERNEL_TMA) {
             const int64_t t256 = tm * cdiv(a.N, 256);
             c->bn = plan->force_bn ? plan->force_bn
-                                   : ((t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128);
+                                   : (auto_bn ? auto_bn
+                                              : ((t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128));
             c->stages = dg::tma_stages(c->bn);
         } else {
             c->bn = 128;

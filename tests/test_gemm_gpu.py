@@ -244,14 +244,15 @@ def test_pair_tile_order_does_not_change_bits(plan, group):
 
 def pair_sk_expected(cfg, M, N, K):
     """Stream-K shares the pair kernel should use, from the grid the plan reports:
-    one per cluster when the last wave of tiles is at most half full and at least
-    two full waves precede it; the split covers that partial wave, plus one full
-    wave when the shares would otherwise be shorter than 16 K blocks."""
+    one per cluster when the last wave of tiles is at most half full, at least
+    two full waves precede it and tiles have at least 32 K blocks; the split
+    covers that partial wave, plus one full wave when the shares would otherwise
+    be shorter than 16 K blocks."""
     ncl = cfg["grid"] // 2
     units = -(-M // 256) * -(-N // cfg["block_n"])
     num_kb = -(-K // 64)
     rem = units % ncl
-    if rem == 0 or 2 * rem > ncl or units // ncl < 2:
+    if rem == 0 or 2 * rem > ncl or units // ncl < 2 or num_kb < 32:
         return 0
     sk = rem if rem * num_kb // ncl >= 16 else rem + ncl
     return ncl if sk * num_kb // ncl >= 16 else 0
@@ -268,11 +269,11 @@ def query_pair(plan, A, B, M, N, K, block_n, split=0):
 
 
 # (M, K, N, dtype, block_n), with 76 clusters: 160 tiles of 256 columns over
-# K = 1024 (8 + 76 split tiles, two shares per split tile); 176 tiles of 128
+# K = 3072 (8 + 76 split tiles, two shares per split tile); 176 tiles of 128
 # columns over K = 4096 (the 24 tiles of the partial wave, each split over 4-5
 # shares); 190 tiles of 256 columns over K = 2048 (38 split tiles, 2-3 shares
 # each).
-SK_EXACT = [(2048, 1024, 5120, "bf16", 256), (2048, 4096, 2816, "f16", 128),
+SK_EXACT = [(2048, 3072, 5120, "bf16", 256), (2048, 4096, 2816, "f16", 128),
             (2560, 2048, 4864, "bf16", 256)]
 
 
@@ -293,9 +294,9 @@ def test_pair_stream_k_integer_exact(plan, M, K, N, dtype, block_n):
 
 @pytest.mark.parametrize("block_n", [128, 256])
 def test_pair_stream_k_ragged(plan, block_n):
-    """Ragged M, N and K in the split tiles: 10 x 17 (or 33) tiles, K = 1000."""
-    M, K, N = 2500, 1000, 4100
-    lda, ldb = 1000, 4104
+    """Ragged M, N and K in the split tiles: 10 x 17 (or 33) tiles, K = 2100."""
+    M, K, N = 2500, 2100, 4100
+    lda, ldb = 2104, 4104
     A, B = workloads.custom(M, K, N, "bf16", seed=31 + block_n, dist="normal", lda=lda, ldb=ldb)
     cfg = query_pair(plan, A, B, M, N, K, block_n)
     assert cfg["shares"] == pair_sk_expected(cfg, M, N, K), cfg
@@ -539,6 +540,16 @@ def test_kernel_selection(plan):
     assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["block_m"] == 16
     # 112 tiles of 128 columns already saturate HBM: one share per tile, no split.
     assert s["shares"] == 112 and s["split_k"] == 1, s
+    # Tile shape by estimated time: pair tiles once their waves are cheaper than
+    # one-CTA tiles' (few K-long tiles), 128 x 128 one-CTA tiles for small ones.
+    for shape, kern, bn in [((2048, 8192, 2048), g.GEMM_KERNEL_PAIR, 256),
+                            ((512, 8192, 8192), g.GEMM_KERNEL_PAIR, 256),
+                            ((1536, 1536, 1536), g.GEMM_KERNEL_TMA, 128),
+                            ((128, 8192, 8192), g.GEMM_KERNEL_TMA, 128),
+                            ((1024, 8192, 1024), g.GEMM_KERNEL_TMA, 128)]:
+        r = q(*shape)
+        assert r["kernel"] == kern and r["block_n"] == bn, (shape, r)
+    assert q(4096, 1024, 4096)["shares"] == 0       # 16 K blocks: no stream-K phase
     t = q(16, 4096, 4864)    # 38 tiles: stream-K spreads them over the SMs
     assert t["shares"] > 38 and t["split_k"] > 1, t
     assert q(64, 512, 512)["kernel"] == g.GEMM_KERNEL_SKINNY

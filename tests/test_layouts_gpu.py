@@ -138,7 +138,7 @@ def test_integer_exact_every_layout_and_output(plan, out, op_a, op_b):
 
 @pytest.mark.parametrize("out", [g.GEMM_OUT_F32, g.GEMM_OUT_F16, g.GEMM_OUT_BF16])
 @pytest.mark.parametrize("op_a,op_b", [(N_, N_), (T_, T_)])
-@pytest.mark.parametrize("M,K,N", [(2048, 1024, 5120), (2560, 2048, 4864)])
+@pytest.mark.parametrize("M,K,N", [(2048, 2048, 5120), (2560, 2048, 4864)])
 def test_pair_stream_k_layouts_and_outputs(plan, out, op_a, op_b, M, K, N):
     """Pair tiles with a stream-K phase (160 tiles of 256 columns, two shares per
     split tile; 190 tiles, 2-3 shares per split tile): the fix-up
