@@ -200,7 +200,8 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  * all tiles are cut into that many equal contiguous runs, one CTA each
  * (0 = automatic); for PAIR, `split_k` = 1 turns off the stream-K phase that
  * otherwise splits the last, partial wave of pair tiles (plus one full wave)
- * by K across all clusters (any other value = automatic) -- and `block_n`
+ * by K across all clusters, `split_k` = 2 splits every tile's K loop over all
+ * clusters (whole-problem stream-K), any other value = automatic -- and `block_n`
  * tile columns for TMA/PAIR (128 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
  * arguments (e.g. SKINNY with M > 64, or TMA with an operand that is neither
