@@ -293,6 +293,19 @@ def test_pair_stream_k_integer_exact(plan, M, K, N, dtype, block_n):
 
 
 @pytest.mark.parametrize("block_n", [128, 256])
+def test_pair_whole_problem_stream_k(plan, block_n):
+    """split_k = 2: every tile's 128 K blocks split over all clusters (76 shares of
+    27 or 54 K blocks: 3-6 shares per tile); integer inputs stay exact."""
+    M, K, N = 1024, 8192, 1024
+    A, B = int_inputs(M, K, N, "bf16", seed=77)
+    cfg = query_pair(plan, A, B, M, N, K, block_n, split=2)
+    assert cfg["shares"] == cfg["grid"] // 2 and cfg["split_k"] >= 3, cfg
+    got = run(plan, A, B, M, N, K, ldc=N + 4, kernel=g.GEMM_KERNEL_PAIR, split=2, block_n=block_n)
+    assert_guards(got, M, N)
+    assert np.array_equal(got[:M, :N], oracle.gemm(A, B))
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
 def test_pair_stream_k_ragged(plan, block_n):
     """Ragged M, N and K in the split tiles: 10 x 17 (or 33) tiles, K = 2100."""
     M, K, N = 2500, 2100, 4100
