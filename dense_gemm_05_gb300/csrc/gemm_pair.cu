@@ -216,7 +216,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         const int et = threadIdx.x - 32;         // 0..127
         const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
         const uint32_t tempty1 = mapa_shared(smem_u32(&tempty[1]), 0);
-        const uint32_t ebuf = smem_u32(sEpi) + (warp - 1) * kEpiBufBytes;
+        const uint32_t ebuf = smem_u32(sEpi) + (warp - 1) * kEpiWarpBytes;
+        uint32_t eseq = 0;                       // chunk counter of this warp's two buffers
         int acc = 0;
         uint32_t acc_phase = 0;
         PairWalker walk(p, cid, ncl);
@@ -267,10 +268,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 };
                 auto store_round = [&](int c0, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
                     if (p.c_type == kOutF32) {
-                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
-                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0 + 32, hi, lo);
+                        epi_store_chunk(p, &mapC, ebuf, eseq, lane, row - lane, col0 + c0, lo, hi);
+                        epi_store_chunk(p, &mapC, ebuf, eseq, lane, row - lane, col0 + c0 + 32, hi,
+                                        lo);
                     } else {
-                        epi_store_chunk(p, &mapC, ebuf, lane, row - lane, col0 + c0, lo, hi);
+                        epi_store_chunk(p, &mapC, ebuf, eseq, lane, row - lane, col0 + c0, lo, hi);
                     }
                 };
                 // Sum one 64-column round of the tile in share order.  fold: this
@@ -374,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                 }
             } else {
-                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+                epilogue_staged<BN>(p, &mapC, ebuf, eseq, taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
                                      mbar_arrive_cluster(tempty_peer0);

@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
     } else if (warp <= 4) {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        uint32_t eseq = 0;                      // chunk counter of this warp's two buffers
         const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -223,7 +224,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                                    static_cast<uint32_t>(acc * BN);
             const uint32_t tempty_bar = smem_u32(&tempty[acc]);
             if (!GENERIC) {
-                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiBufBytes, taddr, lane,
+                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiWarpBytes, eseq,
+                                    taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
                                      mbar_arrive(tempty_bar);

@@ -183,6 +183,11 @@ __device__ __forceinline__ void bulk_commit_group() {
 }
 
 // Wait until every committed bulk store of this thread has finished reading shared memory.
+// Wait until at most one bulk group of this thread still has to read its source.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_wait_group_read0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }

@@ -148,19 +148,26 @@ __device__ __forceinline__ void store_c32(const Params& p, int64_t off, const ui
 // address) the warp writes it back row by row, each row as 128 contiguous
 // bytes across the lanes, masked at M and N -- coalesced, where storing each
 // lane's own row directly would touch 32 rows per instruction.
-constexpr int kEpiBufBytes = 4096;             // per epilogue warp
-constexpr int kEpiSmemBytes = 4 * kEpiBufBytes;
+constexpr int kEpiBufBytes = 4096;             // one chunk
+constexpr int kEpiWarpBytes = 2 * kEpiBufBytes;    // two chunk buffers per epilogue warp
+constexpr int kEpiSmemBytes = 4 * kEpiWarpBytes;
 
 // Columns of one chunk for the output type (128 bytes of C).
 __device__ __forceinline__ int epi_chunk_cols(int c_type) { return c_type == kOutF32 ? 32 : 64; }
 
 // lo (and hi, for 16-bit output) hold the chunk's accumulator values for this
 // lane's row: 32 fp32 bit patterns, or 64 values to be rounded to 16 bits.
+// The warp's two chunk buffers (at warp_buf) alternate by `seq`, which the
+// warp keeps across all its chunks, so a chunk is written while the previous
+// one is still being stored.
 __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorMap* mapC,
-                                                uint32_t buf, int lane, int row0, int col,
-                                                const uint32_t (&lo)[32],
+                                                uint32_t warp_buf, uint32_t& seq, int lane,
+                                                int row0, int col, const uint32_t (&lo)[32],
                                                 const uint32_t (&hi)[32]) {
-    if (p.c_tma && lane == 0) bulk_wait_group_read0();   // the previous chunk has left the buffer
+    const uint32_t buf = warp_buf + (seq & 1u) * static_cast<uint32_t>(kEpiBufBytes);
+    ++seq;
+    // The store that last read this buffer (two chunks ago) must have read it.
+    if (p.c_tma && lane == 0) bulk_wait_group_read1();
     __syncwarp();
     const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
     if (p.c_type == kOutF32) {
@@ -219,8 +226,8 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
 // the final chunks are still being stored.
 template <int BN, typename Release>
 __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorMap* mapC,
-                                             uint32_t buf, uint32_t taddr, int lane, int row0,
-                                             int col0, Release release) {
+                                             uint32_t warp_buf, uint32_t& seq, uint32_t taddr,
+                                             int lane, int row0, int col0, Release release) {
     const int cw = epi_chunk_cols(p.c_type);
     const int nchunks = BN / cw;
 #pragma unroll 1
@@ -236,7 +243,7 @@ __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorM
         }
         tmem_ld_wait(lo);
         if (ch == nchunks - 1) release();
-        epi_store_chunk(p, mapC, buf, lane, row0, col0 + ch * cw, lo, hi);
+        epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * cw, lo, hi);
     }
 }
 
