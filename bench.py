@@ -436,12 +436,13 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
 
 def attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src) -> dict:
     """Attention forward (a ranked next row of the hot-path table): seq 8192, d 64,
-    16 heads, bf16, causal and not.  Tensor-core work, but bounded in practice by
+    16 heads, bf16, causal and not; and d 128 causal.  Tensor-core work, but bounded in practice by
     the exponentials of the softmax (one per score).  Events around every launch,
     median of 20; torch's scaled_dot_product_attention on the same tensors for
     context."""
     out = {}
-    for name in ("attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16"):
+    for name in ("attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16",
+                 "attn_bh16_s8192_d128_bf16_causal"):
         w = workloads.ATTN_WORKLOADS[name]
         Q, K, V = workloads.make_qkv(w)
         q, k, v = Q.to(dev), K.to(dev), V.to(dev)
@@ -460,7 +461,8 @@ def attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src) -> di
         out[name] = {"tflops": tf, "pct_of_peak": 100 * tf / peaks["bf16_tflops"],
                      "median_us": t * 1e6, "flops": w.flops,
                      "flops_counted": "4 * BH * d * (query, key) pairs kept by the mask",
-                     "kernel": "attention_fwd_kernel: 2 query tiles of 128 per CTA, 128-key blocks",
+                     "kernel": (f"attention_fwd_kernel: {2 if w.d == 64 else 1} query tile(s) "
+                                "of 128 per CTA, 128-key blocks"),
                      "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
                      "torch_sdpa_tflops": w.flops / (tms[len(tms) // 2] / 1e3) / 1e12}
         del q, k, v, o

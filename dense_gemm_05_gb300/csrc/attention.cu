@@ -49,25 +49,37 @@ namespace {
 __device__ int g_attn_status;
 
 constexpr int kBQ = 128;                  // queries per tile (TMEM lanes)
-constexpr int kTiles = 2;                 // query tiles per CTA, sharing every K/V block
 constexpr int kBKV = 128;                 // keys per block
-constexpr int kD = 64;                    // head dimension
 constexpr int kStages = 3;                // K/V ring depth
-constexpr int kQBytes = kBQ * kD * 2;     // 16 KiB per tile: 128 rows of 128 B (K-major operand)
-constexpr int kKBytes = kBKV * kD * 2;    // 16 KiB: K-major operand, N = keys
-constexpr int kVBytes = kBKV * kD * 2;    // 16 KiB: two 8 KiB MN-major halves of 64 keys
-constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + 5 * kTiles;
-constexpr int kSmemBytes =
-    1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
-constexpr int kThreads = 32 * (1 + kTiles + 4 * kTiles);   // producer, an MMA warp and a
-                                                           // softmax warpgroup per tile
+constexpr int kAtomBytes = 128 * 128;     // 128 rows x 64 elements of a K-major operand (16 KiB)
+constexpr int kSubBytes = 64 * 128;       // 64 keys x 64 d of the MN-major V operand (8 KiB)
 constexpr uint32_t kTmemCols = 512;       // per tile t at 256 t: S (128 columns of fp32),
 constexpr uint32_t kTmemP = 128;          //   P (64 columns, two 16-bit values each),
-constexpr uint32_t kTmemO = 192;          //   O (64 columns of fp32)
+constexpr uint32_t kTmemO = 192;          //   O (d columns of fp32)
 constexpr uint32_t kTmemTile = 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-static_assert(kSmemBytes <= 232448, "shared memory");
+// Sizes for head dimension D (64 or 128).  Rows of D elements are D/64 K-major
+// atoms of 128 B; with D = 64 two query tiles share each K/V block (TMEM: two
+// tiles of S + P + O = 2 x 256 columns), with D = 128 one (128 + 64 + 128).
+template <int D>
+struct AttnCfg {
+    static constexpr int kD = D;
+    static constexpr int kAtoms = D / 64;
+    static constexpr int kTiles = D == 64 ? 2 : 1;
+    static constexpr int kQBytes = kBQ * D * 2;       // per tile: kAtoms atoms
+    static constexpr int kKBytes = kBKV * D * 2;      // kAtoms atoms, N = keys
+    static constexpr int kVBytes = kBKV * D * 2;      // [64-key half][64-d sub-tile]
+    static constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + 5 * kTiles;
+    static constexpr int kSmemBytes =
+        1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
+    static constexpr int kThreads = 32 * (1 + kTiles + 4 * kTiles);   // producer, MMA warp,
+                                                                      // softmax warpgroups
+    static_assert(D == 64 || D == 128, "head dimension");
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(kTmemO + D <= kTmemTile || kTiles == 1, "TMEM per tile");
+    static_assert((kTiles - 1) * kTmemTile + kTmemO + D <= kTmemCols, "TMEM");
+};
 
 struct AttnParams {
     void* O;
@@ -82,11 +94,18 @@ struct AttnParams {
     uint64_t timeout_ns;
 };
 
-template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool BF16, int D>
+__global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     attention_fwd_kernel(const __grid_constant__ CUtensorMap mapQ,
                          const __grid_constant__ CUtensorMap mapK,
                          const __grid_constant__ CUtensorMap mapV, const AttnParams p) {
+    using Cfg = AttnCfg<D>;
+    constexpr int kD = D;
+    constexpr int kAtoms = Cfg::kAtoms;
+    constexpr int kTiles = Cfg::kTiles;
+    constexpr int kQBytes = Cfg::kQBytes;
+    constexpr int kKBytes = Cfg::kKBytes;
+    constexpr int kVBytes = Cfg::kVBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -162,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qb = dg::smem_u32(q_full);
             dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
             for (int t = 0; t < kTiles; ++t)
-                dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes), &mapQ, qb, 0,
-                                (pair * kTiles + t) * kBQ, h);
+                for (int a = 0; a < kAtoms; ++a)
+                    dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes + a * kAtomBytes), &mapQ, qb,
+                                    64 * a, (pair * kTiles + t) * kBQ, h);
             bool ok = true;
             for (int j = 0; ok && j < nkv_max; ++j) {
                 const int st = j % kStages;
@@ -180,12 +200,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint32_t kb = dg::smem_u32(&k_full[st]);
                 dg::mbar_arrive_expect_tx(kb, kKBytes);
-                dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes), &mapK, kb, 0, j * kBKV, h);
+                for (int a = 0; a < kAtoms; ++a)
+                    dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes + a * kAtomBytes), &mapK, kb,
+                                    64 * a, j * kBKV, h);
                 const uint32_t vb = dg::smem_u32(&v_full[st]);
                 dg::mbar_arrive_expect_tx(vb, kVBytes);
                 const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
-                dg::tma_load_3d(vdst, &mapV, vb, 0, j * kBKV, h);
-                dg::tma_load_3d(vdst + kVBytes / 2, &mapV, vb, 0, j * kBKV + kBKV / 2, h);
+                for (int hh = 0; hh < 2; ++hh)
+                    for (int a = 0; a < kAtoms; ++a)
+                        dg::tma_load_3d(vdst + (hh * kAtoms + a) * kSubBytes, &mapV, vb, 64 * a,
+                                        j * kBKV + hh * (kBKV / 2), h);
             }
         }
         __syncwarp();
@@ -218,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
 #pragma unroll
                 for (int k16 = 0; k16 < kD / 16; ++k16)
-                    dg::tc_mma_f16(s_tmem, dg::operand_desc<false>(q_addr, k16),
-                                   dg::operand_desc<false>(k_addr, k16), idesc_s,
-                                   k16 > 0 ? 1u : 0u);
+                    dg::tc_mma_f16(s_tmem,
+                                   dg::operand_desc<false>(q_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                   dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                   idesc_s, k16 > 0 ? 1u : 0u);
                 dg::tc_commit(dg::smem_u32(&s_full[t]));
                 return true;
             };
@@ -246,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dg::tc_mma_f16_ts(o_tmem, p_tmem + static_cast<uint32_t>(k16 * 8),
                                       dg::operand_desc<true>(v_addr + (k16 >> 2) * (kVBytes / 2),
                                                              k16 & 3),
-                                      idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);
+                                      idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);   // N = d: kAtoms
+                                                                                 // sub-tiles 8 KiB apart
                 dg::tc_commit(dg::smem_u32(&pv_done[t]));
                 dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
             }
@@ -474,15 +500,15 @@ EncodeTiledFn encode_fn() {
 }
 
 // [BH, seq, d] view with row pitch ld and head pitch hs (elements); boxes of
-// 64 d x `rows` rows x 1 head, 128-byte swizzle, zero fill beyond seq.
-bool encode_qkv(CUtensorMap* map, bool bf16, const void* ptr, int64_t BH, int64_t seq, int64_t ld,
-                int64_t hs, uint32_t rows) {
+// 64 d (one 128-byte swizzle row) x `rows` rows x 1 head, zero fill beyond seq.
+bool encode_qkv(CUtensorMap* map, bool bf16, const void* ptr, int64_t BH, int64_t seq, int64_t d,
+                int64_t ld, int64_t hs, uint32_t rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(seq),
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(seq),
                           static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, static_cast<cuuint64_t>(hs) * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(kD), rows, 1u};
+    cuuint32_t box[3] = {64u, rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
               const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -497,7 +523,7 @@ struct DeviceFacts {
 
 std::mutex g_mu;
 DeviceFacts g_dev[64];
-bool g_attr_set[2] = {false, false};
+bool g_attr_set[4] = {false, false, false, false};   // [bf16 + 2 * (d == 128)]
 
 bool device_ok(bool* sm103) {
     int dev = 0;
@@ -544,7 +570,7 @@ gemm_status_t check(const void* Q, const void* K, const void* V, const void* O, 
          reinterpret_cast<uintptr_t>(V)) % 16u != 0u ||
         reinterpret_cast<uintptr_t>(O) % static_cast<uintptr_t>(osz) != 0u)
         return GEMM_ERR_INVALID_ARG;
-    if (d != kD) return GEMM_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return GEMM_ERR_UNSUPPORTED;
     if (ld % 8 != 0 || hs % 8 != 0 || BH > 65535 || seq > INT32_MAX ||
         ld > (int64_t(1) << 36) || hs > (int64_t(1) << 36) || ldo > (int64_t(1) << 36) ||
         hso > (int64_t(1) << 36))
@@ -585,7 +611,8 @@ gemm_status_t attention_fwd_query(const void* Q, const void* K, const void* V, c
     out->block_kv = kBKV;
     out->head_dim = static_cast<int32_t>(d);
     out->stages = kStages;
-    out->grid_x = static_cast<int32_t>(((seq + kBQ - 1) / kBQ + kTiles - 1) / kTiles);
+    const int tiles_per_cta = d == 64 ? AttnCfg<64>::kTiles : AttnCfg<128>::kTiles;
+    out->grid_x = static_cast<int32_t>(((seq + kBQ - 1) / kBQ + tiles_per_cta - 1) / tiles_per_cta);
     out->grid_y = static_cast<int32_t>(BH);
     out->causal = causal ? 1 : 0;
     return GEMM_OK;
@@ -603,20 +630,27 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
     if (!sm103) return GEMM_ERR_UNSUPPORTED;
     const bool bf16 = dtype == GEMM_BF16;
     CUtensorMap mq, mk, mv;
-    if (!encode_qkv(&mq, bf16, Q, BH, seq, ld, head_stride, kBQ) ||
-        !encode_qkv(&mk, bf16, K, BH, seq, ld, head_stride, kBKV) ||
-        !encode_qkv(&mv, bf16, V, BH, seq, ld, head_stride, kBKV / 2))
+    if (!encode_qkv(&mq, bf16, Q, BH, seq, d, ld, head_stride, kBQ) ||
+        !encode_qkv(&mk, bf16, K, BH, seq, d, ld, head_stride, kBKV) ||
+        !encode_qkv(&mv, bf16, V, BH, seq, d, ld, head_stride, kBKV / 2))
         return GEMM_ERR_CUDA;
-    auto kernel = bf16 ? attention_fwd_kernel<true> : attention_fwd_kernel<false>;
+    using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, AttnParams);
+    const bool d64 = d == 64;
+    const Kernel kernel = d64 ? (bf16 ? attention_fwd_kernel<true, 64> : attention_fwd_kernel<false, 64>)
+                              : (bf16 ? attention_fwd_kernel<true, 128> : attention_fwd_kernel<false, 128>);
+    const int smem_bytes = d64 ? AttnCfg<64>::kSmemBytes : AttnCfg<128>::kSmemBytes;
+    const int threads = d64 ? AttnCfg<64>::kThreads : AttnCfg<128>::kThreads;
+    const int tiles_per_cta = d64 ? AttnCfg<64>::kTiles : AttnCfg<128>::kTiles;
     {
         std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_attr_set[bf16 ? 1 : 0]) {
+        const int which = (bf16 ? 1 : 0) + (d64 ? 0 : 2);
+        if (!g_attr_set[which]) {
             if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemBytes) != cudaSuccess) {
+                                     smem_bytes) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return GEMM_ERR_CUDA;
             }
-            g_attr_set[bf16 ? 1 : 0] = true;
+            g_attr_set[which] = true;
         }
     }
     AttnParams p{};
@@ -632,12 +666,12 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
     p.seq = static_cast<int32_t>(seq);
     p.causal = causal ? 1 : 0;
     p.ntiles = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
-    p.npairs = (p.ntiles + kTiles - 1) / kTiles;
+    p.npairs = (p.ntiles + tiles_per_cta - 1) / tiles_per_cta;
     p.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.timeout_ns = kTimeoutNs;
     const dim3 grid(static_cast<unsigned>(p.npairs), static_cast<unsigned>(BH));
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    kernel<<<grid, kThreads, kSmemBytes, s>>>(mq, mk, mv, p);
+    kernel<<<grid, threads, smem_bytes, s>>>(mq, mk, mv, p);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
     if (debug_sync()) {
         if (cudaStreamSynchronize(s) != cudaSuccess) {

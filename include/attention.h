@@ -25,7 +25,7 @@
  * out_type.  Keys i >= seq do not exist (they take no part; the section's
  * kernel leaves that boundary handling out).
  *
- * Limits: d == 64; ld and head_stride multiples of 8 elements and Q, K, V
+ * Limits: d == 64 or 128; ld and head_stride multiples of 8 elements and Q, K, V
  * 16-byte aligned (tensor-memory-access boxes); BH <= 65535; seq < 2^31.
  *
  * Ownership: the caller owns all buffers and the stream; nothing is allocated
@@ -34,7 +34,7 @@
  *
  * Errors: GEMM_ERR_INVALID_ARG for null pointers (when BH*seq > 0), negative
  * sizes, ld < d, ldo < d, misaligned pointers, or O overlapping Q, K or V;
- * GEMM_ERR_UNSUPPORTED for d != 64, strides that are not multiples of 8,
+ * GEMM_ERR_UNSUPPORTED for d other than 64 or 128, strides that are not multiples of 8,
  * BH > 65535, an unknown dtype/out_type, or a device that is not sm_103;
  * GEMM_ERR_CUDA when the launch fails.  BH == 0 or seq == 0 is a no-op.
  */
@@ -48,11 +48,11 @@ extern "C" {
 #endif
 
 typedef struct {
-    int32_t block_q;      /* queries per block (TMEM lanes); a CTA holds two blocks */
+    int32_t block_q;      /* queries per block (TMEM lanes) */
     int32_t block_kv;     /* keys per step of the online softmax */
     int32_t head_dim;
     int32_t stages;       /* K/V shared-memory ring depth */
-    int32_t grid_x;       /* CTAs per head (each holds two query blocks) */
+    int32_t grid_x;       /* CTAs per head (each holds two query blocks for d = 64, one for 128) */
     int32_t grid_y;       /* heads */
     int32_t causal;
 } attention_config_t;

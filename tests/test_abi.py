@@ -111,7 +111,7 @@ def test_attention_argument_checks_need_no_gpu():
     assert af(0, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, BF16, F32, 0) == g.GEMM_ERR_INVALID_ARG
     assert af(a, b, c, o, 2, 8, 64, 32, 512, 64, 512, 0, BF16, F32, 0) == g.GEMM_ERR_INVALID_ARG  # ld < d
     assert af(a + 8, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, F16, F32, 0) == g.GEMM_ERR_INVALID_ARG  # align
-    assert af(a, b, c, o, 2, 8, 128, 128, 1024, 128, 1024, 0, F16, F32, 0) == g.GEMM_ERR_UNSUPPORTED  # d
+    assert af(a, b, c, o, 2, 8, 96, 96, 768, 96, 768, 0, F16, F32, 0) == g.GEMM_ERR_UNSUPPORTED    # d
     assert af(a, b, c, o, 2, 8, 64, 68, 544, 64, 512, 0, F16, F32, 0) == g.GEMM_ERR_UNSUPPORTED   # ld % 8
     assert af(a, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, 7, F32, 0) == g.GEMM_ERR_UNSUPPORTED     # dtype
     assert af(a, b, c, o, 2, 8, 64, 64, 512, 64, 512, 0, F16, 9, 0) == g.GEMM_ERR_UNSUPPORTED     # out
@@ -119,5 +119,7 @@ def test_attention_argument_checks_need_no_gpu():
     with pytest.raises(g.GemmError):
         g.attention_fwd_query(a, b, c, o, -1, 8, 64, 64, 512, 64, 512, 0, F16, F32)
     cfg = g.attention_fwd_query(a, b, c, o, 3, 1000, 64, 64, 64000, 64, 64000, 1, BF16, F32)
-    # 8 query blocks of 128 per head, two per CTA
+    # 8 query blocks of 128 per head, two per CTA (d = 64) or one (d = 128)
     assert cfg["grid_x"] == 4 and cfg["grid_y"] == 3 and cfg["block_q"] == 128 and cfg["causal"] == 1
+    cfg = g.attention_fwd_query(a, b, c, o, 3, 1000, 128, 128, 128000, 128, 128000, 0, BF16, F32)
+    assert cfg["grid_x"] == 8 and cfg["head_dim"] == 128

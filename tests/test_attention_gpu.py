@@ -63,7 +63,7 @@ def assert_attn_close(got, Q, K, V, causal, head, rows, out_dtype, what):
 
 def run(Q, K, V, causal, out_dtype=torch.float32, layout="heads"):
     """Q, K, V: CPU [BH, seq, d].  layout 'heads' = contiguous [BH, seq, d];
-    'interleaved' = stored [seq, BH, d]; 'padded' = rows padded to 72 elements."""
+    'interleaved' = stored [seq, BH, d]; 'padded' = rows padded to d + 8 elements."""
     dev = torch.device("cuda:0")
     BH, seq, d = Q.shape
     if layout == "heads":
@@ -72,7 +72,7 @@ def run(Q, K, V, causal, out_dtype=torch.float32, layout="heads"):
         q, k, v = (t.transpose(0, 1).contiguous().to(dev).transpose(0, 1) for t in (Q, K, V))
     else:
         def pad(t):
-            buf = torch.full((BH, seq, 72), float("nan"), dtype=t.dtype)
+            buf = torch.full((BH, seq, d + 8), float("nan"), dtype=t.dtype)
             buf[:, :, :d] = t
             return buf.to(dev)[:, :, :d]
         q, k, v = pad(Q), pad(K), pad(V)
@@ -96,20 +96,22 @@ SEQS = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 300, 513]
 
 @pytest.mark.parametrize("seq", SEQS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_lengths(seq, causal):
+@pytest.mark.parametrize("d", [64, 128])
+def test_lengths(seq, causal, d):
     dt = "bf16" if seq % 2 else "f16"
-    Q, K, V = workloads.custom_qkv(3, seq, 64, dt, seed=seq * 3 + causal)
+    Q, K, V = workloads.custom_qkv(3, seq, d, dt, seed=seq * 3 + causal + d)
     got = run(Q, K, V, causal)
     assert np.all(np.isfinite(got))
     for h in range(3):
         assert_attn_close(got[h], Q, K, V, causal, h, np.arange(seq), torch.float32,
-                          f"seq {seq} causal {causal} head {h}")
+                          f"d {d} seq {seq} causal {causal} head {h}")
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("layout", ["heads", "interleaved", "padded"])
-def test_layouts_and_output_types(out_dtype, layout):
-    Q, K, V = workloads.custom_qkv(4, 333, 64, "bf16", seed=7)
+@pytest.mark.parametrize("d", [64, 128])
+def test_layouts_and_output_types(out_dtype, layout, d):
+    Q, K, V = workloads.custom_qkv(4, 333, d, "bf16", seed=7 + d)
     got = run(Q, K, V, True, out_dtype=out_dtype, layout=layout)
     for h in range(4):
         assert_attn_close(got[h], Q, K, V, True, h, np.arange(333), out_dtype, f"{layout} {out_dtype} head {h}")
@@ -143,7 +145,8 @@ def test_repeatable_bits():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("name", ["attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16"])
+@pytest.mark.parametrize("name", ["attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16",
+                                  "attn_bh16_s8192_d128_bf16_causal"])
 def test_full_size_sampled(name):
     """The measured workloads, launched as bench.py launches them: sampled rows of
     three heads (first and last rows of the sequence included) against the oracle;

@@ -200,6 +200,8 @@ ATTN_WORKLOADS: dict[str, AttnWorkload] = {
                      "the section's sequence length 8192 and head dimension 64, causal, 16 heads"),
         AttnWorkload("attn_bh16_s8192_d64_bf16", 16, 8192, 64, "bf16", False, 33,
                      "the same without the mask"),
+        AttnWorkload("attn_bh16_s8192_d128_bf16_causal", 16, 8192, 128, "bf16", True, 34,
+                     "head dimension 128, causal, 16 heads"),
     ]
 }
 
