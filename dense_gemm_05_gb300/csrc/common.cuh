@@ -170,6 +170,16 @@ cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
                         const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
                         uint32_t idesc, int grid, cudaStream_t stream);
 
+// Small M on 2-CTA clusters: a cluster per BN-column strip of C splits the K loop in
+// halves and exchanges half of its partial through distributed shared memory.
+// ms in {16, 32, 64} (M padded), bn in {128, 192, 256}; grid = 2 x strips; num_kb >= 2.
+int skpair_stages(int ms, int bn);
+cudaError_t skpair_prepare();
+int skpair_max_clusters();       // co-resident 2-CTA clusters (0 = unknown)
+cudaError_t launch_skpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
+                          const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
+                          cudaStream_t stream);
+
 // Copy a rows x cols 16-bit matrix (pitch lds) into dst with pitch ldd (a multiple
 // of 8 elements, dst 16-byte aligned), zero-filling columns [cols, ldd).
 cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,

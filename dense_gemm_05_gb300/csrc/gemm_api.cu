@@ -46,6 +46,7 @@ struct gemm_plan_s {
     int force_split = 0;
     int force_bn = 0;
     int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
+    int skpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
     bool debug_sync = false;
     uint64_t timeout_ns = 2000000000ull;
 };
@@ -181,7 +182,7 @@ struct Args {
 struct Choice {
     int kernel = GEMM_KERNEL_NONE;
     int bn = 0;          // TMA/GENERIC: tile columns
-    int ms = 0;          // SKINNY: padded M (MMA N)
+    int ms = 0;          // SKINNY, SKINNY_PAIR: padded M
     int split = 1;       // SKINNY: most stream-K shares that touch one tile
     int shares = 0;      // SKINNY: stream-K shares
     int max_slots = 0;   // SKINNY: workspace slots per tile
@@ -314,6 +315,33 @@ bool plan_staging(const gemm_plan_s* plan, const Args& a, Staging* st, Args* out
     return true;
 }
 
+// Small M on 2-CTA clusters, strip width when not forced: 128 columns while
+// the strips of 128 fit on the SMs in one wave, else 256 (wider strips stream
+// B faster per SM: 512-byte row pieces), 192 with M > 32 (whose 256-column
+// stages leave room for only four in flight), if those fit in one wave.
+// Measured at M = 16, K = 4096: N = 8192 128 columns 13.6 us, 256 14.3;
+// N = 14336 256 columns 21.1 us, 192 21.9; at M = 64 192 columns 23.1 us, 256 24.4.
+int skpair_auto_width(const gemm_plan_s* plan, const Args& a) {
+    if (2 * cdiv(a.N, 128) <= plan->num_sms) return 128;
+    if (a.M > 32 && cdiv(a.N, 192) <= plan->skpair_clusters) return 192;
+    return 256;
+}
+
+// The cluster kernel is chosen (returning its strip width) when its first wave
+// keeps at least 3/5 of the SMs streaming B and there are at least 8 K blocks
+// per half; otherwise (0) the stream-K kernel, which balances any shape but
+// pays a global fix-up (measured at M = 16, K = 4096: N = 4096, 64 CTAs of the
+// cluster kernel 12.3 us against 11.3 for stream-K; N = 8192, 128 CTAs 13.6
+// against 16.1; N = 28672, two waves, 42.6 against 49.1).
+int skpair_auto_bn(const gemm_plan_s* plan, const Args& a) {
+    if (plan->skpair_clusters <= 0 || cdiv(a.K, dg::kBK) < 16) return 0;
+    const int bn = skpair_auto_width(plan, a);
+    const int64_t strips = cdiv(a.N, bn);
+    const int64_t first_wave = std::min<int64_t>(strips, plan->skpair_clusters);
+    if (5 * 2 * first_wave < 3 * int64_t(plan->num_sms)) return 0;
+    return bn;
+}
+
 gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
     *c = Choice{};
     if (a.M == 0 || a.N == 0) {
@@ -329,7 +357,11 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
     int auto_bn = 0;
     if (kernel == 0) {
         if (tma && a.M <= 64 && a.op_a == GEMM_OP_N) {
-            kernel = GEMM_KERNEL_SKINNY;
+            // A cluster per strip of columns (K split in two) when the strips
+            // fill nearly every SM in one wave; otherwise stream-K over tiles.
+            const int bn = skpair_auto_bn(plan, a);
+            kernel = bn ? GEMM_KERNEL_SKINNY_PAIR : GEMM_KERNEL_SKINNY;
+            auto_bn = bn;
         } else if (tma) {
             // The cheapest of pair tiles 256 x 256, one-CTA tiles 128 x 256 and
             // 128 x 128 under est_seconds (waves x time of one tile).
@@ -355,13 +387,19 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         }
     }
     if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY ||
-         kernel == GEMM_KERNEL_PAIR) && !tma)
+         kernel == GEMM_KERNEL_PAIR || kernel == GEMM_KERNEL_SKINNY_PAIR) && !tma)
         return GEMM_ERR_UNSUPPORTED;
-    if (kernel == GEMM_KERNEL_SKINNY && (a.M > 64 || a.op_a != GEMM_OP_N))
+    if ((kernel == GEMM_KERNEL_SKINNY || kernel == GEMM_KERNEL_SKINNY_PAIR) &&
+        (a.M > 64 || a.op_a != GEMM_OP_N))
         return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_SKINNY_PAIR && (cdiv(a.K, dg::kBK) < 2 || plan->skpair_clusters <= 0))
+        return GEMM_ERR_UNSUPPORTED;
+    // 192-column tiles exist only in the small-M cluster kernel.
+    if (plan->force_bn == 192 && kernel != GEMM_KERNEL_SKINNY_PAIR) return GEMM_ERR_UNSUPPORTED;
     if (kernel == GEMM_KERNEL_PAIR && plan->pair_clusters[0] <= 0) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_SKINNY &&
-        kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR)
+        kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR &&
+        kernel != GEMM_KERNEL_SKINNY_PAIR)
         return GEMM_ERR_UNSUPPORTED;
     c->kernel = kernel;
     c->num_kb = static_cast<int>(cdiv(a.K, dg::kBK));
@@ -373,6 +411,18 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (!choose_shares(plan, c, plan->force_split)) return GEMM_ERR_UNSUPPORTED;
         c->units = c->shares;
         c->stages = dg::skinny_stages(c->ms);
+    } else if (kernel == GEMM_KERNEL_SKINNY_PAIR) {
+        c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : 64);
+        c->bn = plan->force_bn ? plan->force_bn : (auto_bn ? auto_bn : skpair_auto_width(plan, a));
+        c->tiles_m = 1;
+        const int64_t strips = cdiv(a.N, c->bn);
+        if (strips > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+        c->tiles_n = static_cast<int>(strips);
+        c->units = c->tiles_n;
+        c->split = 2;
+        c->grid = 2 * c->tiles_n;
+        c->stages = dg::skpair_stages(c->ms, c->bn);
+        return GEMM_OK;
     } else if (kernel == GEMM_KERNEL_PAIR) {
         const int64_t tm = cdiv(a.M, 2 * dg::kBM);
         const int64_t t256 = tm * cdiv(a.N, 256);
@@ -546,7 +596,8 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
     if (encode_fn() == nullptr) return GEMM_ERR_CUDA;
     if (dg::tma_prepare() != cudaSuccess || dg::generic_prepare() != cudaSuccess ||
-        dg::skinny_prepare() != cudaSuccess || dg::pair_prepare() != cudaSuccess) {
+        dg::skinny_prepare() != cudaSuccess || dg::pair_prepare() != cudaSuccess ||
+        dg::skpair_prepare() != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -558,6 +609,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     // persistent grids by what the device can co-schedule.
     p->pair_clusters[0] = dg::pair_max_clusters(128);
     p->pair_clusters[1] = dg::pair_max_clusters(256);
+    p->skpair_clusters = dg::skpair_max_clusters();
     p->debug_sync = env_flag("GEMM_DEBUG_SYNC");
     if (const char* t = std::getenv("GEMM_WAIT_TIMEOUT_MS")) {
         const long long ms = std::atoll(t);
@@ -611,9 +663,11 @@ gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group) {
 gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
                               int32_t block_n) {
     if (plan == nullptr || split_k < 0) return GEMM_ERR_INVALID_ARG;
-    if (block_n != 0 && block_n != 128 && block_n != 256) return GEMM_ERR_INVALID_ARG;
+    if (block_n != 0 && block_n != 128 && block_n != 192 && block_n != 256)
+        return GEMM_ERR_INVALID_ARG;
     if (kernel != 0 && kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_GENERIC &&
-        kernel != GEMM_KERNEL_SKINNY && kernel != GEMM_KERNEL_PAIR)
+        kernel != GEMM_KERNEL_SKINNY && kernel != GEMM_KERNEL_PAIR &&
+        kernel != GEMM_KERNEL_SKINNY_PAIR)
         return GEMM_ERR_INVALID_ARG;
     plan->force_kernel = kernel;
     plan->force_split = split_k;
@@ -646,8 +700,9 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     if (st != GEMM_OK) return st;
     gemm_config_t cfg{};
     cfg.kernel = c.kernel;
-    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY) ? c.ms
-                  : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM : dg::kBM);
+    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY || c.kernel == GEMM_KERNEL_SKINNY_PAIR)
+                      ? c.ms
+                      : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM : dg::kBM);
     cfg.block_n = (c.kernel == GEMM_KERNEL_SKINNY) ? 128 : c.bn;
     cfg.block_k = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : dg::kBK;
     cfg.stages = c.stages;
@@ -655,7 +710,8 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     cfg.grid = c.grid;
     cfg.cluster = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL)
                       ? 0
-                      : (c.kernel == GEMM_KERNEL_PAIR ? 2 : 1);
+                      : ((c.kernel == GEMM_KERNEL_PAIR || c.kernel == GEMM_KERNEL_SKINNY_PAIR) ? 2
+                                                                                          : 1);
     cfg.group = (c.kernel == GEMM_KERNEL_TMA || c.kernel == GEMM_KERNEL_GENERIC ||
                  c.kernel == GEMM_KERNEL_PAIR)
                     ? plan->group
@@ -776,6 +832,16 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             err = dg::launch_pair(c.bn, a_mn, b_mn, ma, mb, mc, p,
                                   dg::idesc_f16(bf16, a_mn, b_mn, 2 * dg::kBM, c.bn), c.grid,
                                   stream);
+        } else if (c.kernel == GEMM_KERNEL_SKINNY_PAIR) {
+            // A tile (M <= 64 rows, K-major) as the MMA's 128-row A operand, the
+            // B tile (bn columns) as its B operand.
+            CUtensorMap ma, mb;
+            if (!map_a(&ma, static_cast<uint32_t>(c.ms)) ||
+                !map_b(&mb, static_cast<uint32_t>(c.bn)))
+                return GEMM_ERR_CUDA;
+            err = dg::launch_skpair(c.ms, c.bn, b_mn, ma, mb, p,
+                                    dg::idesc_f16(bf16, false, b_mn, dg::kBM, c.bn), c.grid,
+                                    stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {
             err = dg::launch_generic(a_mn, b_mn, p,
                                      dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, 128), c.grid,

@@ -127,12 +127,17 @@ def test_workload_skinny_full_and_deterministic(plan):
     A, B = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
     cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
-    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY, cfg
+    # 56 strips of 256 columns on 56 two-CTA clusters.
+    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR, cfg
+    assert cfg["block_n"] == 256 and cfg["grid"] == 112 and cfg["cluster"] == 2, cfg
     got1 = run(plan, A, B, w.M, w.N, w.K)
     got2 = run(plan, A, B, w.M, w.N, w.K)
     assert_guards(got1, w.M, w.N)
     assert np.array_equal(got1, got2), "split-K result changed between runs"
     assert_close(got1[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+    # the stream-K kernel on the same problem agrees within the tolerance too
+    got3 = run(plan, A, B, w.M, w.N, w.K, kernel=g.GEMM_KERNEL_SKINNY, expect=g.GEMM_KERNEL_SKINNY)
+    assert_close(got3[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " stream-K")
 
 
 @pytest.mark.parametrize("M,K,N,dtype,shares", [
@@ -145,11 +150,63 @@ def test_workload_skinny_full_and_deterministic(plan):
 ])
 def test_skinny_stream_k_shapes(plan, M, K, N, dtype, shares):
     A, B = workloads.custom(M, K, N, dtype, seed=M + K + N, dist="normal")
-    got1 = run(plan, A, B, M, N, K, split=shares, expect=g.GEMM_KERNEL_SKINNY)
-    got2 = run(plan, A, B, M, N, K, split=shares, expect=g.GEMM_KERNEL_SKINNY)
+    got1 = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_SKINNY, split=shares,
+               expect=g.GEMM_KERNEL_SKINNY)
+    got2 = run(plan, A, B, M, N, K, kernel=g.GEMM_KERNEL_SKINNY, split=shares,
+               expect=g.GEMM_KERNEL_SKINNY)
     assert_guards(got1, M, N)
     assert np.array_equal(got1, got2), "stream-K result changed between runs"
     assert_close(got1[:M, :N], A, B, M, N, K, f"skinny {M}x{N}x{K} shares={shares}")
+
+
+@pytest.mark.parametrize("M,K,N,dtype,block_n", [
+    (16, 4096, 14336, "bf16", 0),    # the M=16 workload: automatic 192-column strips
+    (1, 256, 1000, "f16", 128),      # M = 1, 4 K blocks, ragged last strip
+    (33, 1000, 700, "bf16", 192),    # M padded to 64 (two TMEM lane quadrants), ragged K and N
+    (64, 130, 513, "f16", 256),      # 3 K blocks: halves of 1 and 2, ragged everywhere
+    (17, 2048, 9728, "bf16", 128),   # M padded to 32, 76 strips
+    (16, 128, 256, "bf16", 256),     # 2 K blocks: one per CTA, a single strip
+    (8, 512, 40000, "bf16", 128),    # 313 strips: more clusters than fit at once
+])
+def test_skinny_pair_shapes(plan, M, K, N, dtype, block_n):
+    """Small M on 2-CTA clusters (K halves exchanged through distributed shared memory)."""
+    A, B = workloads.custom(M, K, N, dtype, seed=M + K + N + 1, dist="normal")
+    kernel = 0 if block_n == 0 else g.GEMM_KERNEL_SKINNY_PAIR
+    got1 = run(plan, A, B, M, N, K, kernel=kernel, block_n=block_n,
+               expect=g.GEMM_KERNEL_SKINNY_PAIR)
+    got2 = run(plan, A, B, M, N, K, kernel=kernel, block_n=block_n)
+    assert_guards(got1, M, N)
+    assert np.array_equal(got1, got2), "result changed between runs"
+    assert_close(got1[:M, :N], A, B, M, N, K, f"skinny pair {M}x{N}x{K} bn={block_n}")
+
+
+def test_skinny_pair_query(plan):
+    dev = torch.device("cuda:0")
+    a = torch.empty(64, 4096, dtype=torch.bfloat16, device=dev)
+    b = torch.empty(4096, 40000, dtype=torch.bfloat16, device=dev)
+    c = torch.empty(64, 40000, device=dev)
+    plan.force(g.GEMM_KERNEL_SKINNY_PAIR, 0, 192)
+    try:
+        cfg = plan.query(a, b, c, 20, 1000, 4096)
+        assert cfg["block_m"] == 32 and cfg["block_n"] == 192 and cfg["split_k"] == 2, cfg
+        assert cfg["tiles"] == 6 and cfg["grid"] == 12 and cfg["cluster"] == 2, cfg
+        plan.force(g.GEMM_KERNEL_SKINNY_PAIR, 0, 0)
+        assert plan.query(a, b, c, 20, 1000, 4096)["block_n"] == 128
+        assert plan.query(a, b, c, 20, 14336, 4096)["block_n"] == 256
+        assert plan.query(a, b, c, 40, 14336, 4096)["block_n"] == 192
+        with pytest.raises(RuntimeError):
+            plan.query(a, b, c, 65, 1000, 4096)          # M > 64
+        with pytest.raises(RuntimeError):
+            plan.query(a, b, c, 16, 1000, 64)            # one K block
+        plan.force(g.GEMM_KERNEL_TMA, 0, 192)            # 192 columns: this kernel only
+        with pytest.raises(RuntimeError):
+            plan.query(a, b, c, 16, 1000, 4096)
+    finally:
+        plan.force(0, 0, 0)
+    # automatic: few strips leave SMs idle, so the stream-K kernel is chosen
+    assert plan.query(a, b, c, 16, 4096, 4096)["kernel"] == g.GEMM_KERNEL_SKINNY
+    assert plan.query(a, b, c, 16, 8192, 4096)["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR
+    assert plan.query(a, b, c, 16, 14336, 512)["kernel"] == g.GEMM_KERNEL_SKINNY   # 8 K blocks
 
 
 def _sample_entries(M, N, bm, bn, n_random, seed):
@@ -359,15 +416,17 @@ def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
     (g.GEMM_KERNEL_SKINNY, 12, (16, 4096, 1024), "bf16"),
     (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
     (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
+    (g.GEMM_KERNEL_SKINNY_PAIR, 192, (16, 4096, 1024), "bf16"),
+    (g.GEMM_KERNEL_SKINNY_PAIR, 128, (40, 1000, 520), "f16"),
     (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1104), "bf16"),
     (g.GEMM_KERNEL_PAIR, 256, (600, 1024, 1104), "f16"),
     (g.GEMM_KERNEL_PAIR, 256, (1024, 4096, 1024), "bf16"),
 ])
 def test_small_integer_inputs_are_bit_exact(plan, kernel, split, shape, dtype):
-    """For the pair kernel the second parameter is the pair tile width (block_n)."""
+    """For the pair kernels the second parameter is the tile width (block_n)."""
     M, K, N = shape
     A, B = int_inputs(M, K, N, dtype, seed=M + K + N)
-    if kernel == g.GEMM_KERNEL_PAIR:
+    if kernel in (g.GEMM_KERNEL_PAIR, g.GEMM_KERNEL_SKINNY_PAIR):
         got = run(plan, A, B, M, N, K, kernel=kernel, block_n=split, expect=kernel)
     else:
         got = run(plan, A, B, M, N, K, kernel=kernel, split=split, expect=kernel)
@@ -390,6 +449,9 @@ def test_mn_major_layout_pin(plan):
     A16 = torch.eye(16, K, dtype=torch.bfloat16)
     got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SKINNY, split=2)
     assert np.array_equal(got[:16, :N], B[:16].double().numpy())
+    for bn in (128, 192, 256):
+        got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SKINNY_PAIR, block_n=bn)
+        assert np.array_equal(got[:16, :N], B[:16].double().numpy()), bn
 
 
 # ---------------------------------------------------------------- ragged sweep
@@ -550,9 +612,12 @@ def test_kernel_selection(plan):
     r = q(200, 4096, 4100, ldb=4101)            # a 33.6 MB B does not fit the staging buffer
     assert r["kernel"] == g.GEMM_KERNEL_GENERIC and r["staged"] == 0, r
     s = q(16, 4096, 14336)
-    assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["block_m"] == 16
-    # 112 tiles of 128 columns already saturate HBM: one share per tile, no split.
-    assert s["shares"] == 112 and s["split_k"] == 1, s
+    # 56 strips of 256 columns, K halved over the two CTAs of each cluster.
+    assert s["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR and s["block_m"] == 16, s
+    assert s["block_n"] == 256 and s["split_k"] == 2 and s["tiles"] == 56, s
+    s = q(16, 4096, 4096)
+    # 32 tiles of 128 columns: stream-K shares put every SM on the stream.
+    assert s["kernel"] == g.GEMM_KERNEL_SKINNY and s["block_m"] == 16, s
     # Tile shape by estimated time: pair tiles once their waves are cheaper than
     # one-CTA tiles' (few K-long tiles), 128 x 128 one-CTA tiles for small ones.
     for shape, kern, bn in [((2048, 8192, 2048), g.GEMM_KERNEL_PAIR, 256),

@@ -90,15 +90,20 @@ def test_operand_layouts(plan, kernel, op_a, op_b):
 
 
 @pytest.mark.parametrize("op_b", [N_, T_])
-@pytest.mark.parametrize("shares", [0, 7])
-def test_skinny_weight_layout(plan, op_b, shares):
-    """M <= 64 with B stored N x K (the weight layout): swap-AB reads it K-major."""
+@pytest.mark.parametrize("kernel,shares,block_n", [(g.GEMM_KERNEL_SKINNY, 0, 0),
+                                                   (g.GEMM_KERNEL_SKINNY, 7, 0),
+                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 128),
+                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 192),
+                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 256)])
+def test_skinny_weight_layout(plan, op_b, kernel, shares, block_n):
+    """M <= 64 with B stored N x K (the weight layout): swap-AB reads it K-major,
+    the cluster kernel as a K-major MMA B operand."""
     M, K, N = 40, 520, 392
     A, B = workloads.custom(M, K, N, "f16", seed=5 + op_b, dist="normal")
     dev = torch.device("cuda:0")
     a, b = A.to(dev), stored(B, op_b).to(dev)
     c = torch.full((M + 2, N), SENTINEL, dtype=torch.float32, device=dev)
-    plan.force(g.GEMM_KERNEL_SKINNY, shares, 0)
+    plan.force(kernel, shares, block_n)
     try:
         st = g.gemm_run_ex(plan.handle, N_, op_b, a.data_ptr(), K, b.data_ptr(), b.stride(0),
                            c.data_ptr(), N, g.GEMM_OUT_F32, M, N, K, g.GEMM_F16,
@@ -114,7 +119,8 @@ def test_skinny_weight_layout(plan, op_b, shares):
 @pytest.mark.parametrize("kernel,shape", [(g.GEMM_KERNEL_PAIR, (600, 320, 520)),
                                           (g.GEMM_KERNEL_TMA, (300, 256, 264)),
                                           (g.GEMM_KERNEL_GENERIC, (130, 96, 72)),
-                                          (g.GEMM_KERNEL_SKINNY, (16, 1024, 1000))])
+                                          (g.GEMM_KERNEL_SKINNY, (16, 1024, 1000)),
+                                          (g.GEMM_KERNEL_SKINNY_PAIR, (16, 1024, 1000))])
 def test_16bit_outputs(plan, out, kernel, shape):
     M, K, N = shape
     A, B = workloads.custom(M, K, N, "bf16", seed=M + out, dist="normal")
