@@ -188,9 +188,17 @@ def cpu_baseline(w, A, B, budget_s: float = 12.0) -> dict:
     oracle.gemm(A[:rows], B, N=cols)
     dt = time.perf_counter() - t0
     fl = 2.0 * rows * cols * w.K
+    # the same oracle on one core: whole rows, as many as about 3 s allow
+    rate1 = fl / dt / cores
+    rows1 = max(1, min(w.M, int(rate1 * 3.0 / (2.0 * w.N * w.K))))
+    t1 = time.perf_counter()
+    oracle.gemm(A[:rows1], B, nthreads=1)
+    dt1 = time.perf_counter() - t1
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"C[0:{rows}, 0:{cols}] of {w.name} (K = {w.K}; fp64 i-k-j loop, "
-                      f"{cores} threads), {dt:.1f} s"}
+                      f"{cores} threads), {dt:.1f} s",
+            "one_core": {"value": 2.0 * rows1 * w.N * w.K / dt1 / 1e12, "unit": "TFLOP/s",
+                         "cores": 1, "sample": f"C[0:{rows1}, 0:{w.N}] of {w.name}, {dt1:.1f} s"}}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -429,8 +437,64 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
                    "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                    "bytes_alg": w.bytes_alg}
     del a, bs, c
+    out.update(small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src))
     out.update(softmax_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
     out.update(attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
+    return out
+
+
+def small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
+    """The two small configurations (256^3 fp16 and the ragged 1023x1000x1029 fp16
+    with tight pitches, so that B's 1029 is not 16-byte aligned and is staged):
+    GPU time per launch from a replayed
+    CUDA graph of 20 launches, and the one-off cost of a single call -- host
+    enqueue plus launch latency, from the call until the stream has finished --
+    reported separately, as the launch overhead dominates at these sizes."""
+    out = {}
+    for name in ("gemm256_f16", "ragged1023x1000x1029_f16"):
+        w = workloads.WORKLOADS[name]
+        A, B = workloads.make_inputs(w)
+        a, b = A.to(dev), B.to(dev)      # tight pitches (the ragged B: 1029, not 16-byte)
+        c = torch.empty(w.M, w.N, dtype=torch.float32, device=dev)
+        cfg = plan.query(a, b, c, w.M, w.N, w.K)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                plan.run(a, b, c, w.M, w.N, w.K, stream=stream)
+        torch.cuda.synchronize()
+        per_graph = 20
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for _ in range(per_graph):
+                plan.run(a, b, c, w.M, w.N, w.K, stream=cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(15)]
+        for e0, e1 in ev:
+            e0.record()
+            graph.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        ms = sorted(e0.elapsed_time(e1) / per_graph for e0, e1 in ev)
+        t = ms[len(ms) // 2] / 1e3
+        # one call at a time: from the call until the stream is idle again
+        walls = []
+        for _ in range(50):
+            t0 = time.perf_counter()
+            plan.run(a, b, c, w.M, w.N, w.K, stream=stream)
+            stream.synchronize()
+            walls.append(time.perf_counter() - t0)
+        walls.sort()
+        wall = walls[len(walls) // 2]
+        roof = max(w.flops / (peaks["bf16_tflops"] * 1e12), w.bytes_alg / (peaks["hbm_gbs"] * 1e9))
+        out[name] = {"tflops": w.flops / t / 1e12, "gpu_us_per_launch": t * 1e6,
+                     "single_call_us": wall * 1e6, "launch_overhead_us": (wall - t) * 1e6,
+                     "roofline_us": roof * 1e6, "roofline_frac": roof / t,
+                     "timing": f"CUDA graph of {per_graph} launches replayed 15 times (median); "
+                               "single call = host enqueue to stream idle, median of 50",
+                     "kernel": cfg["kernel_name"], "staged": cfg["staged"]}
+        del a, b, c
     return out
 
 
