@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -135,6 +136,27 @@ inline int64_t skinny_auto_shares(int tiles, int num_kb, int num_sms) {
 
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error; none synchronises.
+
+// Launch as a programmatic dependent of the previous work in the stream: the
+// kernel may start (barrier setup, TMEM allocation, descriptor prefetch) while
+// that work drains, and waits for it (griddepcontrol.wait) before it touches
+// global memory.  Every kernel launched this way makes that wait before its
+// first global access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // a_mn: A is stored K x M (transposed, M contiguous); otherwise M x K.
 // b_mn: B is stored K x N (N contiguous); otherwise N x K (transposed).

@@ -150,6 +150,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     cluster_sync();      // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();      // the previous grid's writes (A, B, C, workspace, counters) are done
+    griddep_launch_dependents();
 
     const int num_kb = p.num_kb;
     const int cid = static_cast<int>(cluster_id_x());
@@ -483,10 +485,9 @@ cudaError_t set_attrs() {
 template <int BN, int STAGES, bool A_MN, bool B_MN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
-    gemm_pair_kernel<BN, STAGES, A_MN, B_MN>
-        <<<grid, PairCfg<BN, STAGES>::kThreads, PairCfg<BN, STAGES>::kSmemBytes, s>>>(a, b, c, p,
-                                                                                   idesc);
-    return cudaGetLastError();
+    return launch_pdl(gemm_pair_kernel<BN, STAGES, A_MN, B_MN>, dim3(grid),
+                      dim3(PairCfg<BN, STAGES>::kThreads), PairCfg<BN, STAGES>::kSmemBytes, s, a, b,
+                      c, p, idesc);
 }
 
 template <int BN, int STAGES>

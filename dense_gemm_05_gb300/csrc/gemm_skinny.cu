@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();                  // the previous grid's writes (A, B, C, workspace, counters) are done
+    griddep_launch_dependents();
     const int num_kb = p.num_kb;
 
     if (warp == 0) {
@@ -374,15 +376,12 @@ cudaError_t set_attrs() {
 template <int MS, int STAGES>
 cudaError_t launch(bool b_mn, const CUtensorMap& b, const CUtensorMap& a, const Params& p,
                    uint32_t idesc, int grid, cudaStream_t s) {
+    using Cfg = SkCfg<MS, STAGES>;
     if (b_mn)
-        gemm_skinny_kernel<MS, STAGES, true>
-            <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p,
-                                                                                   idesc);
-    else
-        gemm_skinny_kernel<MS, STAGES, false>
-            <<<grid, SkCfg<MS, STAGES>::kThreads, SkCfg<MS, STAGES>::kSmemBytes, s>>>(b, a, p,
-                                                                                   idesc);
-    return cudaGetLastError();
+        return launch_pdl(gemm_skinny_kernel<MS, STAGES, true>, dim3(grid), dim3(Cfg::kThreads),
+                          Cfg::kSmemBytes, s, b, a, p, idesc);
+    return launch_pdl(gemm_skinny_kernel<MS, STAGES, false>, dim3(grid), dim3(Cfg::kThreads),
+                      Cfg::kSmemBytes, s, b, a, p, idesc);
 }
 }  // namespace
 

@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();                  // the previous grid's writes (A, B, C, workspace) are done
+    griddep_launch_dependents();
 
     const int total = p.tiles_m * p.tiles_n;
     const int num_kb = p.num_kb;
@@ -367,9 +369,8 @@ template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
     using Cfg = TcCfg<BN, STAGES, GENERIC>;
-    gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>
-        <<<grid, Cfg::kThreads, Cfg::kSmemBytes, s>>>(a, b, c, p, idesc);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>, dim3(grid),
+                      dim3(Cfg::kThreads), Cfg::kSmemBytes, s, a, b, c, p, idesc);
 }
 
 template <int BN, int STAGES, bool GENERIC>

@@ -4,6 +4,7 @@
 // aligned rows).  One thread writes one 16-byte piece (8 elements) of a
 // destination row; the columns from `cols` up to the padded pitch are zero.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace dg {
 
@@ -12,6 +13,8 @@ namespace {
 __global__ void __launch_bounds__(256)
     stage_rows_kernel(const uint16_t* __restrict__ src, int64_t lds, uint16_t* __restrict__ dst,
                       int64_t ldd, int64_t rows, int64_t cols) {
+    griddep_wait();        // src may be written, dst still read, by the previous grid
+    griddep_launch_dependents();
     const int64_t pieces = (cols + 7) / 8;          // per row; ldd >= 8 * pieces
     const int64_t total = rows * pieces;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -37,9 +40,8 @@ cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, i
     const int64_t total = rows * ((cols + 7) / 8);
     const int64_t blocks = (total + 255) / 256;
     const int64_t cap = int64_t(num_sms) * 8;
-    stage_rows_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(
-        src, lds, dst, ldd, rows, cols);
-    return cudaGetLastError();
+    return launch_pdl(stage_rows_kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)),
+                      dim3(256), 0, stream, src, lds, dst, ldd, rows, cols);
 }
 
 }  // namespace dg
