@@ -53,7 +53,7 @@ def load_peaks() -> tuple[dict, str]:
 # a traffic figure taken with ncu is reported only while these files are unchanged.
 HEADLINE_KERNEL_SOURCES = ("common.cuh", "ptx.cuh", "tiles.cuh", "gemm_pair.cu")
 KERNEL_SYMBOLS = {"pair": "gemm_pair_kernel", "tma": "gemm_tc_kernel", "generic": "gemm_tc_kernel",
-                  "skinny": "gemm_skinny_kernel", "skinny_pair": "gemm_skpair_kernel"}
+                  "skinny": "gemm_skinny_kernel", "split_pair": "gemm_splitpair_kernel"}
 
 
 def kernel_source_hash() -> str:

@@ -44,10 +44,10 @@ GEMM_KERNEL_TMA = 2
 GEMM_KERNEL_GENERIC = 3
 GEMM_KERNEL_SKINNY = 4
 GEMM_KERNEL_PAIR = 5
-GEMM_KERNEL_SKINNY_PAIR = 6
+GEMM_KERNEL_SPLIT_PAIR = 6
 
 KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 5: "pair",
-                6: "skinny_pair"}
+                6: "split_pair"}
 
 #: Every function the header declares (checked by the tests against the library's exports).
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",

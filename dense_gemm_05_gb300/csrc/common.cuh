@@ -192,13 +192,14 @@ cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
                         const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
                         uint32_t idesc, int grid, cudaStream_t stream);
 
-// Small M on 2-CTA clusters: a cluster per BN-column strip of C splits the K loop in
-// halves and exchanges half of its partial through distributed shared memory.
-// ms in {16, 32, 64} (M padded), bn in {128, 192, 256}; grid = 2 x strips; num_kb >= 2.
-int skpair_stages(int ms, int bn);
-cudaError_t skpair_prepare();
-int skpair_max_clusters();       // co-resident 2-CTA clusters (0 = unknown)
-cudaError_t launch_skpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
+// 2-CTA clusters that split each output tile's K loop in halves and exchange half
+// of their partials through distributed shared memory.  ms in {16, 32, 64} (M <= 64
+// padded: one strip of rows) with bn in {128, 192, 256}, or ms = 128 (tiles of 128
+// rows) with bn = 128; grid = 2 x tiles_m x tiles_n; num_kb >= 2; A not transposed.
+int splitpair_stages(int ms, int bn);
+cudaError_t splitpair_prepare();
+int splitpair_max_clusters();       // co-resident 2-CTA clusters (0 = unknown)
+cudaError_t launch_splitpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
                           const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
                           cudaStream_t stream);
 

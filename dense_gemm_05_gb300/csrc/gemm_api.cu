@@ -46,7 +46,7 @@ struct gemm_plan_s {
     int force_split = 0;
     int force_bn = 0;
     int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
-    int skpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
+    int splitpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
     bool debug_sync = false;
     uint64_t timeout_ns = 2000000000ull;
 };
@@ -57,6 +57,7 @@ constexpr size_t kWorkspaceBytes = size_t(64) << 20;   // split-K / stream-K par
 constexpr int64_t kPairMinShareKb = 16;   // a pair stream-K share streams at least this many K blocks
 constexpr size_t kStageBytes = size_t(32) << 20;       // staging copies of misaligned operands
 constexpr int kPairMinSkKb = 32;          // K blocks per tile below which no pair stream-K phase
+constexpr int kSplitPairMinKb = 12;       // K blocks below which M > 64 keeps one-CTA tiles
 
 // Kernel choice: flop/s each SM sustains on one tile of each kind, measured on
 // GB300 with one wave of tiles (bf16, K = 8192): pair tiles 256 x 256 (two
@@ -182,7 +183,7 @@ struct Args {
 struct Choice {
     int kernel = GEMM_KERNEL_NONE;
     int bn = 0;          // TMA/GENERIC: tile columns
-    int ms = 0;          // SKINNY, SKINNY_PAIR: padded M
+    int ms = 0;          // SKINNY, SPLIT_PAIR: padded M
     int split = 1;       // SKINNY: most stream-K shares that touch one tile
     int shares = 0;      // SKINNY: stream-K shares
     int max_slots = 0;   // SKINNY: workspace slots per tile
@@ -321,9 +322,9 @@ bool plan_staging(const gemm_plan_s* plan, const Args& a, Staging* st, Args* out
 // stages leave room for only four in flight), if those fit in one wave.
 // Measured at M = 16, K = 4096: N = 8192 128 columns 13.6 us, 256 14.3;
 // N = 14336 256 columns 21.1 us, 192 21.9; at M = 64 192 columns 23.1 us, 256 24.4.
-int skpair_auto_width(const gemm_plan_s* plan, const Args& a) {
+int splitpair_auto_width(const gemm_plan_s* plan, const Args& a) {
     if (2 * cdiv(a.N, 128) <= plan->num_sms) return 128;
-    if (a.M > 32 && cdiv(a.N, 192) <= plan->skpair_clusters) return 192;
+    if (a.M > 32 && cdiv(a.N, 192) <= plan->splitpair_clusters) return 192;
     return 256;
 }
 
@@ -333,11 +334,11 @@ int skpair_auto_width(const gemm_plan_s* plan, const Args& a) {
 // pays a global fix-up (measured at M = 16, K = 4096: N = 4096, 64 CTAs of the
 // cluster kernel 12.3 us against 11.3 for stream-K; N = 8192, 128 CTAs 13.6
 // against 16.1; N = 28672, two waves, 42.6 against 49.1).
-int skpair_auto_bn(const gemm_plan_s* plan, const Args& a) {
-    if (plan->skpair_clusters <= 0 || cdiv(a.K, dg::kBK) < 16) return 0;
-    const int bn = skpair_auto_width(plan, a);
+int splitpair_auto_bn(const gemm_plan_s* plan, const Args& a) {
+    if (plan->splitpair_clusters <= 0 || cdiv(a.K, dg::kBK) < 16) return 0;
+    const int bn = splitpair_auto_width(plan, a);
     const int64_t strips = cdiv(a.N, bn);
-    const int64_t first_wave = std::min<int64_t>(strips, plan->skpair_clusters);
+    const int64_t first_wave = std::min<int64_t>(strips, plan->splitpair_clusters);
     if (5 * 2 * first_wave < 3 * int64_t(plan->num_sms)) return 0;
     return bn;
 }
@@ -359,9 +360,20 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (tma && a.M <= 64 && a.op_a == GEMM_OP_N) {
             // A cluster per strip of columns (K split in two) when the strips
             // fill nearly every SM in one wave; otherwise stream-K over tiles.
-            const int bn = skpair_auto_bn(plan, a);
-            kernel = bn ? GEMM_KERNEL_SKINNY_PAIR : GEMM_KERNEL_SKINNY;
+            const int bn = splitpair_auto_bn(plan, a);
+            kernel = bn ? GEMM_KERNEL_SPLIT_PAIR : GEMM_KERNEL_SKINNY;
             auto_bn = bn;
+        } else if (tma && a.op_a == GEMM_OP_N && plan->splitpair_clusters > 0 &&
+                   cdiv(a.M, dg::kBM) * cdiv(a.N, 128) <= plan->splitpair_clusters &&
+                   cdiv(a.K, dg::kBK) >= kSplitPairMinKb) {
+            // Few 128 x 128 tiles (one wave of clusters): each tile's K loop split
+            // over a 2-CTA cluster puts twice as many SMs on the problem as
+            // one-CTA tiles do.  Measured (graph-replayed, M x K x N):
+            // 1024 x 8192 x 1024 39.7 -> 23.1 us, 256 x 4096 x 2048 21.6 -> 14.3,
+            // 1023 x 1000 x 1029 18.9 -> 15.1; at 16 K blocks and fewer it is
+            // about even (1024^3 8.1 vs 8.3 us), below 12 slower (65 x 512 x 512).
+            kernel = GEMM_KERNEL_SPLIT_PAIR;
+            auto_bn = 128;
         } else if (tma) {
             // The cheapest of pair tiles 256 x 256, one-CTA tiles 128 x 256 and
             // 128 x 128 under est_seconds (waves x time of one tile).
@@ -387,19 +399,21 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         }
     }
     if ((kernel == GEMM_KERNEL_TMA || kernel == GEMM_KERNEL_SKINNY ||
-         kernel == GEMM_KERNEL_PAIR || kernel == GEMM_KERNEL_SKINNY_PAIR) && !tma)
+         kernel == GEMM_KERNEL_PAIR || kernel == GEMM_KERNEL_SPLIT_PAIR) && !tma)
         return GEMM_ERR_UNSUPPORTED;
-    if ((kernel == GEMM_KERNEL_SKINNY || kernel == GEMM_KERNEL_SKINNY_PAIR) &&
-        (a.M > 64 || a.op_a != GEMM_OP_N))
+    if (kernel == GEMM_KERNEL_SKINNY && (a.M > 64 || a.op_a != GEMM_OP_N))
         return GEMM_ERR_UNSUPPORTED;
-    if (kernel == GEMM_KERNEL_SKINNY_PAIR && (cdiv(a.K, dg::kBK) < 2 || plan->skpair_clusters <= 0))
+    if (kernel == GEMM_KERNEL_SPLIT_PAIR &&
+        (a.op_a != GEMM_OP_N || (a.M > 64 && plan->force_bn != 0 && plan->force_bn != 128)))
+        return GEMM_ERR_UNSUPPORTED;
+    if (kernel == GEMM_KERNEL_SPLIT_PAIR && (cdiv(a.K, dg::kBK) < 2 || plan->splitpair_clusters <= 0))
         return GEMM_ERR_UNSUPPORTED;
     // 192-column tiles exist only in the small-M cluster kernel.
-    if (plan->force_bn == 192 && kernel != GEMM_KERNEL_SKINNY_PAIR) return GEMM_ERR_UNSUPPORTED;
+    if (plan->force_bn == 192 && kernel != GEMM_KERNEL_SPLIT_PAIR) return GEMM_ERR_UNSUPPORTED;
     if (kernel == GEMM_KERNEL_PAIR && plan->pair_clusters[0] <= 0) return GEMM_ERR_UNSUPPORTED;
     if (kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_SKINNY &&
         kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR &&
-        kernel != GEMM_KERNEL_SKINNY_PAIR)
+        kernel != GEMM_KERNEL_SPLIT_PAIR)
         return GEMM_ERR_UNSUPPORTED;
     c->kernel = kernel;
     c->num_kb = static_cast<int>(cdiv(a.K, dg::kBK));
@@ -411,17 +425,22 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         if (!choose_shares(plan, c, plan->force_split)) return GEMM_ERR_UNSUPPORTED;
         c->units = c->shares;
         c->stages = dg::skinny_stages(c->ms);
-    } else if (kernel == GEMM_KERNEL_SKINNY_PAIR) {
-        c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : 64);
-        c->bn = plan->force_bn ? plan->force_bn : (auto_bn ? auto_bn : skpair_auto_width(plan, a));
-        c->tiles_m = 1;
-        const int64_t strips = cdiv(a.N, c->bn);
-        if (strips > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
-        c->tiles_n = static_cast<int>(strips);
-        c->units = c->tiles_n;
+    } else if (kernel == GEMM_KERNEL_SPLIT_PAIR) {
+        c->ms = a.M <= 16 ? 16 : (a.M <= 32 ? 32 : (a.M <= 64 ? 64 : 128));
+        if (c->ms == 128)
+            c->bn = 128;
+        else
+            c->bn = plan->force_bn ? plan->force_bn
+                                   : (auto_bn ? auto_bn : splitpair_auto_width(plan, a));
+        const int64_t tm = c->ms == 128 ? cdiv(a.M, dg::kBM) : 1;
+        const int64_t tiles = tm * cdiv(a.N, c->bn);
+        if (tiles > INT32_MAX / 2) return GEMM_ERR_UNSUPPORTED;
+        c->tiles_m = static_cast<int>(tm);
+        c->tiles_n = static_cast<int>(cdiv(a.N, c->bn));
+        c->units = static_cast<int>(tiles);
         c->split = 2;
-        c->grid = 2 * c->tiles_n;
-        c->stages = dg::skpair_stages(c->ms, c->bn);
+        c->grid = 2 * c->units;
+        c->stages = dg::splitpair_stages(c->ms, c->bn);
         return GEMM_OK;
     } else if (kernel == GEMM_KERNEL_PAIR) {
         const int64_t tm = cdiv(a.M, 2 * dg::kBM);
@@ -597,7 +616,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     if (encode_fn() == nullptr) return GEMM_ERR_CUDA;
     if (dg::tma_prepare() != cudaSuccess || dg::generic_prepare() != cudaSuccess ||
         dg::skinny_prepare() != cudaSuccess || dg::pair_prepare() != cudaSuccess ||
-        dg::skpair_prepare() != cudaSuccess) {
+        dg::splitpair_prepare() != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -609,7 +628,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     // persistent grids by what the device can co-schedule.
     p->pair_clusters[0] = dg::pair_max_clusters(128);
     p->pair_clusters[1] = dg::pair_max_clusters(256);
-    p->skpair_clusters = dg::skpair_max_clusters();
+    p->splitpair_clusters = dg::splitpair_max_clusters();
     p->debug_sync = env_flag("GEMM_DEBUG_SYNC");
     if (const char* t = std::getenv("GEMM_WAIT_TIMEOUT_MS")) {
         const long long ms = std::atoll(t);
@@ -667,7 +686,7 @@ gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
         return GEMM_ERR_INVALID_ARG;
     if (kernel != 0 && kernel != GEMM_KERNEL_TMA && kernel != GEMM_KERNEL_GENERIC &&
         kernel != GEMM_KERNEL_SKINNY && kernel != GEMM_KERNEL_PAIR &&
-        kernel != GEMM_KERNEL_SKINNY_PAIR)
+        kernel != GEMM_KERNEL_SPLIT_PAIR)
         return GEMM_ERR_INVALID_ARG;
     plan->force_kernel = kernel;
     plan->force_split = split_k;
@@ -700,7 +719,7 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     if (st != GEMM_OK) return st;
     gemm_config_t cfg{};
     cfg.kernel = c.kernel;
-    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY || c.kernel == GEMM_KERNEL_SKINNY_PAIR)
+    cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY || c.kernel == GEMM_KERNEL_SPLIT_PAIR)
                       ? c.ms
                       : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM : dg::kBM);
     cfg.block_n = (c.kernel == GEMM_KERNEL_SKINNY) ? 128 : c.bn;
@@ -710,7 +729,7 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     cfg.grid = c.grid;
     cfg.cluster = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL)
                       ? 0
-                      : ((c.kernel == GEMM_KERNEL_PAIR || c.kernel == GEMM_KERNEL_SKINNY_PAIR) ? 2
+                      : ((c.kernel == GEMM_KERNEL_PAIR || c.kernel == GEMM_KERNEL_SPLIT_PAIR) ? 2
                                                                                           : 1);
     cfg.group = (c.kernel == GEMM_KERNEL_TMA || c.kernel == GEMM_KERNEL_GENERIC ||
                  c.kernel == GEMM_KERNEL_PAIR)
@@ -832,14 +851,14 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             err = dg::launch_pair(c.bn, a_mn, b_mn, ma, mb, mc, p,
                                   dg::idesc_f16(bf16, a_mn, b_mn, 2 * dg::kBM, c.bn), c.grid,
                                   stream);
-        } else if (c.kernel == GEMM_KERNEL_SKINNY_PAIR) {
+        } else if (c.kernel == GEMM_KERNEL_SPLIT_PAIR) {
             // A tile (M <= 64 rows, K-major) as the MMA's 128-row A operand, the
             // B tile (bn columns) as its B operand.
             CUtensorMap ma, mb;
             if (!map_a(&ma, static_cast<uint32_t>(c.ms)) ||
                 !map_b(&mb, static_cast<uint32_t>(c.bn)))
                 return GEMM_ERR_CUDA;
-            err = dg::launch_skpair(c.ms, c.bn, b_mn, ma, mb, p,
+            err = dg::launch_splitpair(c.ms, c.bn, b_mn, ma, mb, p,
                                     dg::idesc_f16(bf16, false, b_mn, dg::kBM, c.bn), c.grid,
                                     stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {

@@ -1,18 +1,20 @@
-// gemm_skpair.cu -- small-M GEMM for sm_103a on every SM without a global
-// split-K reduction.
+// gemm_splitpair.cu -- GEMM for sm_103a whose output tiles are too few to
+// occupy every SM: each tile's K loop is split over the two CTAs of a cluster,
+// without a global split-K reduction.
 //
-// C[M, N] (M <= 64) is cut into strips of BN columns; each strip is computed by
-// a cluster of two CTAs, one per half of the K loop (the K-sum of "Writing GPU
-// kernels in Triton", section 3.3, cut in two; exact up to rounding because the
-// sum is associative).  N on the MMA's N side: the A tile (M rows, zero-filled
-// to a multiple of 16 by the tensor-memory-access engine) is the MMA's A
-// operand of 128 rows, and the B tile the MMA's B operand, so one tcgen05.mma
-// consumes BN x 16 elements of B -- the stream that bounds the problem -- and
-// the tensor core stays far below the rate that the B stream needs (a swap-AB
-// MMA with M = 16 as its N would move only 128 x 16 elements of B per
-// instruction).  Rows M..127 of the 128-row A window hold whatever follows the
-// A tile in shared memory; they only feed accumulator rows that are never
-// read.
+// C[M, N] is cut into tiles of MS rows x BN columns (MS = 16, 32 or 64 for
+// M <= 64: one strip of rows; MS = 128 otherwise, tile rows tm = 0, 1, ...);
+// each tile is computed by a cluster of two CTAs, one per half of the K loop
+// (the K-sum of "Writing GPU kernels in Triton", section 3.3, cut in two; exact
+// up to rounding because the sum is associative).  N on the MMA's N side: the
+// A tile (MS rows, zero-filled beyond M by the tensor-memory-access engine) is
+// the MMA's A operand of 128 rows, and the B tile the MMA's B operand, so at
+// small M one tcgen05.mma consumes BN x 16 elements of B -- the stream that
+// bounds the problem -- and the tensor core stays far below the rate that the
+// B stream needs (a swap-AB MMA with M = 16 as its N would move only 128 x 16
+// elements of B per instruction).  With MS < 128, rows MS..127 of the 128-row
+// A window hold whatever follows the A tile in shared memory; they only feed
+// accumulator rows that are never read.
 //
 // When both halves are summed, each CTA keeps one half of the strip's columns:
 // it sends the other half of its fp32 partial into the peer CTA's shared memory
@@ -37,7 +39,7 @@
 namespace dg {
 
 template <int MS, int BN, int STAGES>
-struct SkPairCfg {
+struct SplitPairCfg {
     static constexpr int kAStageBytes = MS * kBK * 2;       // A tile: MS rows x 64 k, K-major
     static constexpr int kBStageBytes = BN * kBK * 2;       // B tile: BN n x 64 k
     static constexpr int kHalf = BN / 2;                    // columns kept by each CTA
@@ -48,7 +50,7 @@ struct SkPairCfg {
     static constexpr int kNumBars = 2 * STAGES + 3;
     static constexpr int kSmemBytes =
         1024 + STAGES * (kAStageBytes + kBStageBytes) + kXBytes + 8 * kNumBars + 16;
-    static_assert(MS == 16 || MS == 32 || MS == 64, "MS");
+    static_assert(MS == 16 || MS == 32 || MS == 64 || MS == 128, "MS");
     static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "BN");
     // The MMA reads a 128-row (16 KiB) A window from each A stage; the B ring
     // behind the A stages keeps the last window inside the allocation.
@@ -59,10 +61,10 @@ struct SkPairCfg {
 
 template <int MS, int BN, int STAGES, bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
-    gemm_skpair_kernel(const __grid_constant__ CUtensorMap mapA,
+    gemm_splitpair_kernel(const __grid_constant__ CUtensorMap mapA,
                        const __grid_constant__ CUtensorMap mapB, const Params p,
                        const uint32_t idesc) {
-    using Cfg = SkPairCfg<MS, BN, STAGES>;
+    using Cfg = SplitPairCfg<MS, BN, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -82,8 +84,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
-    const int strip = static_cast<int>(cluster_id_x());
-    const int n0 = strip * BN;
+    const int tile = static_cast<int>(cluster_id_x());
+    const int tm = tile / p.tiles_n;                 // 0 unless MS == 128
+    const int n0 = (tile - tm * p.tiles_n) * BN;
+    const int m0 = tm * kBM;
     const int num_kb = p.num_kb;
     const int kb_half = num_kb / 2;                  // num_kb >= 2: both halves non-empty
     const int kb0 = rank ? kb_half : 0;
@@ -195,17 +199,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 if (__all_sync(0xffffffffu, got)) {
                     const float* xrow = sX + r * Cfg::kXPitch;
                     const int col_base = n0 + static_cast<int>(rank) * Cfg::kHalf;
+                    const int row = m0 + r;
 #pragma unroll 1
                     for (int c = 0; c < Cfg::kHalf; c += 32) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(trow + rank * Cfg::kHalf + c, v);
                         tmem_ld_wait(v);
                         const int col = col_base + c;
-                        if (r < p.M && col < p.N) {
+                        if (row < p.M && col < p.N) {
 #pragma unroll
                             for (int j = 0; j < 32; ++j)
                                 v[j] = __float_as_uint(__uint_as_float(v[j]) + xrow[c + j]);
-                            store_c32(p, static_cast<int64_t>(r) * p.ldc + col, v, p.N - col);
+                            store_c32(p, static_cast<int64_t>(row) * p.ldc + col, v, p.N - col);
                         }
                     }
                 }
@@ -222,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int armed = 0;
             const uint64_t pol_stream = l2_policy_evict_first();   // B: read once
-            const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every strip
+            const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every tile of its rows
             griddep_wait();                   // A and B may be written by the previous grid
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {
@@ -232,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 const uint32_t fb = smem_u32(&full[stage]);
                 mbar_arrive_expect_tx(
                     fb, static_cast<uint32_t>(Cfg::kAStageBytes + Cfg::kBStageBytes));
-                tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb, kb * kBK, 0,
+                tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb, kb * kBK, m0,
                                  pol_keep);
                 load_operand_hint<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb, n0,
                                         kb * kBK, BN, pol_stream);
@@ -290,9 +295,9 @@ constexpr int stages_for() {
 template <int MS, int BN, bool B_MN>
 cudaError_t set_attr_one() {
     constexpr int S = stages_for<MS, BN>();
-    return cudaFuncSetAttribute(gemm_skpair_kernel<MS, BN, S, B_MN>,
+    return cudaFuncSetAttribute(gemm_splitpair_kernel<MS, BN, S, B_MN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SkPairCfg<MS, BN, S>::kSmemBytes);
+                                SplitPairCfg<MS, BN, S>::kSmemBytes);
 }
 
 template <int MS, int BN>
@@ -305,8 +310,10 @@ cudaError_t set_attrs_bn() {
 template <int MS>
 cudaError_t set_attrs_ms() {
     cudaError_t e = set_attrs_bn<MS, 128>();
-    if (e == cudaSuccess) e = set_attrs_bn<MS, 192>();
-    if (e == cudaSuccess) e = set_attrs_bn<MS, 256>();
+    if constexpr (MS != 128) {                       // 128-row tiles: 128 columns only
+        if (e == cudaSuccess) e = set_attrs_bn<MS, 192>();
+        if (e == cudaSuccess) e = set_attrs_bn<MS, 256>();
+    }
     return e;
 }
 
@@ -322,20 +329,24 @@ cudaError_t launch_bn(bool b_mn, const CUtensorMap& a, const CUtensorMap& b, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = SkPairCfg<MS, BN, S>::kSmemBytes;
+    cfg.dynamicSmemBytes = SplitPairCfg<MS, BN, S>::kSmemBytes;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (b_mn) return cudaLaunchKernelEx(&cfg, gemm_skpair_kernel<MS, BN, S, true>, a, b, p, idesc);
-    return cudaLaunchKernelEx(&cfg, gemm_skpair_kernel<MS, BN, S, false>, a, b, p, idesc);
+    if (b_mn) return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, true>, a, b, p, idesc);
+    return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, false>, a, b, p, idesc);
 }
 
 template <int MS>
 cudaError_t launch_ms(int bn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
                       const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
-    if (bn == 128) return launch_bn<MS, 128>(b_mn, a, b, p, idesc, grid, s);
-    if (bn == 192) return launch_bn<MS, 192>(b_mn, a, b, p, idesc, grid, s);
-    return launch_bn<MS, 256>(b_mn, a, b, p, idesc, grid, s);
+    if constexpr (MS == 128) {
+        return launch_bn<MS, 128>(b_mn, a, b, p, idesc, grid, s);
+    } else {
+        if (bn == 128) return launch_bn<MS, 128>(b_mn, a, b, p, idesc, grid, s);
+        if (bn == 192) return launch_bn<MS, 192>(b_mn, a, b, p, idesc, grid, s);
+        return launch_bn<MS, 256>(b_mn, a, b, p, idesc, grid, s);
+    }
 }
 
 template <int MS, int BN>
@@ -349,11 +360,11 @@ int max_clusters_one() {
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(192, 1, 1);
-    cfg.dynamicSmemBytes = SkPairCfg<MS, BN, S>::kSmemBytes;
+    cfg.dynamicSmemBytes = SplitPairCfg<MS, BN, S>::kSmemBytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_skpair_kernel<MS, BN, S, true>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_splitpair_kernel<MS, BN, S, true>, &cfg) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -362,27 +373,30 @@ int max_clusters_one() {
 }
 }  // namespace
 
-int skpair_stages(int ms, int bn) {
+int splitpair_stages(int ms, int bn) {
     if (ms == 16) return bn == 128 ? stages_for<16, 128>() : (bn == 192 ? stages_for<16, 192>() : stages_for<16, 256>());
     if (ms == 32) return bn == 128 ? stages_for<32, 128>() : (bn == 192 ? stages_for<32, 192>() : stages_for<32, 256>());
+    if (ms == 128) return stages_for<128, 128>();
     return bn == 128 ? stages_for<64, 128>() : (bn == 192 ? stages_for<64, 192>() : stages_for<64, 256>());
 }
 
-cudaError_t skpair_prepare() {
+cudaError_t splitpair_prepare() {
     cudaError_t e = set_attrs_ms<16>();
     if (e == cudaSuccess) e = set_attrs_ms<32>();
     if (e == cudaSuccess) e = set_attrs_ms<64>();
+    if (e == cudaSuccess) e = set_attrs_ms<128>();
     return e;
 }
 
 // All (MS, BN) instantiations hold one CTA per SM, so one query serves them.
-int skpair_max_clusters() { return max_clusters_one<64, 256>(); }
+int splitpair_max_clusters() { return max_clusters_one<64, 256>(); }
 
-cudaError_t launch_skpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
+cudaError_t launch_splitpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
                           const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
                           cudaStream_t stream) {
     if (ms == 16) return launch_ms<16>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
     if (ms == 32) return launch_ms<32>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
+    if (ms == 128) return launch_ms<128>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
     return launch_ms<64>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
 }
 

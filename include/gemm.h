@@ -88,18 +88,20 @@ typedef enum {
                                    (leading dimensions or pointers not 16-byte aligned) */
     GEMM_KERNEL_SKINNY = 4,     /* small M: swap-AB + split-K, deterministic reduction */
     GEMM_KERNEL_PAIR = 5,       /* 2-SM (cta_group::2) pair tiles for large problems */
-    GEMM_KERNEL_SKINNY_PAIR = 6 /* small M: a 2-CTA cluster per strip of block_n columns of C
-                                   splits K in halves; the halves' fp32 partials meet in
-                                   distributed shared memory (no workspace, deterministic).
-                                   Chosen for M <= 64 when the first wave of strips keeps
-                                   >= 3/5 of the SMs busy and K >= 1024 */
+    GEMM_KERNEL_SPLIT_PAIR = 6  /* a 2-CTA cluster per output tile (M <= 64: a strip of all
+                                   rows x block_n columns; else 128 x 128) splits K in
+                                   halves; the halves' fp32 partials meet in distributed
+                                   shared memory (no workspace, deterministic).  Chosen for
+                                   M <= 64 when the first wave of strips keeps >= 3/5 of the
+                                   SMs busy and K >= 1024, and for M > 64 when the 128 x 128
+                                   tiles fit one wave of clusters and K >= 768 */
 } gemm_kernel_t;
 
 typedef struct {
     int32_t kernel;       /* gemm_kernel_t */
     int32_t block_m;      /* rows of C per tile (per CTA pair for GEMM_KERNEL_PAIR; the padded
-                             M, 16, 32 or 64, for SKINNY and SKINNY_PAIR) */
-    int32_t block_n;      /* columns of C per tile (SKINNY_PAIR: 128, 192 or 256 per strip) */
+                             M, 16, 32 or 64, for SKINNY and SPLIT_PAIR) */
+    int32_t block_n;      /* columns of C per tile (SPLIT_PAIR: 128, 192 or 256 per strip) */
     int32_t block_k;      /* K depth of one pipeline stage */
     int32_t stages;       /* shared-memory ring depth */
     int32_t split_k;      /* most K slices any output tile is split into (1 = none) */
@@ -201,18 +203,19 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
 
 /*
  * Force the next gemm_run calls on this plan to use `kernel` (a
- * gemm_kernel_t of TMA, GENERIC, SKINNY, PAIR or SKINNY_PAIR; 0 = automatic choice),
+ * gemm_kernel_t of TMA, GENERIC, SKINNY, PAIR or SPLIT_PAIR; 0 = automatic choice),
  * `split_k` stream-K shares for SKINNY -- the (tile, K block) iterations of
  * all tiles are cut into that many equal contiguous runs, one CTA each
  * (0 = automatic); for PAIR, `split_k` = 1 turns off the stream-K phase that
  * otherwise splits the last, partial wave of pair tiles (plus one full wave)
  * by K across all clusters, `split_k` = 2 splits every tile's K loop over all
  * clusters (whole-problem stream-K), any other value = automatic -- and `block_n`
- * tile columns for TMA/PAIR (128 or 256) or strip columns for SKINNY_PAIR (128,
+ * tile columns for TMA/PAIR (128 or 256) or strip columns for SPLIT_PAIR (128,
  * 192 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
- * arguments (e.g. SKINNY or SKINNY_PAIR with M > 64, SKINNY_PAIR with K < 128,
- * block_n 192 with another kernel, or TMA with an operand that is neither
+ * arguments (e.g. SKINNY with M > 64, SPLIT_PAIR with K < 128, with A transposed,
+ * or with block_n other than 128 for M > 64, block_n 192 with another kernel, or
+ * TMA with an operand that is neither
  * 16-byte aligned nor small enough for the staging buffer).  Forcing GENERIC
  * also turns staging off (misaligned operands are read in place).
  * Errors: INVALID_ARG (null plan, unknown kernel, negative split, bad block_n).

@@ -92,15 +92,21 @@ def test_workload_256_f16_full(plan):
 
 def test_workload_ragged_f16_full(plan):
     """M=1023 K=1000 N=1029: ldb = 1029 halves is not a 16-byte pitch -> B is staged
-    into 16-byte rows and the TMA kernel reads the copy."""
+    into 16-byte rows and the TMA-fed kernels read the copy: automatically the
+    split-K cluster kernel (72 tiles of 128 x 128 on 144 SMs), and the one-CTA
+    kernel when forced."""
     w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
     A, B = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
     cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
-    assert cfg["kernel"] == g.GEMM_KERNEL_TMA and cfg["staged"] == 2, cfg
-    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_TMA)
+    assert cfg["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and cfg["staged"] == 2, cfg
+    assert cfg["block_m"] == 128 and cfg["block_n"] == 128 and cfg["grid"] == 144, cfg
+    got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_SPLIT_PAIR)
     assert_guards(got, w.M, w.N)
     assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name)
+    got = run(plan, A, B, w.M, w.N, w.K, kernel=g.GEMM_KERNEL_TMA, expect=g.GEMM_KERNEL_TMA)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " one-CTA tiles")
 
 
 def test_workload_ragged_f16_generic_in_place(plan):
@@ -117,9 +123,13 @@ def test_workload_ragged_f16_padded_pitch_uses_tma(plan):
     """Same logical shape with 16-byte pitches (NaN padding): TMA path, ragged edges."""
     w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
     A, B = workloads.make_inputs(w, lda=1008, ldb=1032)
-    got = run(plan, A, B, w.M, w.N, w.K, ldc=1032, expect=g.GEMM_KERNEL_TMA)
+    got = run(plan, A, B, w.M, w.N, w.K, ldc=1032, kernel=g.GEMM_KERNEL_TMA,
+              expect=g.GEMM_KERNEL_TMA)
     assert_guards(got, w.M, w.N)
     assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " padded")
+    got = run(plan, A, B, w.M, w.N, w.K, ldc=1032, expect=g.GEMM_KERNEL_SPLIT_PAIR)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " padded, split pair")
 
 
 def test_workload_skinny_full_and_deterministic(plan):
@@ -128,7 +138,7 @@ def test_workload_skinny_full_and_deterministic(plan):
     dev = torch.device("cuda:0")
     cfg = plan.query(A.to(dev), B.to(dev), torch.empty(w.M, w.N, device=dev))
     # 56 strips of 256 columns on 56 two-CTA clusters.
-    assert cfg["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR, cfg
+    assert cfg["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR, cfg
     assert cfg["block_n"] == 256 and cfg["grid"] == 112 and cfg["cluster"] == 2, cfg
     got1 = run(plan, A, B, w.M, w.N, w.K)
     got2 = run(plan, A, B, w.M, w.N, w.K)
@@ -160,42 +170,51 @@ def test_skinny_stream_k_shapes(plan, M, K, N, dtype, shares):
 
 
 @pytest.mark.parametrize("M,K,N,dtype,block_n", [
-    (16, 4096, 14336, "bf16", 0),    # the M=16 workload: automatic 192-column strips
+    (16, 4096, 14336, "bf16", 0),    # the M=16 workload: automatic 256-column strips
     (1, 256, 1000, "f16", 128),      # M = 1, 4 K blocks, ragged last strip
+    (1023, 1000, 1029, "f16", 0),    # 128-row tiles, 8 x 9 of them, ragged M, K and N
+    (129, 520, 300, "bf16", 128),    # 128-row tiles: 2 rows of tiles, the second holds one row
+    (600, 2048, 1100, "bf16", 128),  # 5 x 9 tiles
+    (256, 130, 4000, "f16", 128),    # 3 K blocks, 64 tiles
+    (640, 1024, 2048, "bf16", 128),  # 80 tiles: more clusters than fit at once
     (33, 1000, 700, "bf16", 192),    # M padded to 64 (two TMEM lane quadrants), ragged K and N
     (64, 130, 513, "f16", 256),      # 3 K blocks: halves of 1 and 2, ragged everywhere
     (17, 2048, 9728, "bf16", 128),   # M padded to 32, 76 strips
     (16, 128, 256, "bf16", 256),     # 2 K blocks: one per CTA, a single strip
     (8, 512, 40000, "bf16", 128),    # 313 strips: more clusters than fit at once
 ])
-def test_skinny_pair_shapes(plan, M, K, N, dtype, block_n):
+def test_split_pair_shapes(plan, M, K, N, dtype, block_n):
     """Small M on 2-CTA clusters (K halves exchanged through distributed shared memory)."""
     A, B = workloads.custom(M, K, N, dtype, seed=M + K + N + 1, dist="normal")
-    kernel = 0 if block_n == 0 else g.GEMM_KERNEL_SKINNY_PAIR
+    kernel = 0 if block_n == 0 else g.GEMM_KERNEL_SPLIT_PAIR
     got1 = run(plan, A, B, M, N, K, kernel=kernel, block_n=block_n,
-               expect=g.GEMM_KERNEL_SKINNY_PAIR)
+               expect=g.GEMM_KERNEL_SPLIT_PAIR)
     got2 = run(plan, A, B, M, N, K, kernel=kernel, block_n=block_n)
     assert_guards(got1, M, N)
     assert np.array_equal(got1, got2), "result changed between runs"
     assert_close(got1[:M, :N], A, B, M, N, K, f"skinny pair {M}x{N}x{K} bn={block_n}")
 
 
-def test_skinny_pair_query(plan):
+def test_split_pair_query(plan):
     dev = torch.device("cuda:0")
     a = torch.empty(64, 4096, dtype=torch.bfloat16, device=dev)
     b = torch.empty(4096, 40000, dtype=torch.bfloat16, device=dev)
     c = torch.empty(64, 40000, device=dev)
-    plan.force(g.GEMM_KERNEL_SKINNY_PAIR, 0, 192)
+    plan.force(g.GEMM_KERNEL_SPLIT_PAIR, 0, 192)
     try:
         cfg = plan.query(a, b, c, 20, 1000, 4096)
         assert cfg["block_m"] == 32 and cfg["block_n"] == 192 and cfg["split_k"] == 2, cfg
         assert cfg["tiles"] == 6 and cfg["grid"] == 12 and cfg["cluster"] == 2, cfg
-        plan.force(g.GEMM_KERNEL_SKINNY_PAIR, 0, 0)
+        plan.force(g.GEMM_KERNEL_SPLIT_PAIR, 0, 0)
         assert plan.query(a, b, c, 20, 1000, 4096)["block_n"] == 128
         assert plan.query(a, b, c, 20, 14336, 4096)["block_n"] == 256
         assert plan.query(a, b, c, 40, 14336, 4096)["block_n"] == 192
+        r = plan.query(a, b, c, 65, 1000, 4096)          # M > 64: tiles of 128 x 128
+        assert r["block_m"] == 128 and r["block_n"] == 128 and r["tiles"] == 8, r
+        plan.force(g.GEMM_KERNEL_SPLIT_PAIR, 0, 192)
         with pytest.raises(RuntimeError):
-            plan.query(a, b, c, 65, 1000, 4096)          # M > 64
+            plan.query(a, b, c, 65, 1000, 4096)          # M > 64 takes 128 columns only
+        plan.force(g.GEMM_KERNEL_SPLIT_PAIR, 0, 0)
         with pytest.raises(RuntimeError):
             plan.query(a, b, c, 16, 1000, 64)            # one K block
         plan.force(g.GEMM_KERNEL_TMA, 0, 192)            # 192 columns: this kernel only
@@ -205,7 +224,7 @@ def test_skinny_pair_query(plan):
         plan.force(0, 0, 0)
     # automatic: few strips leave SMs idle, so the stream-K kernel is chosen
     assert plan.query(a, b, c, 16, 4096, 4096)["kernel"] == g.GEMM_KERNEL_SKINNY
-    assert plan.query(a, b, c, 16, 8192, 4096)["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR
+    assert plan.query(a, b, c, 16, 8192, 4096)["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR
     assert plan.query(a, b, c, 16, 14336, 512)["kernel"] == g.GEMM_KERNEL_SKINNY   # 8 K blocks
 
 
@@ -416,8 +435,9 @@ def int_inputs(M, K, N, dtype, seed, lda=None, ldb=None):
     (g.GEMM_KERNEL_SKINNY, 12, (16, 4096, 1024), "bf16"),
     (g.GEMM_KERNEL_SKINNY, 0, (33, 2048, 640), "f16"),
     (g.GEMM_KERNEL_SKINNY, 3, (64, 1000, 256), "bf16"),
-    (g.GEMM_KERNEL_SKINNY_PAIR, 192, (16, 4096, 1024), "bf16"),
-    (g.GEMM_KERNEL_SKINNY_PAIR, 128, (40, 1000, 520), "f16"),
+    (g.GEMM_KERNEL_SPLIT_PAIR, 192, (16, 4096, 1024), "bf16"),
+    (g.GEMM_KERNEL_SPLIT_PAIR, 128, (40, 1000, 520), "f16"),
+    (g.GEMM_KERNEL_SPLIT_PAIR, 128, (300, 1000, 520), "bf16"),
     (g.GEMM_KERNEL_PAIR, 128, (600, 1024, 1104), "bf16"),
     (g.GEMM_KERNEL_PAIR, 256, (600, 1024, 1104), "f16"),
     (g.GEMM_KERNEL_PAIR, 256, (1024, 4096, 1024), "bf16"),
@@ -426,7 +446,7 @@ def test_small_integer_inputs_are_bit_exact(plan, kernel, split, shape, dtype):
     """For the pair kernels the second parameter is the tile width (block_n)."""
     M, K, N = shape
     A, B = int_inputs(M, K, N, dtype, seed=M + K + N)
-    if kernel in (g.GEMM_KERNEL_PAIR, g.GEMM_KERNEL_SKINNY_PAIR):
+    if kernel in (g.GEMM_KERNEL_PAIR, g.GEMM_KERNEL_SPLIT_PAIR):
         got = run(plan, A, B, M, N, K, kernel=kernel, block_n=split, expect=kernel)
     else:
         got = run(plan, A, B, M, N, K, kernel=kernel, split=split, expect=kernel)
@@ -450,7 +470,7 @@ def test_mn_major_layout_pin(plan):
     got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SKINNY, split=2)
     assert np.array_equal(got[:16, :N], B[:16].double().numpy())
     for bn in (128, 192, 256):
-        got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SKINNY_PAIR, block_n=bn)
+        got = run(plan, A16, B, 16, N, K, kernel=g.GEMM_KERNEL_SPLIT_PAIR, block_n=bn)
         assert np.array_equal(got[:16, :N], B[:16].double().numpy()), bn
 
 
@@ -607,13 +627,13 @@ def test_kernel_selection(plan):
         return plan.query(a, b, c, M, N, K)
     assert q(8192, 8192, 8192)["kernel"] == g.GEMM_KERNEL_PAIR
     assert q(8192, 8192, 8192)["block_n"] == 256
-    r = q(1023, 1000, 1029)                     # odd ldb: B staged, then TMA
-    assert r["kernel"] == g.GEMM_KERNEL_TMA and r["staged"] == 2, r
+    r = q(1023, 1000, 1029)                     # odd ldb: B staged, then TMA-fed split pairs
+    assert r["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and r["staged"] == 2, r
     r = q(200, 4096, 4100, ldb=4101)            # a 33.6 MB B does not fit the staging buffer
     assert r["kernel"] == g.GEMM_KERNEL_GENERIC and r["staged"] == 0, r
     s = q(16, 4096, 14336)
     # 56 strips of 256 columns, K halved over the two CTAs of each cluster.
-    assert s["kernel"] == g.GEMM_KERNEL_SKINNY_PAIR and s["block_m"] == 16, s
+    assert s["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and s["block_m"] == 16, s
     assert s["block_n"] == 256 and s["split_k"] == 2 and s["tiles"] == 56, s
     s = q(16, 4096, 4096)
     # 32 tiles of 128 columns: stream-K shares put every SM on the stream.
@@ -623,8 +643,9 @@ def test_kernel_selection(plan):
     for shape, kern, bn in [((2048, 8192, 2048), g.GEMM_KERNEL_PAIR, 256),
                             ((512, 8192, 8192), g.GEMM_KERNEL_PAIR, 256),
                             ((1536, 1536, 1536), g.GEMM_KERNEL_TMA, 128),
-                            ((128, 8192, 8192), g.GEMM_KERNEL_TMA, 128),
-                            ((1024, 8192, 1024), g.GEMM_KERNEL_TMA, 128)]:
+                            ((128, 8192, 8192), g.GEMM_KERNEL_SPLIT_PAIR, 128),
+                            ((1024, 8192, 1024), g.GEMM_KERNEL_SPLIT_PAIR, 128),
+                            ((1024, 512, 1024), g.GEMM_KERNEL_TMA, 128)]:
         r = q(*shape)
         assert r["kernel"] == kern and r["block_n"] == bn, (shape, r)
     assert q(4096, 1024, 4096)["shares"] == 0       # 16 K blocks: no stream-K phase

@@ -92,9 +92,9 @@ def test_operand_layouts(plan, kernel, op_a, op_b):
 @pytest.mark.parametrize("op_b", [N_, T_])
 @pytest.mark.parametrize("kernel,shares,block_n", [(g.GEMM_KERNEL_SKINNY, 0, 0),
                                                    (g.GEMM_KERNEL_SKINNY, 7, 0),
-                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 128),
-                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 192),
-                                                   (g.GEMM_KERNEL_SKINNY_PAIR, 0, 256)])
+                                                   (g.GEMM_KERNEL_SPLIT_PAIR, 0, 128),
+                                                   (g.GEMM_KERNEL_SPLIT_PAIR, 0, 192),
+                                                   (g.GEMM_KERNEL_SPLIT_PAIR, 0, 256)])
 def test_skinny_weight_layout(plan, op_b, kernel, shares, block_n):
     """M <= 64 with B stored N x K (the weight layout): swap-AB reads it K-major,
     the cluster kernel as a K-major MMA B operand."""
@@ -120,7 +120,8 @@ def test_skinny_weight_layout(plan, op_b, kernel, shares, block_n):
                                           (g.GEMM_KERNEL_TMA, (300, 256, 264)),
                                           (g.GEMM_KERNEL_GENERIC, (130, 96, 72)),
                                           (g.GEMM_KERNEL_SKINNY, (16, 1024, 1000)),
-                                          (g.GEMM_KERNEL_SKINNY_PAIR, (16, 1024, 1000))])
+                                          (g.GEMM_KERNEL_SPLIT_PAIR, (16, 1024, 1000)),
+                                          (g.GEMM_KERNEL_SPLIT_PAIR, (300, 1024, 520))])
 def test_16bit_outputs(plan, out, kernel, shape):
     M, K, N = shape
     A, B = workloads.custom(M, K, N, "bf16", seed=M + out, dist="normal")
