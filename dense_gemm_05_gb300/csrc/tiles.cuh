@@ -164,9 +164,15 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
                                                 uint32_t warp_buf, uint32_t& seq, int lane,
                                                 int row0, int col, const uint32_t (&lo)[32],
                                                 const uint32_t (&hi)[32]) {
+    // A chunk wholly outside C (rows from row0 or columns from col beyond M or N)
+    // is skipped without touching a buffer: the two buffers then alternate over
+    // the stores actually issued, so the wait below always covers the store that
+    // last read the buffer about to be rewritten.  (row0 and col are the same on
+    // every lane.)
+    if (row0 >= p.M || col >= p.N) return;
     const uint32_t buf = warp_buf + (seq & 1u) * static_cast<uint32_t>(kEpiBufBytes);
     ++seq;
-    // The store that last read this buffer (two chunks ago) must have read it.
+    // The store that last read this buffer (two stores ago) must have read it.
     if (p.c_tma && lane == 0) bulk_wait_group_read1();
     __syncwarp();
     const uint32_t row = buf + static_cast<uint32_t>(lane * 128);
@@ -191,7 +197,7 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
     if (p.c_tma) {
         fence_proxy_async_smem();              // generic stores -> visible to the TMA engine
         __syncwarp();
-        if (lane == 0 && row0 < p.M && col < p.N) {
+        if (lane == 0) {
             tma_store_2d(mapC, buf, col, row0);
             bulk_commit_group();
         }
@@ -230,6 +236,25 @@ __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorM
                                              int lane, int row0, int col0, Release release) {
     const int cw = epi_chunk_cols(p.c_type);
     const int nchunks = BN / cw;
+    if (cw == 32) {
+        // fp32 C: two chunks' TMEM loads in flight before one wait, so the load
+        // latency is paid once per 64 columns.  (The destination registers of a
+        // tcgen05.ld are undefined until tcgen05.wait::ld, so a load must not be
+        // left in flight across other code: the compiler may move or spill them.)
+        static_assert(BN % 64 == 0, "chunk pairs");
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 32; ch += 2) {
+            uint32_t a[32], b[32], none[32];
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>(ch * 32), a);
+            tmem_ld_32x32b_x32(taddr + static_cast<uint32_t>((ch + 1) * 32), b);
+            tmem_ld_wait(a);
+            tmem_ld_wait(b);
+            if (ch + 2 == BN / 32) release();
+            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * 32, a, none);
+            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + (ch + 1) * 32, b, none);
+        }
+        return;
+    }
 #pragma unroll 1
     for (int ch = 0; ch < nchunks; ++ch) {
         uint32_t lo[32], hi[32];
