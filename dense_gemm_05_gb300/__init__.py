@@ -53,7 +53,8 @@ KERNEL_NAMES = {0: "none", 1: "zero_fill", 2: "tma", 3: "generic", 4: "skinny", 
 ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_status_string",
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
-                 "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query")
+                 "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
+                 "gemm_plan_create_model")
 
 SOFTMAX_PATH_NONE = 0
 SOFTMAX_PATH_WARP = 1
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
         vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
         L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int]
         L.gemm_plan_create.restype = i32
+        L.gemm_plan_create_model.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32]
+        L.gemm_plan_create_model.restype = i32
         L.gemm_run.argtypes = [vp, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, vp]
         L.gemm_run.restype = i32
         L.gemm_plan_destroy.argtypes = [vp]
@@ -173,6 +176,18 @@ def gemm_plan_create(device: int = 0) -> int:
     st = lib().gemm_plan_create(ctypes.byref(h), int(device))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_plan_create")
+    return h.value
+
+
+def gemm_plan_create_model(num_sms: int = 152, pair_clusters_128: int = 76,
+                           pair_clusters_256: int = 76, splitpair_clusters: int = 76) -> int:
+    """A plan for a modelled device (no GPU needed), for gemm_query/gemm_query_ex only;
+    the defaults are what a GB300 reports."""
+    h = ctypes.c_void_p()
+    st = lib().gemm_plan_create_model(ctypes.byref(h), int(num_sms), int(pair_clusters_128),
+                                      int(pair_clusters_256), int(splitpair_clusters))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan_create_model")
     return h.value
 
 

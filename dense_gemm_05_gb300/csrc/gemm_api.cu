@@ -48,6 +48,7 @@ struct gemm_plan_s {
     int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
     int splitpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
     bool debug_sync = false;
+    bool model = false;              // a device model for gemm_query only (no device, no memory)
     uint64_t timeout_ns = 2000000000ull;
 };
 
@@ -288,7 +289,7 @@ struct Staging {
 bool plan_staging(const gemm_plan_s* plan, const Args& a, Staging* st, Args* out) {
     *out = a;
     *st = Staging{};
-    if (plan->force_kernel == GEMM_KERNEL_GENERIC || plan->stage == nullptr || a.M == 0 ||
+    if (plan->force_kernel == GEMM_KERNEL_GENERIC || plan->stage_bytes == 0 || a.M == 0 ||
         a.N == 0 || a.K == 0)
         return false;
     const bool a_bad = !tma_ok(a.A, a.lda);
@@ -662,8 +663,34 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_create_model(gemm_plan_t* out, int32_t num_sms, int32_t pair_clusters_128,
+                                     int32_t pair_clusters_256, int32_t splitpair_clusters) {
+    if (out == nullptr) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_sms < 1 || num_sms > 4096) return GEMM_ERR_INVALID_ARG;
+    for (int c : {pair_clusters_128, pair_clusters_256, splitpair_clusters})
+        if (c < 0 || 2 * c > num_sms) return GEMM_ERR_INVALID_ARG;
+    gemm_plan_s* p = new (std::nothrow) gemm_plan_s();
+    if (p == nullptr) return GEMM_ERR_OOM;
+    p->model = true;
+    p->device = -1;
+    p->num_sms = num_sms;
+    p->pair_clusters[0] = pair_clusters_128;
+    p->pair_clusters[1] = pair_clusters_256;
+    p->splitpair_clusters = splitpair_clusters;
+    p->ws_bytes = kWorkspaceBytes;       // what a device plan holds, so the choices match
+    p->stage_bytes = kStageBytes;
+    p->counters_len = kMaxCounters;
+    *out = p;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     if (plan == nullptr) return GEMM_OK;
+    if (plan->model) {
+        delete plan;
+        return GEMM_OK;
+    }
     DeviceGuard guard(plan->device);
     cudaFree(plan->ws);
     cudaFree(plan->counters);
@@ -743,7 +770,7 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
 }
 
 gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) {
-    if (plan == nullptr) return GEMM_ERR_INVALID_ARG;
+    if (plan == nullptr || plan->model) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_args(a_in);
     if (st != GEMM_OK) return st;
     Args a;

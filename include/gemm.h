@@ -173,6 +173,24 @@ GEMM_API gemm_status_t gemm_query_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t
                                      int64_t M, int64_t N, int64_t K,
                                      gemm_dtype_t dtype, gemm_config_t *out);
 
+/*
+ * A plan for a modelled device, for gemm_query / gemm_query_ex only: the kernel
+ * and configuration choice of a device with `num_sms` SMs and the given numbers
+ * of co-resident 2-CTA clusters for the pair kernel (128- and 256-column tiles)
+ * and the split-pair kernel (a GB300 reports 152, 76, 76, 76), with the
+ * workspace, staging and counter capacities of a device plan.  Touches no
+ * device and allocates no device memory, so the planner can be examined on a
+ * host without a GPU; the query's pointer arguments are only checked for
+ * alignment and overlap.  gemm_run / gemm_run_ex on it return INVALID_ARG;
+ * gemm_plan_force and gemm_plan_set_group apply as to a device plan.
+ * Errors: INVALID_ARG (null out, num_sms outside 1..4096, a cluster count
+ * negative or above num_sms / 2), OOM.
+ */
+GEMM_API gemm_status_t gemm_plan_create_model(gemm_plan_t *out, int32_t num_sms,
+                                              int32_t pair_clusters_128,
+                                              int32_t pair_clusters_256,
+                                              int32_t splitpair_clusters);
+
 /* Release the plan and its workspace.  NULL-safe.  Waits for nothing: the
  * caller must make sure no gemm_run using the plan is still in flight. */
 GEMM_API gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
