@@ -192,7 +192,7 @@ def test_split_pair_shapes(plan, M, K, N, dtype, block_n):
     got2 = run(plan, A, B, M, N, K, kernel=kernel, block_n=block_n)
     assert_guards(got1, M, N)
     assert np.array_equal(got1, got2), "result changed between runs"
-    assert_close(got1[:M, :N], A, B, M, N, K, f"skinny pair {M}x{N}x{K} bn={block_n}")
+    assert_close(got1[:M, :N], A, B, M, N, K, f"split pair {M}x{N}x{K} bn={block_n}")
 
 
 def test_split_pair_query(plan):
