@@ -228,6 +228,43 @@ def test_split_pair_query(plan):
     assert plan.query(a, b, c, 16, 14336, 512)["kernel"] == g.GEMM_KERNEL_SKINNY   # 8 K blocks
 
 
+def test_dependent_launches_read_the_previous_output(plan):
+    """Kernels are launched as programmatic dependents: each may start while the
+    previous one drains and must wait before reading its output.  A chain on one
+    stream, each GEMM reading the C of the one before (exact integer values, so
+    any stale or partial read shows): C1 = A B1 (bf16 out, pair tiles), then
+    C1 I (pair tiles), C1[:16] I (stream-K swap-AB, M = 16), C1[:300] I[:, :1024]
+    (split pair with 128-row tiles), each into a NaN-filled buffer."""
+    dev = torch.device("cuda:0")
+    gen = torch.Generator().manual_seed(17)
+    M, K, N = 4096, 256, 4096
+    A = torch.randint(-1, 2, (M, K), generator=gen).to(torch.bfloat16)
+    B1 = torch.randint(-1, 2, (K, N), generator=gen).to(torch.bfloat16)
+    a, b1 = A.to(dev), B1.to(dev)
+    eye = torch.eye(N, dtype=torch.bfloat16, device=dev)
+    c1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    c2 = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    c3 = torch.full((16, N), float("nan"), dtype=torch.float32, device=dev)
+    c4 = torch.full((300, N), float("nan"), dtype=torch.float32, device=dev)
+    assert plan.query_ex(a, b1, c1)["kernel"] == g.GEMM_KERNEL_PAIR
+    assert plan.query_ex(c1, eye, c2)["kernel"] == g.GEMM_KERNEL_PAIR
+    assert plan.query_ex(c1[:16], eye, c3)["kernel"] == g.GEMM_KERNEL_SKINNY
+    assert plan.query_ex(c1[:300], eye[:, :1024], c4[:, :1024])["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR
+    for _ in range(3):
+        for t in (c1, c2, c3, c4):
+            t.fill_(float("nan"))
+        plan.run_ex(a, b1, c1)
+        plan.run_ex(c1, eye, c2)
+        plan.run_ex(c1[:16], eye, c3)
+        plan.run_ex(c1[:300], eye[:, :1024], c4[:, :1024])
+        torch.cuda.synchronize()
+        ref = torch.from_numpy(oracle.gemm(A, B1))          # |entries| <= 256: exact in bf16
+        assert torch.equal(c1.cpu().double(), ref)
+        assert torch.equal(c2.cpu(), c1.float().cpu())
+        assert torch.equal(c3.cpu(), c1[:16].float().cpu())
+        assert torch.equal(c4[:, :1024].cpu(), c1[:300, :1024].float().cpu())
+
+
 def _sample_entries(M, N, bm, bn, n_random, seed):
     """n_random uniform entries plus, for every tile on the border of C, its four
     corners and 16 random entries."""
