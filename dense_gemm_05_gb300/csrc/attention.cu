@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/attention.h"
+#include "common.cuh"
 #include "ptx.cuh"
 #include "tiles.cuh"
 
@@ -169,6 +170,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     __syncthreads();
     dg::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    dg::griddep_wait();              // Q, K, V may be written, O still read, by the previous grid
+    dg::griddep_launch_dependents();
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -671,8 +674,12 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
     p.timeout_ns = kTimeoutNs;
     const dim3 grid(static_cast<unsigned>(p.npairs), static_cast<unsigned>(BH));
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    kernel<<<grid, threads, smem_bytes, s>>>(mq, mk, mv, p);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    // Launched as a programmatic dependent (the kernel waits before touching memory).
+    if (dg::launch_pdl(kernel, grid, dim3(threads), size_t(smem_bytes), s, mq, mk, mv, p) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     if (debug_sync()) {
         if (cudaStreamSynchronize(s) != cudaSuccess) {
             (void)cudaGetLastError();

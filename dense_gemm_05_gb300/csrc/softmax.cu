@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/softmax.h"
+#include "common.cuh"
 #include "ptx.cuh"
 
 namespace {
@@ -134,6 +135,8 @@ __global__ void __launch_bounds__(TPR == 32 ? kWarpRowsBlock : TPR)
     __shared__ float red[32];
     const int t = threadIdx.x % TPR;
     const int g = threadIdx.x / TPR;
+    dg::griddep_wait();              // X may be written, Y still read, by the previous grid
+    dg::griddep_launch_dependents();
     for (int64_t r = int64_t(blockIdx.x) * kRows + g; r < M; r += int64_t(gridDim.x) * kRows) {
         const float* xr = X + r * ldx;
         float* yr = Y + r * ldy;
@@ -205,6 +208,8 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
         dg::fence_mbar_init();
     }
     __syncthreads();
+    dg::griddep_wait();              // X may be written, Y still read, by the previous grid
+    dg::griddep_launch_dependents();
 
     if (warp == NW) {
         // ------------------------------------------------------------ producer
@@ -339,6 +344,8 @@ __global__ void __launch_bounds__(kStreamThreads)
     constexpr int64_t kStep = int64_t(kStreamThreads) * kStreamSlab;
     __shared__ float red[32];
     const int t = threadIdx.x;
+    dg::griddep_wait();              // X may be written, Y still read, by the previous grid
+    dg::griddep_launch_dependents();
     for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
         const float* xr = X + r * ldx;
         float* yr = Y + r * ldy;
@@ -591,12 +598,18 @@ gemm_status_t softmax_rows(const float* X, int64_t ldx, float* Y, int64_t ldy, i
     const gemm_status_t st = plan(X, ldx, Y, ldy, M, N, &c);
     if (st != GEMM_OK || c.cfg.path == SOFTMAX_PATH_NONE) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (c.sfn != nullptr)
-        c.sfn<<<c.cfg.grid, c.cfg.block, c.smem, s>>>(X, ldx, Y, ldy, M, N, c.cfg.slots,
-                                                      c.slot_bytes, c.cfg.vec == 4, kTimeoutNs);
-    else
-        c.fn<<<c.cfg.grid, c.cfg.block, 0, s>>>(X, ldx, Y, ldy, M, N);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    // Launched as programmatic dependents (the kernels wait before touching memory).
+    const cudaError_t e =
+        c.sfn != nullptr
+            ? dg::launch_pdl(c.sfn, dim3(c.cfg.grid), dim3(c.cfg.block), size_t(c.smem), s, X, ldx,
+                             Y, ldy, M, N, int(c.cfg.slots), int(c.slot_bytes),
+                             int(c.cfg.vec == 4), kTimeoutNs)
+            : dg::launch_pdl(c.fn, dim3(c.cfg.grid), dim3(c.cfg.block), size_t(0), s, X, ldx, Y,
+                             ldy, M, N);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     if (debug_sync() && c.sfn != nullptr) {
         if (cudaStreamSynchronize(s) != cudaSuccess) {
             (void)cudaGetLastError();
