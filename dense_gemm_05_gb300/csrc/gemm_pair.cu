@@ -39,12 +39,13 @@ struct PairCfg {
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-// The work of one cluster, in order: first its stream-K share of the tiles
+// The work of one cluster, in order: its stream-K share of the tiles
 // [0, sk_tiles) -- one contiguous run of the (tile, K block) iterations of
-// those tiles, cut into per-tile segments -- then the whole tiles
-// sk_tiles + cid, sk_tiles + cid + clusters, ...  Doing the split tiles first
-// lets their fix-ups (run by the epilogue warps) overlap the MMAs of the
-// whole tiles that follow.
+// those tiles, cut into per-tile segments -- and the whole tiles
+// sk_tiles + cid, sk_tiles + cid + clusters, ...; the share comes first, or
+// after the first whole tile when the cluster has at least two.  Keeping the
+// split tiles before most whole tiles lets their fix-ups (run by the epilogue
+// warps) overlap the MMAs of the whole tiles that follow.
 struct PairSeg {
     int tile;
     int kb0, kb1;     // K blocks [kb0, kb1) of the tile
@@ -53,11 +54,17 @@ struct PairSeg {
 
 struct PairWalker {
     int num_kb, ncl, total, next_dp, share;
+    bool dp_first;       // one whole tile still to be walked before the stream-K share
     int64_t t_sk, g, it, end;
 
     __device__ PairWalker(const Params& p, int cid, int nclusters)
         : num_kb(p.num_kb), ncl(nclusters), total(p.tiles_m * p.tiles_n), share(cid) {
         const int sk = p.shares > 0 ? p.sk_tiles : 0;
+        // With at least two whole tiles per cluster, the first whole tile runs
+        // before the stream-K share: the share then reads operands the first
+        // wave has brought into L2 (a cold share streamed at about 0.5 us per K
+        // block against 0.3), and its fix-up still overlaps later whole tiles.
+        dp_first = sk > 0 && total - sk >= 2 * nclusters;
         t_sk = int64_t(sk) * num_kb;
         g = p.shares;
         if (sk > 0 && cid < g) {
@@ -69,6 +76,17 @@ struct PairWalker {
         next_dp = sk + cid;
     }
     __device__ bool next(PairSeg& s) {
+        if (dp_first) {
+            dp_first = false;
+            if (next_dp < total) {
+                s.tile = next_dp;
+                s.kb0 = 0;
+                s.kb1 = num_kb;
+                s.share = -1;
+                next_dp += ncl;
+                return true;
+            }
+        }
         if (it < end) {
             s.tile = static_cast<int>(it / num_kb);
             s.kb0 = static_cast<int>(it - int64_t(s.tile) * num_kb);
