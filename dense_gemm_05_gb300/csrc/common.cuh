@@ -33,6 +33,7 @@ struct Params {
     int32_t a_vec, b_vec;   // generic producer: 16-byte vector loads are legal
     int32_t c_vec;          // 16-byte vector stores of C are legal
     int32_t c_tma;          // the epilogue writes C with TMA stores (mapC is valid)
+    int32_t prefetch_kb;    // split pair, skinny: K blocks per CTA warmed in L2 before the grid wait
     float* ws;              // skinny: split-K partial sums
     int* counters;          // skinny: per-tile arrival counters (zero between launches)
     int* status;            // device error word (kDevTimeout on a wait that gave up)

@@ -59,6 +59,8 @@ constexpr int64_t kPairMinShareKb = 16;   // a pair stream-K share streams at le
 constexpr size_t kStageBytes = size_t(32) << 20;       // staging copies of misaligned operands
 constexpr int kPairMinSkKb = 32;          // K blocks per tile below which no pair stream-K phase
 constexpr int kSplitPairMinKb = 12;       // K blocks below which M > 64 keeps one-CTA tiles
+constexpr int kL2PrefetchKb = 6;          // split pair, one tile row: K blocks per CTA warmed in L2 early
+constexpr int kL2PrefetchKbSkinny = 3;    // the same for the swap-AB stream-K kernel (deeper was slower)
 
 // Kernel choice: flop/s each SM sustains on one tile of each kind, measured on
 // GB300 with one wave of tiles (bf16, K = 8192): pair tiles 256 x 256 (two
@@ -885,6 +887,12 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             if (!map_a(&ma, static_cast<uint32_t>(c.ms)) ||
                 !map_b(&mb, static_cast<uint32_t>(c.bn)))
                 return GEMM_ERR_CUDA;
+            // With one row of tiles every CTA streams its own B strip once from
+            // DRAM: its first K blocks are prefetched into L2 before the wait on
+            // the previous grid (not after a staging copy, which is still writing
+            // them).  With several tile rows B is shared through L2 and the early
+            // reads only compete (measured slower at 1024 x 1024 x 8192).
+            p.prefetch_kb = (!staged && c.tiles_m == 1) ? kL2PrefetchKb : 0;
             err = dg::launch_splitpair(c.ms, c.bn, b_mn, ma, mb, p,
                                     dg::idesc_f16(bf16, false, b_mn, dg::kBM, c.bn), c.grid,
                                     stream);
@@ -898,6 +906,7 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             CUtensorMap mb, ma;
             if (!map_b(&mb, 128) || !map_a(&ma, static_cast<uint32_t>(c.ms)))
                 return GEMM_ERR_CUDA;
+            p.prefetch_kb = staged ? 0 : kL2PrefetchKbSkinny;    // one tile row, as above
             err = dg::launch_skinny(c.ms, b_mn, mb, ma, p,
                                     dg::idesc_f16(bf16, b_mn, false, 128, c.ms), c.grid, stream);
         }

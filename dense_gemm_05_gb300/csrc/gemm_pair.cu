@@ -297,8 +297,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 };
                 // Sum one 64-column round of the tile in share order.  fold: this
                 // share's own partial comes straight from TMEM (it never published).
-                // Sum one 64-column round of the tile in share order.  fold: this
-                // share's own partial comes straight from TMEM (it never published).
                 auto sum_round = [&](int c0, bool fold, uint32_t (&lo)[32], uint32_t (&hi)[32]) {
                     float4 s4[16];
 #pragma unroll 1

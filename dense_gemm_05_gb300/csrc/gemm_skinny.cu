@@ -138,6 +138,18 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 5 && lane == 0) {
         prefetch_tmap(&mapA);
         prefetch_tmap(&mapB);
+        // Warm L2 with the first K blocks of this CTA's first segment while the
+        // previous grid finishes (a prefetch hands no data to this CTA).
+        SegmentWalker walk(p.tiles_n, p.num_kb, p.shares);
+        Segment sg;
+        if (p.prefetch_kb > 0 && walk.next(sg)) {
+            const uint64_t pol_stream = l2_policy_evict_first();
+            const uint64_t pol_keep = l2_policy_evict_last();
+            for (int kb = sg.kb0; kb < sg.kb1 && kb < sg.kb0 + p.prefetch_kb; ++kb) {
+                prefetch_operand_hint<B_MN>(&mapB, sg.tile * 128, kb * kBK, 128, pol_stream);
+                tma_prefetch_2d_hint(&mapA, kb * kBK, 0, pol_keep);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();

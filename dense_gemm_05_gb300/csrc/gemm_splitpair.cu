@@ -37,7 +37,10 @@
 // the remote arrive is waited for only by the epilogue, the TMEM address is
 // handed over by a named barrier), and it is launched as a programmatic
 // dependent of the previous kernel in the stream: its prologue overlaps that
-// kernel's tail and every access to global memory waits for it to finish.
+// kernel's tail and every load waits for it to finish.  Before that wait, with
+// one row of tiles, the producer prefetches its first K blocks into L2 (the
+// host sets how many in Params::prefetch_kb; graph-replayed at M = 16, N =
+// 14336: 20.8 -> 19.7 us).
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tiles.cuh"
@@ -279,6 +282,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             int armed = 0;
             const uint64_t pol_stream = l2_policy_evict_first();   // B: read once
             const uint64_t pol_keep = l2_policy_evict_last();      // A: read by every tile of its rows
+            // While the previous grid finishes, warm L2 with this CTA's first K
+            // blocks: a prefetch hands no data to this CTA, so it needs no wait,
+            // and the first loads after the wait then find their lines in L2.
+            for (int kb = kb0; kb < kb1 && kb < kb0 + p.prefetch_kb; ++kb) {
+                tma_prefetch_2d_hint(&mapA, kb * kBK, m0, pol_keep);
+                prefetch_operand_hint<B_MN>(&mapB, n0, kb * kBK, BN, pol_stream);
+            }
             griddep_wait();                   // A and B may be written by the previous grid
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns)) {

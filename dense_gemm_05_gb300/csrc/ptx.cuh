@@ -148,6 +148,18 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// 2-D tiled bulk tensor prefetch global -> L2 (no shared memory, no barrier).
+// It only warms L2, the device's point of coherence, so it may run before the
+// previous grid's writes are visible: later loads still read the current data.
+__device__ __forceinline__ void tma_prefetch_2d_hint(const CUtensorMap* map, int32_t x, int32_t y,
+                                                     uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // 3-D tiled bulk tensor load (x innermost, then y, then z), completion on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z) {

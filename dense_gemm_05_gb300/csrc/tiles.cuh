@@ -61,6 +61,18 @@ __device__ __forceinline__ void load_operand_hint(uint32_t dst, const CUtensorMa
     }
 }
 
+// The boxes of load_operand_hint, prefetched into L2 only.
+template <bool MN_MAJOR>
+__device__ __forceinline__ void prefetch_operand_hint(const CUtensorMap* map, int mn0, int k0,
+                                                      int rows, uint64_t policy) {
+    if constexpr (MN_MAJOR) {
+        for (int j = 0; j < rows / kSubN; ++j)
+            tma_prefetch_2d_hint(map, mn0 + j * kSubN, k0, policy);
+    } else {
+        tma_prefetch_2d_hint(map, k0, mn0, policy);
+    }
+}
+
 // Same for a CTA of a pair: completion is counted on `bar_cluster`, which may
 // be the peer CTA's barrier.
 template <bool MN_MAJOR>
