@@ -128,9 +128,18 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.y;
-    const int pair = p.causal ? (p.npairs - 1 - static_cast<int>(blockIdx.x))
-                              : static_cast<int>(blockIdx.x);   // heavy causal pairs first
+    // Causal: the work of a pair grows with its index, so blocks take pairs in
+    // launch order (x fastest, then y) heaviest first across all heads: the
+    // heaviest pair of every head, then the next, ...  Taking one head after
+    // another instead leaves the last heads' heavy pairs to the final wave.
+    int h = blockIdx.y;
+    int pair = blockIdx.x;
+    if (p.causal) {
+        const int64_t heads = gridDim.y;
+        const int64_t linear = blockIdx.x + static_cast<int64_t>(blockIdx.y) * gridDim.x;
+        h = static_cast<int>(linear % heads);
+        pair = p.npairs - 1 - static_cast<int>(linear / heads);
+    }
     // Key blocks each tile needs (0 for a tile beyond the sequence).
     int nkv[kTiles];
 #pragma unroll
