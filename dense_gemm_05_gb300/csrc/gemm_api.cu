@@ -250,8 +250,10 @@ constexpr int64_t kMaxShares = dg::kSkinnyMaxShares;
 
 // Skinny stream-K shares.  `shares` <= 0: dg::skinny_auto_shares; otherwise
 // exactly that many shares.  Falls back to one share per tile (no partial
-// tiles) when the workspace or counters cannot hold the partials.  Returns
-// false if even that is impossible.
+// tiles) when the workspace or counters cannot hold the partials; that
+// needs neither, so it is open to any number of tiles (the CTAs walk the
+// shares persistently).  Returns false for a forced share count that does
+// not fit.
 bool choose_shares(const gemm_plan_s* plan, Choice* c, int64_t shares) {
     const int64_t T = int64_t(c->tiles_n) * c->num_kb;
     int64_t G = shares > 0 ? shares : dg::skinny_auto_shares(c->tiles_n, c->num_kb, plan->num_sms);
@@ -261,7 +263,7 @@ bool choose_shares(const gemm_plan_s* plan, Choice* c, int64_t shares) {
     const bool aligned = (G % c->tiles_n == 0) && (G / c->tiles_n == 1);   // one share per tile
     if (!aligned &&
         (c->tiles_n > plan->counters_len || need > static_cast<int64_t>(plan->ws_bytes))) {
-        if (shares > 0 || c->tiles_n > kMaxShares) return false;
+        if (shares > 0) return false;
         G = c->tiles_n;
     }
     c->shares = static_cast<int>(G);

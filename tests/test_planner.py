@@ -160,3 +160,14 @@ def test_model_plan_runs_nothing_and_rejects_bad_facts():
     for facts in [(0, 0, 0, 0), (152, 77, 76, 76), (152, 76, -1, 76), (5000, 0, 0, 0)]:
         with pytest.raises(g.GemmError):
             g.gemm_plan_create_model(*facts)
+
+
+@pytest.mark.parametrize("N,K", [(4096 * 128 + 128, 64), (50_000_008, 64), (600_000, 512)])
+def test_small_m_many_tiles_short_k(model, N, K):
+    """M <= 64 with more 128-column tiles than the stream-K share limit and K too
+    short for the cluster kernel: one share per tile, which needs no workspace,
+    so any number of tiles is accepted."""
+    r = q(model, 16, N, K)
+    tiles = -(-N // 128)
+    assert (r["kernel"], r["tiles"], r["shares"], r["split_k"], r["grid"]) == \
+        (g.GEMM_KERNEL_SKINNY, tiles, tiles, 1, 152), r
