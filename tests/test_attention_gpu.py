@@ -179,3 +179,48 @@ def test_device_errors():
     with pytest.raises(TypeError):
         g.attention(q, q.half(), q)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- maximum sizes
+
+PERIOD = 65537   # prime: an offset that wrapped at a power of two reads a different element
+
+
+@pytest.mark.parametrize("BH,seq,d,causal", [(65535, 512, 128, True), (65535, 640, 64, False)],
+                         ids=["d128-causal", "d64"])
+def test_most_heads_past_2_31_elements(BH, seq, d, causal):
+    """BH at its limit (65535 heads, the grid's y extent), Q, K and V of 2.7e9-4.3e9
+    elements each: flat element i of each is a block value at i mod PERIOD, so every
+    head differs; sampled rows of the first, middle and last heads against the oracle."""
+    gen = torch.Generator().manual_seed(71)
+    blks = [torch.randn(PERIOD, generator=gen).to(torch.bfloat16) for _ in range(3)]
+    dev = torch.device("cuda:0")
+    n = BH * seq * d
+    q, k, v = (b.to(dev).repeat(-(-n // PERIOD))[:n].view(BH, seq, d) for b in blks)
+    out = g.attention(q, k, v, causal=causal)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out).all())
+    rng = np.random.default_rng(72)
+    idx = np.arange(seq * d)
+    for h in (0, BH // 2, BH - 1):
+        head = [b[torch.from_numpy((h * seq * d + idx) % PERIOD)].view(1, seq, d) for b in blks]
+        rows = np.unique(np.concatenate([[0, 1, 127, 128, seq - 1], rng.integers(0, seq, 8)]))
+        got = out[h, torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        assert_attn_close(got, *head, causal, 0, rows, torch.float32, f"{BH} heads, head {h}")
+    del q, k, v, out
+    torch.cuda.empty_cache()
+
+
+def test_longest_sequence_sampled():
+    """seq = 2^20 + 3 (ragged), causal, d = 64: 8193 key blocks for the last queries."""
+    Q, K, V = workloads.custom_qkv(1, (1 << 20) + 3, 64, "bf16", seed=81)
+    dev = torch.device("cuda:0")
+    out = g.attention(Q.to(dev), K.to(dev), V.to(dev), causal=True)
+    torch.cuda.synchronize()
+    seq = Q.shape[1]
+    rng = np.random.default_rng(82)
+    rows = np.unique(np.concatenate([[0, 1, 1 << 20, seq - 2, seq - 1], rng.integers(0, seq, 8)]))
+    got = out[0, torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+    assert_attn_close(got, Q, K, V, True, 0, rows, torch.float32, "seq 2^20 + 3")
+    del out
+    torch.cuda.empty_cache()

@@ -184,3 +184,48 @@ def test_device_errors():
     with pytest.raises(TypeError):
         g.softmax(x.double())
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- maximum sizes
+
+PERIOD = 65537   # prime: an offset that wrapped at a power of two reads a different element
+
+
+def _periodic_rows(M, N, seed):
+    """X (on the GPU, M x N contiguous) whose flat element i is blk[i mod PERIOD],
+    blk drawn N(0, 1) in float32; returns (blk as numpy, X)."""
+    gen = torch.Generator().manual_seed(seed)
+    blk = torch.randn(PERIOD, generator=gen)
+    x = blk.cuda().repeat(-(-(M * N) // PERIOD))[: M * N].view(M, N)
+    return blk.numpy(), x
+
+
+def _row_of(blk, N, r):
+    start = (r * N) % PERIOD
+    return np.tile(np.roll(blk, -start), -(-N // PERIOD) + 1)[:N]
+
+
+@pytest.mark.parametrize("M,N", [(2_200_007, 1000), (65_600, 32_768), (17, (1 << 27) + 5)],
+                         ids=["warp-path", "cta-path", "two-pass-path"])
+def test_inputs_beyond_2_31_elements(M, N):
+    """More than 2^31 elements in X and Y (8.6-9.1 GB each), one case per path:
+    sampled rows (first, last, the first row past element 2^31, random) against
+    the oracle, and every row's sum near 1."""
+    blk, x = _periodic_rows(M, N, seed=61)
+    y = g.softmax(x)
+    torch.cuda.synchronize()
+    cfg = g.softmax_rows_query(x.data_ptr(), N, y.data_ptr(), N, M, N)
+    rng = np.random.default_rng(62)
+    first = -(-(1 << 31) // N)
+    assert first < M
+    extra = rng.integers(0, M, 12 if N < (1 << 20) else 0)
+    rows = np.unique(np.concatenate([[0, M - 1, first], extra])).astype(np.int64)
+    for r in rows:
+        got = y[int(r)].double().cpu().numpy()[None, :]
+        assert_softmax_close(got, _row_of(blk, N, int(r))[None, :], N, cfg, f"{M} x {N} row {r}")
+    spread = float(blk.max() - blk.min())         # bounds |x - m| and its weighted mean
+    bound = (4 * spread + chain_bound(cfg, N) + 12) * U
+    sums = y.sum(dim=1, dtype=torch.float64).cpu().numpy()
+    assert np.all(np.abs(sums - 1.0) <= bound), np.abs(sums - 1.0).max()
+    del x, y
+    torch.cuda.empty_cache()
