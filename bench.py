@@ -384,7 +384,15 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
                    "median_ms": t * 1e3, "l2": "flushed before each launch",
                    "kernel": cfg["kernel_name"], "block_n": cfg["block_n"],
                    "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst"}
-    del a, b, c, flush
+    # Context only (not on the measured path): cuBLAS through torch.matmul on the same
+    # inputs and flush.  torch gives bf16 output for bf16 inputs (half our C bytes).
+    cb = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    ref_call = lambda: torch.matmul(a, b, out=cb)  # noqa: E731
+    time_launches(torch, None, [ref_call] * 5, stream)
+    tms = sorted(time_launches(torch, None, [ref_call] * 30, stream, between=lambda: flush.zero_()))
+    out[w.name]["torch_matmul_tflops"] = w.flops / (tms[len(tms) // 2] / 1e3) / 1e12
+    out[w.name]["torch_matmul"] = "cuBLAS via torch.matmul, bf16 output, same flush; context"
+    del a, b, c, cb, flush
     # M=16 skinny: B copies rotated so that the working set exceeds L2 several times.
     w = workloads.WORKLOADS["skinny16x4096x14336_bf16"]
     A, B = workloads.make_inputs(w)
@@ -436,7 +444,30 @@ def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
                    "shares": cfg["shares"], "host_us_per_call": host_us,
                    "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                    "bytes_alg": w.bytes_alg}
-    del a, bs, c
+    # Context only: cuBLAS through torch.matmul (bf16 output), the same rotation and
+    # graph replay; GB/s over the same algorithmic bytes.
+    cb = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(stream):
+        for bb in bs:
+            torch.matmul(a, bb, out=cb)
+    torch.cuda.synchronize()
+    rgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(rgraph):
+        for i in range(per_graph):
+            torch.matmul(a, bs[i % copies], out=cb)
+    rgraph.replay()
+    torch.cuda.synchronize()
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for e0, e1 in rev:
+        e0.record()
+        rgraph.replay()
+        e1.record()
+    torch.cuda.synchronize()
+    rms = sorted(e0.elapsed_time(e1) / per_graph for e0, e1 in rev)
+    out[w.name]["torch_matmul_gbs"] = w.bytes_alg / (rms[len(rms) // 2] / 1e3) / 1e9
+    out[w.name]["torch_matmul"] = "cuBLAS via torch.matmul, bf16 output, same rotation; context"
+    del a, bs, c, cb, rgraph
     out.update(small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src))
     out.update(softmax_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
     out.update(attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src))
