@@ -54,7 +54,7 @@ ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_stat
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
                  "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
-                 "gemm_plan_create_model")
+                 "gemm_plan_create_model", "gemm_noop_launch")
 
 SOFTMAX_PATH_NONE = 0
 SOFTMAX_PATH_WARP = 1
@@ -65,7 +65,7 @@ SOFTMAX_PATH_NAMES = {0: "none", 1: "warp", 2: "cta", 3: "stream"}
 #: Limits of gemm_run_noalloc (mirrors of the header's macros).
 GEMM_NOALLOC_MAX_M = 64
 GEMM_NOALLOC_MAX_N = 131072
-GEMM_NOALLOC_SCRATCH_BYTES = 8392704
+GEMM_NOALLOC_SCRATCH_BYTES = 8392960
 
 
 class GemmError(RuntimeError):
@@ -142,6 +142,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_tile_coord.restype = i32
         L.gemm_wait_selftest.argtypes = [u32, vp]
         L.gemm_wait_selftest.restype = i32
+        L.gemm_noop_launch.argtypes = [i32, i32, vp]
+        L.gemm_noop_launch.restype = i32
         L.gemm_run_noalloc.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, vp]
         L.gemm_run_noalloc.restype = i32
         L.gemm_run_ex.argtypes = [vp, i32, i32, vp, i64, vp, i64, vp, i64, i32, i64, i64, i64,
@@ -245,6 +247,11 @@ def gemm_tile_coord(t: int, tiles_m: int, tiles_n: int, group: int) -> tuple[int
 
 def gemm_wait_selftest(timeout_us: int, stream: int = 0) -> int:
     return int(lib().gemm_wait_selftest(timeout_us, stream))
+
+
+def gemm_noop_launch(grid: int, cluster: int = 1, stream: int = 0) -> int:
+    """Enqueue one kernel with no work, launched like the GEMM kernels (the launch floor)."""
+    return int(lib().gemm_noop_launch(grid, cluster, stream))
 
 
 def gemm_run_noalloc(A: int, lda: int, B: int, ldb: int, C: int, ldc: int, M: int, N: int,

@@ -212,4 +212,8 @@ cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, i
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);
 
+// A kernel with no work, launched like the GEMM kernels (grid, cluster of 1 or 2,
+// programmatic dependent launch): the launch floor.
+cudaError_t launch_noop(int grid, int cluster, cudaStream_t stream);
+
 }  // namespace dg

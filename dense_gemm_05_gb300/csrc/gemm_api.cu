@@ -583,6 +583,31 @@ cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t str
     return cudaGetLastError();
 }
 
+// No work: the dependency wait and the early release of the next kernel, as
+// every GEMM kernel does them.
+__global__ void __launch_bounds__(192) noop_kernel() {
+    griddep_wait();
+    griddep_launch_dependents();
+}
+
+cudaError_t launch_noop(int grid, int cluster, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, noop_kernel);
+}
+
 }  // namespace dg
 
 extern "C" {
@@ -998,6 +1023,17 @@ gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st* stream
     }
     cudaFree(d);
     return st;
+}
+
+gemm_status_t gemm_noop_launch(int32_t grid, int32_t cluster, struct CUstream_st* stream_handle) {
+    if (grid < 1 || grid > 65535 || (cluster != 1 && cluster != 2) || grid % cluster != 0)
+        return GEMM_ERR_INVALID_ARG;
+    if (dg::launch_noop(grid, cluster, reinterpret_cast<cudaStream_t>(stream_handle)) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
 }
 
 }  // extern "C"

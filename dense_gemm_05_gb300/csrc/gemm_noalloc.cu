@@ -10,6 +10,7 @@
 // kernel needs -- fp32 partial tiles and per-tile arrival counters -- in one
 // fixed array of static device memory that every GPU which loads the library
 // holds until the process exits.  The caller still passes A, B and C.
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -23,27 +24,35 @@
 
 namespace {
 
-constexpr int64_t kScratchWsBytes = int64_t(GEMM_NOALLOC_SCRATCH_BYTES) - 4096;
+// Layout of the scratch array: fp32 partial tiles, then (256 bytes further on)
+// the device status word, then the per-tile arrival counters right behind it,
+// so that one memset clears the status word and the counters a call uses.
+constexpr int64_t kScratchWsBytes = int64_t(8) << 20;
+constexpr int64_t kStatusOffset = kScratchWsBytes;
+constexpr int64_t kCountersOffset = kStatusOffset + 16;
 constexpr int kScratchCounters = 1024;   // one per 128-column tile of C
 static_assert(int64_t(kScratchCounters) * 128 == GEMM_NOALLOC_MAX_N, "counter capacity");
-static_assert(kScratchCounters * 4 <= 4096, "counters fit the reserved tail");
+static_assert(kCountersOffset + kScratchCounters * 4 <= GEMM_NOALLOC_SCRATCH_BYTES, "layout");
 
 }  // namespace
 
-// The scratch array: partial tiles in the first kScratchWsBytes, then the counters.
-// In host code this name is only a stand-in; its device address comes from
-// cudaGetSymbolAddress below.
+// The scratch array.  In host code this name is only a stand-in; its device
+// address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GEMM_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Per-device set-up.  A set-up that failed is not remembered: the next call
+// on that device tries again (the failure may have been a transient lack of
+// device memory for the array or the kernels' code).
 struct DeviceState {
-    std::once_flag once;
-    gemm_status_t status = GEMM_ERR_CUDA;
+    std::mutex mu;
+    std::atomic<bool> ready{false};
     unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
     int num_sms = 0;
+    bool debug_sync = false;
 };
 
 DeviceState g_state[kMaxDevices];
@@ -55,35 +64,37 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn g_encode = nullptr;
 std::once_flag g_encode_once;
 
-// Set-up for the current device, once: architecture check, kernel attributes,
-// and the device address of the scratch array.
-void setup_device(DeviceState* s, int dev) {
+// Set-up for the current device: architecture check, kernel attributes (which
+// also loads the kernels onto the device), and the device address of the
+// scratch array (which loads the array).  Done under the device's lock until it
+// succeeds once; afterwards the fast path only reads `ready`.
+gemm_status_t setup_device(DeviceState* s, int dev) {
+    if (s->ready.load(std::memory_order_acquire)) return GEMM_OK;
+    std::lock_guard<std::mutex> lock(s->mu);
+    if (s->ready.load(std::memory_order_relaxed)) return GEMM_OK;
     int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
-        s->status = GEMM_ERR_CUDA;
-        return;
+        return GEMM_ERR_CUDA;
     }
-    if (major != 10 || minor != 3) {
-        s->status = GEMM_ERR_UNSUPPORTED;
-        return;
-    }
+    if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED;
     if (dg::skinny_prepare() != cudaSuccess) {
         (void)cudaGetLastError();
-        s->status = GEMM_ERR_CUDA;
-        return;
+        return GEMM_ERR_CUDA;
     }
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
         (void)cudaGetLastError();
-        s->status = GEMM_ERR_CUDA;
-        return;
+        return GEMM_ERR_CUDA;
     }
     s->scratch = static_cast<unsigned char*>(ptr);
     s->num_sms = sms;
-    s->status = GEMM_OK;
+    const char* v = std::getenv("GEMM_DEBUG_SYNC");
+    s->debug_sync = v != nullptr && v[0] != '\0' && v[0] != '0';
+    s->ready.store(true, std::memory_order_release);
+    return GEMM_OK;
 }
 
 bool encode_2d(CUtensorMap* map, gemm_dtype_t dt, const void* ptr, int64_t inner, int64_t outer,
@@ -132,7 +143,20 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     if (dtype != GEMM_F16 && dtype != GEMM_BF16) return GEMM_ERR_UNSUPPORTED;
     if (M > GEMM_NOALLOC_MAX_M || N > GEMM_NOALLOC_MAX_N || K > INT32_MAX - 1024)
         return GEMM_ERR_UNSUPPORTED;
+
+    // The device set-up comes first, so that a call with M == 0 or N == 0 (which
+    // launches nothing) can be used to do it at a time of the caller's choosing.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    DeviceState* s = &g_state[dev];
+    const gemm_status_t ready = setup_device(s, dev);
+    if (ready != GEMM_OK) return ready;
     if (M == 0 || N == 0) return GEMM_OK;
+
     if (C == nullptr || ldc < N || ldc > (int64_t(1) << 40) ||
         reinterpret_cast<uintptr_t>(C) % 4u != 0u)
         return GEMM_ERR_INVALID_ARG;
@@ -158,16 +182,6 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     // The kernel stages A and B with TMA: 16-byte aligned bases and pitches.
     if (!aligned16(A, lda) || !aligned16(B, ldb)) return GEMM_ERR_UNSUPPORTED;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
-    DeviceState* s = &g_state[dev];
-    std::call_once(s->once, setup_device, s, dev);
-    if (s->status != GEMM_OK) return s->status;
-
     // Stream-K shares as gemm_run chooses them; if their partial tiles would not
     // fit the scratch, one share per tile (no partials).
     const int ms = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
@@ -180,9 +194,13 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
             kScratchWsBytes)
         shares = tiles_n;
     const int max_slots = dg::shares_per_tile_bound(T, shares, num_kb);
-    int* counters = reinterpret_cast<int*>(s->scratch + kScratchWsBytes);
-    // The array keeps whatever the previous call left: the counters must start at zero.
-    if (cudaMemsetAsync(counters, 0, sizeof(int) * tiles_n, stream) != cudaSuccess) {
+    int* status = reinterpret_cast<int*>(s->scratch + kStatusOffset);
+    int* counters = reinterpret_cast<int*>(s->scratch + kCountersOffset);
+    // The array keeps whatever the previous call left: the status word and the
+    // counters this call uses must start at zero.
+    if (cudaMemsetAsync(status, 0, static_cast<size_t>(kCountersOffset - kStatusOffset) +
+                                       sizeof(int) * static_cast<size_t>(tiles_n),
+                        stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -213,7 +231,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.c_vec = 0;
     p.ws = reinterpret_cast<float*>(s->scratch);
     p.counters = counters;
-    p.status = nullptr;
+    p.status = status;
     p.timeout_ns = 2000000000ull;
     const int grid = shares < s->num_sms ? static_cast<int>(shares) : s->num_sms;
     const bool bf16 = dtype == GEMM_BF16;
@@ -221,6 +239,16 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
                           stream) != cudaSuccess) {
         (void)cudaGetLastError();
         return GEMM_ERR_CUDA;
+    }
+    if (s->debug_sync) {
+        // Debug mode: wait for the kernel and report a bounded wait that gave up.
+        int dev_status = 0;
+        if (cudaStreamSynchronize(stream) != cudaSuccess ||
+            cudaMemcpy(&dev_status, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (dev_status != 0) return GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;
 }

@@ -261,6 +261,20 @@ GEMM_API gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles
 GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st *stream);
 
 /*
+ * Launch floor probe (the pages have no counterpart): enqueue on `stream` one
+ * kernel that does no work, launched the way the GEMM kernels are -- `grid`
+ * CTAs of 192 threads in clusters of `cluster` (1 or 2) CTAs, as a
+ * programmatic dependent of the previous work in the stream (it waits for
+ * that work, then lets the next kernel start).  Timing a graph of these
+ * launches gives the fixed cost that every launch of a short GEMM pays, the
+ * bound against which the small problems are measured.  Asynchronous; reads
+ * and writes no memory.
+ * Errors: INVALID_ARG (grid outside 1..65535, cluster not 1 or 2, grid not a
+ * multiple of cluster), CUDA (launch failure).
+ */
+GEMM_API gemm_status_t gemm_noop_launch(int32_t grid, int32_t cluster, struct CUstream_st *stream);
+
+/*
  * gemm_run_noalloc -- C = A @ B for small M without a plan and without any
  * allocation.  The pages have no counterpart to this entry point; it exists
  * for callers that cannot allocate device memory.  A serving process that
@@ -268,9 +282,10 @@ GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_s
  * a library's workspace, and a latency-sensitive loop that shares the GPU
  * with other streams cannot take the device-wide synchronisation that
  * cudaMalloc/cudaFree may cause.  Such callers pass A, B and C as usual; the
- * scratch the split-K kernel needs (fp32 partial tiles and per-tile counters)
- * lives in one static device array of GEMM_NOALLOC_SCRATCH_BYTES that every
- * GPU which loads this library holds until the process exits.
+ * scratch the split-K kernel needs (fp32 partial tiles, a status word and
+ * per-tile counters) lives in one static device array of
+ * GEMM_NOALLOC_SCRATCH_BYTES, which a device holds from this entry point's
+ * first call on it until the process exits.
  *
  * Same operation, layout and argument rules as gemm_run, on the CURRENT device
  * and `stream`.  Limits: M <= GEMM_NOALLOC_MAX_M, N <= GEMM_NOALLOC_MAX_N,
@@ -279,19 +294,33 @@ GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_s
  * is chosen to fit the scratch.  This call never calls cudaMalloc, cudaFree or
  * any allocating routine.
  *
- * The first call on a device does a one-time set-up for that device (checks
- * the architecture, sets kernel attributes and looks up the scratch array's
- * device address); make that first call before any stream capture.  Every
- * call on a device shares the one scratch array, which keeps the last call's
- * contents (each call clears the counters it uses): calls that can overlap on
- * the GPU -- on different streams, or from different threads -- race and give
- * wrong results.  Serialise them.
+ * Set-up: the first call on a device (any call that passes the size checks,
+ * including one with M == 0 or N == 0, which launches nothing) checks the
+ * architecture, sets kernel attributes and looks up the scratch array's device
+ * address.  With CUDA's default lazy module loading, that is the moment the
+ * array and this entry point's kernels are placed in device memory, so a
+ * caller that will later give all free memory to its own pool makes its first
+ * call -- e.g. gemm_run_noalloc(NULL, 0, NULL, 0, NULL, 0, 0, 0, 0, GEMM_BF16,
+ * NULL) -- before it does, and before any stream capture.  A set-up that
+ * fails is retried by the next call.  With CUDA_MODULE_LOADING=EAGER the array
+ * is placed when the library is loaded.
+ *
+ * Every call on a device shares the one scratch array, which keeps the last
+ * call's contents (each call clears the status word and the counters it
+ * uses): calls that can overlap on the GPU -- on different streams, or from
+ * different threads -- race and give wrong results.  Serialise them.
+ *
  * Errors: INVALID_ARG and UNSUPPORTED as above, CUDA for a failed set-up or
- * launch.
+ * launch.  A bounded device-side wait that gives up (the kernel then stops
+ * and C is left incomplete) is recorded in the status word but NOT reported
+ * by the call, which does not wait for the kernel -- unless GEMM_DEBUG_SYNC=1
+ * was set when the device was set up: then every call waits for its kernel
+ * and returns GEMM_ERR_TIMEOUT for a wait that gave up.
  */
 #define GEMM_NOALLOC_MAX_M 64
 #define GEMM_NOALLOC_MAX_N 131072
-#define GEMM_NOALLOC_SCRATCH_BYTES 8392704   /* 8 MiB of partial tiles + 4 KiB of counters */
+#define GEMM_NOALLOC_SCRATCH_BYTES 8392960   /* 8 MiB of partial tiles, 16 B of status, 4 KiB of
+                                                counters, rounded up to 256 B */
 GEMM_API gemm_status_t gemm_run_noalloc(const void *A, int64_t lda,
                                         const void *B, int64_t ldb,
                                         float *C, int64_t ldc,
