@@ -197,12 +197,14 @@ cudaError_t launch_pair(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
 // of their partials through distributed shared memory.  ms in {16, 32, 64} (M <= 64
 // padded: one strip of rows) with bn in {128, 192, 256}, or ms = 128 (tiles of 128
 // rows) with bn = 128; grid = 2 x tiles_m x tiles_n; num_kb >= 2; A not transposed.
-int splitpair_stages(int ms, int bn);
+// b_gen (ms = 128, b_mn only): B is not 16-byte aligned and is read in place with
+// ordinary loads (mapB unused).
+int splitpair_stages(int ms, int bn, bool b_gen);
 cudaError_t splitpair_prepare();
 int splitpair_max_clusters();       // co-resident 2-CTA clusters (0 = unknown)
-cudaError_t launch_splitpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
-                          const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                          cudaStream_t stream);
+cudaError_t launch_splitpair(int ms, int bn, bool b_mn, bool b_gen, const CUtensorMap& mapA,
+                             const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                             uint32_t idesc, int grid, cudaStream_t stream);
 
 // Copy a rows x cols 16-bit matrix (pitch lds) into dst with pitch ldd (a multiple
 // of 8 elements, dst 16-byte aligned), zero-filling columns [cols, ldd).

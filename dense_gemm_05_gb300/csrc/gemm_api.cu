@@ -45,6 +45,7 @@ struct gemm_plan_s {
     int force_kernel = 0;
     int force_split = 0;
     int force_bn = 0;
+    bool staging = true;             // copy misaligned operands to 16-byte rows when they fit
     int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
     int splitpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
     bool debug_sync = false;
@@ -293,7 +294,8 @@ struct Staging {
 bool plan_staging(const gemm_plan_s* plan, const Args& a, Staging* st, Args* out) {
     *out = a;
     *st = Staging{};
-    if (plan->force_kernel == GEMM_KERNEL_GENERIC || plan->stage_bytes == 0 || a.M == 0 ||
+    if (plan->force_kernel == GEMM_KERNEL_GENERIC || !plan->staging || plan->stage_bytes == 0 ||
+        a.M == 0 ||
         a.N == 0 || a.K == 0)
         return false;
     const bool a_bad = !tma_ok(a.A, a.lda);
@@ -348,7 +350,32 @@ int splitpair_auto_bn(const gemm_plan_s* plan, const Args& a) {
     return bn;
 }
 
-gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
+// B read in place by the split-pair kernel (no staging copy): A 16-byte aligned
+// and not transposed, B stored K x N (N contiguous) with a base or pitch that is
+// not a multiple of 16 bytes, and a problem the split-pair kernel takes with
+// 128 x 128 tiles -- by the automatic rule of `choose` (M > 64, the tiles fit one
+// wave of clusters, at least kSplitPairMinKb K blocks) or forced -- when B does
+// not fit the staging buffer (or staging is off).  A staged B is faster where it
+// fits: on the ragged 1023 x 1000 x 1029 fp16 workload (graph-replayed) 12.2 us
+// staged against 14.0 us read in place, whose loader warps (copies of each
+// row's aligned span, then a shift into the swizzled stage) add about 0.55 us
+// per K block over TMA; where B does not fit, the alternative is the generic
+// kernel, about six times slower.
+bool b_in_place(const gemm_plan_s* plan, const Args& a) {
+    if (a.M <= 64 || a.N == 0 || a.K == 0 || a.op_a != GEMM_OP_N || a.op_b != GEMM_OP_N)
+        return false;
+    if (!tma_ok(a.A, a.lda) || tma_ok(a.B, a.ldb) || plan->splitpair_clusters <= 0) return false;
+    const uint64_t staged_b = static_cast<uint64_t>(a.K) * static_cast<uint64_t>((a.N + 7) / 8 * 8) * 2;
+    if (plan->staging && plan->stage_bytes > 0 && staged_b <= plan->stage_bytes) return false;
+    if (plan->force_kernel == GEMM_KERNEL_SPLIT_PAIR)
+        return cdiv(a.K, dg::kBK) >= 2 && (plan->force_bn == 0 || plan->force_bn == 128);
+    if (plan->force_kernel != 0) return false;
+    return cdiv(a.M, dg::kBM) * cdiv(a.N, 128) <= plan->splitpair_clusters &&
+           cdiv(a.K, dg::kBK) >= kSplitPairMinKb;
+}
+
+// b_gen: B is read in place by the split-pair kernel (b_in_place holds).
+gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c, bool b_gen = false) {
     *c = Choice{};
     if (a.M == 0 || a.N == 0) {
         c->kernel = GEMM_KERNEL_NONE;
@@ -358,7 +385,7 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         c->kernel = GEMM_KERNEL_ZERO_FILL;
         return GEMM_OK;
     }
-    const bool tma = tma_ok(a.A, a.lda) && tma_ok(a.B, a.ldb);
+    const bool tma = tma_ok(a.A, a.lda) && (b_gen || tma_ok(a.B, a.ldb));
     int kernel = plan->force_kernel;
     int auto_bn = 0;
     if (kernel == 0) {
@@ -420,6 +447,7 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         kernel != GEMM_KERNEL_GENERIC && kernel != GEMM_KERNEL_PAIR &&
         kernel != GEMM_KERNEL_SPLIT_PAIR)
         return GEMM_ERR_UNSUPPORTED;
+    if (b_gen && kernel != GEMM_KERNEL_SPLIT_PAIR) return GEMM_ERR_UNSUPPORTED;
     c->kernel = kernel;
     c->num_kb = static_cast<int>(cdiv(a.K, dg::kBK));
     if (kernel == GEMM_KERNEL_SKINNY) {
@@ -445,7 +473,7 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c) {
         c->units = static_cast<int>(tiles);
         c->split = 2;
         c->grid = 2 * c->units;
-        c->stages = dg::splitpair_stages(c->ms, c->bn);
+        c->stages = dg::splitpair_stages(c->ms, c->bn, b_gen);
         return GEMM_OK;
     } else if (kernel == GEMM_KERNEL_PAIR) {
         const int64_t tm = cdiv(a.M, 2 * dg::kBM);
@@ -750,6 +778,12 @@ gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_set_staging(gemm_plan_t plan, int32_t enabled) {
+    if (plan == nullptr || (enabled != 0 && enabled != 1)) return GEMM_ERR_INVALID_ARG;
+    plan->staging = enabled != 0;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_tile_coord(int64_t t, int64_t tiles_m, int64_t tiles_n, int32_t group,
                               int64_t* tile_m, int64_t* tile_n) {
     if (tile_m == nullptr || tile_n == nullptr || tiles_m <= 0 || tiles_n <= 0 || group < 0 ||
@@ -767,11 +801,12 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     if (plan == nullptr || out == nullptr) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_args(a_in);
     if (st != GEMM_OK) return st;
-    Args a;
+    Args a = a_in;
     Staging sg;
-    plan_staging(plan, a_in, &sg, &a);
+    const bool b_gen = b_in_place(plan, a_in);
+    if (!b_gen) plan_staging(plan, a_in, &sg, &a);
     Choice c;
-    st = choose(plan, a, &c);
+    st = choose(plan, a, &c, b_gen);
     if (st != GEMM_OK) return st;
     gemm_config_t cfg{};
     cfg.kernel = c.kernel;
@@ -793,7 +828,7 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
                     : 0;
     cfg.tiles = c.units;
     cfg.shares = c.shares;
-    cfg.staged = (sg.a ? 1 : 0) | (sg.b ? 2 : 0);
+    cfg.staged = (sg.a ? 1 : 0) | (sg.b ? 2 : 0) | (b_gen ? 4 : 0);
     *out = cfg;
     return GEMM_OK;
 }
@@ -802,11 +837,12 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
     if (plan == nullptr || plan->model) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = check_args(a_in);
     if (st != GEMM_OK) return st;
-    Args a;
+    Args a = a_in;
     Staging sg;
-    const bool staged = plan_staging(plan, a_in, &sg, &a);
+    const bool b_gen = b_in_place(plan, a_in);
+    const bool staged = b_gen ? false : plan_staging(plan, a_in, &sg, &a);
     Choice c;
-    st = choose(plan, a, &c);
+    st = choose(plan, a, &c, b_gen);
     if (st != GEMM_OK) return st;
     if (c.kernel == GEMM_KERNEL_NONE) return GEMM_OK;
 
@@ -909,10 +945,12 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
                                   stream);
         } else if (c.kernel == GEMM_KERNEL_SPLIT_PAIR) {
             // A tile (M <= 64 rows, K-major) as the MMA's 128-row A operand, the
-            // B tile (bn columns) as its B operand.
+            // B tile (bn columns) as its B operand.  A B read in place (b_gen) has
+            // no tensor map.
             CUtensorMap ma, mb;
+            memset(&mb, 0, sizeof(mb));
             if (!map_a(&ma, static_cast<uint32_t>(c.ms)) ||
-                !map_b(&mb, static_cast<uint32_t>(c.bn)))
+                (!b_gen && !map_b(&mb, static_cast<uint32_t>(c.bn))))
                 return GEMM_ERR_CUDA;
             // With one row of tiles every CTA streams its own B strip once from
             // DRAM: its first K blocks are prefetched into L2 before the wait on
@@ -920,9 +958,10 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             // them).  With several tile rows B is shared through L2 and the early
             // reads only compete (measured slower at 1024 x 1024 x 8192).
             p.prefetch_kb = (!staged && c.tiles_m == 1) ? kL2PrefetchKb : 0;
-            err = dg::launch_splitpair(c.ms, c.bn, b_mn, ma, mb, p,
-                                    dg::idesc_f16(bf16, false, b_mn, dg::kBM, c.bn), c.grid,
-                                    stream);
+            map_c();
+            err = dg::launch_splitpair(c.ms, c.bn, b_mn, b_gen, ma, mb, mc, p,
+                                       dg::idesc_f16(bf16, false, b_mn, dg::kBM, c.bn), c.grid,
+                                       stream);
         } else if (c.kernel == GEMM_KERNEL_GENERIC) {
             err = dg::launch_generic(a_mn, b_mn, p,
                                      dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, 128), c.grid,

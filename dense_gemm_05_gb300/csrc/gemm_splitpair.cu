@@ -16,17 +16,20 @@
 // A window hold whatever follows the A tile in shared memory; they only feed
 // accumulator rows that are never read.
 //
-// When both halves are summed, each CTA keeps one half of the strip's columns:
-// it sends the other half of its fp32 partial into the peer CTA's shared memory
-// (distributed shared memory of the cluster), receives the peer's half of its
-// own columns, adds the two (a + b: one rounding, the same bits whichever CTA
-// adds) and stores C: with 16-byte stores of fp32 C each thread writes its row
-// directly; otherwise (a C pitch that is not a 16-byte multiple, 16-bit C) the
-// sums go back into the exchange buffer and C is written from it row by row,
-// each warp store covering contiguous columns of one row (measured: the
-// 1023 x 1000 x 1029 workload, whose C rows are not 16-byte aligned, 15.1 ->
-// 13.4 us; with aligned fp32 rows the direct stores are faster).  No workspace,
-// counter or second pass.
+// When both halves are summed, each CTA keeps one half of the strip's columns.
+// After the K loop its operand ring is idle, so each CTA writes the other half
+// of its fp32 partial there ([4 columns][row] float4s, 512 contiguous bytes
+// per warp store) and one thread sends it to the peer with a single bulk
+// shared-to-shared copy (cp.async.bulk.shared::cluster), which completes on the
+// peer's barrier.  (Per-thread remote stores of the same 32 KiB took 2.3 us
+// per launch; the bulk copy runs at the copy engine's rate.)  Each CTA then adds
+// the peer's half of its own columns to its own partial (a + b: one rounding,
+// the same bits whichever CTA adds) and stores C through the chunk epilogue of
+// tiles.cuh: tensor-memory-access stores where C allows them, otherwise
+// 16-byte stores wherever a row's alignment allows.  No workspace, counter or
+// second pass.  A bounded wait that runs out claims the receiving CTA's
+// exchange slot (a compare-and-swap the sender also makes before it sends), so
+// a copy is never in flight into a CTA that has left.
 //
 // Warp roles: warp 0 MMA issuer + TMEM owner, warps 1..4 epilogue (warp w reads
 // TMEM lanes 32 (w % 4) ..; rows of C are lanes), warp 5 TMA producer.
@@ -47,48 +50,70 @@
 
 namespace dg {
 
-template <int MS, int BN, int STAGES>
+// B read in place (B_GEN): raw-row stages of bulk copies in flight per loader warp.
+constexpr int kSplitPairRawStages = 3;
+
+template <int MS, int BN, int STAGES, int RAW = 0>
 struct SplitPairCfg {
     static constexpr int kAStageBytes = MS * kBK * 2;       // A tile: MS rows x 64 k, K-major
     static constexpr int kBStageBytes = BN * kBK * 2;       // B tile: BN n x 64 k
     static constexpr int kHalf = BN / 2;                    // columns kept by each CTA
-    static constexpr int kXPitch = kHalf + 4;               // floats per exchange row (bank spread)
-    static constexpr int kXBytes = MS * kXPitch * 4;
+    static constexpr int kXBytes = MS * kHalf * 4;          // one half of the fp32 partial
+    static constexpr int kRingBytes = STAGES * (kAStageBytes + kBStageBytes);
+    // After the K loop the operand ring is free: it holds the half sent to the
+    // peer, then (from a 1 KiB boundary) the epilogue warps' chunk buffers.
+    static constexpr int kEpiOffset = (kXBytes + 1023) / 1024 * 1024;
     static constexpr int kTmemCols = 256;
     static constexpr int kThreads = 192;
     static constexpr int kEpiWarps = (MS + 31) / 32;        // epilogue warps holding rows
-    static constexpr int kNumBars = 2 * STAGES + 3;
+    // B read in place: RAW stages of raw rows (kRawStageBytes each), one barrier
+    // per stage and loader warp.
+    static constexpr int kRawBytes = RAW * kRawStageBytes;
+    static constexpr int kNumBars = 2 * STAGES + 3 + 4 * RAW;
     static constexpr int kSmemBytes =
-        1024 + STAGES * (kAStageBytes + kBStageBytes) + kXBytes + 8 * kNumBars + 16;
+        1024 + kRingBytes + kXBytes + kRawBytes + 8 * kNumBars + 16;
     static_assert(MS == 16 || MS == 32 || MS == 64 || MS == 128, "MS");
     static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "BN");
     // The MMA reads a 128-row (16 KiB) A window from each A stage; the B ring
     // behind the A stages keeps the last window inside the allocation.
     static_assert(STAGES * kBStageBytes >= kBM * kBK * 2, "A window");
     static_assert(kAStageBytes % 1024 == 0 && kBStageBytes % 1024 == 0, "swizzle atoms");
+    static_assert(kEpiOffset + kEpiSmemBytes <= kRingBytes, "epilogue buffers fit the ring");
+    static_assert(kXBytes % 16 == 0, "bulk copy size");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
-template <int MS, int BN, int STAGES, bool B_MN>
+// B_GEN: B (stored K x N) is not 16-byte aligned and is read in place by the
+// four epilogue warps with ordinary loads while the K loop runs (the
+// unaligned-rows loader of tiles.cuh); A still comes by TMA.  Only with 128-row
+// tiles of 128 columns.
+template <int MS, int BN, int STAGES, bool B_MN, bool B_GEN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_splitpair_kernel(const __grid_constant__ CUtensorMap mapA,
-                       const __grid_constant__ CUtensorMap mapB, const Params p,
-                       const uint32_t idesc) {
-    using Cfg = SplitPairCfg<MS, BN, STAGES>;
+                          const __grid_constant__ CUtensorMap mapB,
+                          const __grid_constant__ CUtensorMap mapC, const Params p,
+                          const uint32_t idesc) {
+    constexpr int RAW = B_GEN ? kSplitPairRawStages : 0;
+    using Cfg = SplitPairCfg<MS, BN, STAGES, RAW>;
+    static_assert(!B_GEN || (MS == 128 && BN == 128 && B_MN), "in-place B loads: 128 x 128 tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;                                       // STAGES packed A tiles
     uint8_t* sB = sA + STAGES * Cfg::kAStageBytes;
-    float* sX = reinterpret_cast<float*>(sB + STAGES * Cfg::kBStageBytes);   // peer's half
-    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sX) + Cfg::kXBytes);
+    float4* sX = reinterpret_cast<float4*>(sB + STAGES * Cfg::kBStageBytes);   // peer's half
+    uint8_t* sRaw = reinterpret_cast<uint8_t*>(sX) + Cfg::kXBytes;             // B_GEN raw rows
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sRaw + Cfg::kRawBytes);
     uint64_t* full = bars;
     uint64_t* empty = bars + STAGES;
     uint64_t* tfull = bars + 2 * STAGES;
-    uint64_t* xfull = tfull + 1;     // the peer's MS rows have arrived in sX
+    uint64_t* xfull = tfull + 1;     // the peer's half has landed in sX
     uint64_t* drain = xfull + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* rawfull = drain + 1;   // [RAW][4]: raw rows of a stage landed, per loader warp
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rawfull + 4 * RAW);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* xstate = const_cast<int*>(abort_flag) + 1;   // 0, then 1 = peer sends, 2 = gave up
+    float4* sSend = reinterpret_cast<float4*>(smem);  // the ring, once the K loop is done
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -106,21 +131,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1u);
+            // B_GEN: the producer's TMA arrival for A plus the 128 loader threads for B
+            mbar_init(smem_u32(&full[s]), B_GEN ? 129u : 1u);
             mbar_init(smem_u32(&empty[s]), 1u);
         }
         mbar_init(smem_u32(tfull), 1u);
-        mbar_init(smem_u32(xfull), static_cast<uint32_t>(MS));
+        mbar_init(smem_u32(xfull), 1u);
         mbar_init(smem_u32(drain), 1u);
+        for (int i = 0; i < 4 * RAW; ++i) mbar_init(smem_u32(&rawfull[i]), 32u);   // a warp's lanes
         *abort_flag = 0;
+        *xstate = 0;
+        // The peer's bulk copy of its half completes on xfull.
+        mbar_arrive_expect_tx(smem_u32(xfull), static_cast<uint32_t>(Cfg::kXBytes));
         fence_mbar_init();
     }
     if (warp == 5 && lane == 0) {
         prefetch_tmap(&mapA);
-        prefetch_tmap(&mapB);
+        if (!B_GEN) prefetch_tmap(&mapB);
+        if (p.c_tma) prefetch_tmap(&mapC);
     }
     __syncthreads();
-    // Released here, waited for (by every thread) before the first remote arrive
+    // Released here, waited for (by every thread) before the first remote access
     // and before leaving: the peer's barriers are initialised when it is passed.
     cluster_arrive_release();
     griddep_launch_dependents();
@@ -173,21 +204,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         named_bar_sync(2, 160);
         tc_fence_after();
         const uint32_t tmem_base = *tmem_slot;
-        griddep_wait();                               // C may still be read by the previous grid
-        cluster_wait_acquire();                       // the peer's exchange barrier exists
+        griddep_wait();                               // C (and B) may still be used by the previous grid
+        cluster_wait_acquire();                       // the peer's barriers exist
+        if constexpr (B_GEN) {
+            // ---------------------------------------------------- B loader (K loop)
+            // Warp w4 copies its 16 rows of each stage into the raw ring (RAW
+            // stages ahead of the MMA), then moves them into the swizzled B stage.
+            const int w4 = warp - 1;
+            const uint32_t raw0 = smem_u32(sRaw);
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0, placed = 0;       // stages of this CTA's K half
+            const int nkb = kb1 - kb0;
+            auto issue = [&](int j) {         // j-th stage of the half into raw slot j % RAW
+                const int slot = j % RAW;
+                unaligned_rows_issue(raw0 + static_cast<uint32_t>(slot * kRawStageBytes),
+                                     smem_u32(&rawfull[slot * 4 + w4]), p.B, p.ldb, n0,
+                                     (kb0 + j) * kBK, p.N, p.K, w4, lane);
+            };
+            for (; issued < RAW && issued < nkb; ++issued) issue(issued);
+            bool failed = false;
+#pragma unroll 1
+            for (; placed < nkb; ++placed) {
+                const int slot = placed % RAW;
+                const uint32_t rphase = static_cast<uint32_t>(placed / RAW) & 1u;
+                bool ok = mbar_wait(smem_u32(&rawfull[slot * 4 + w4]), rphase, abort_flag,
+                                    p.timeout_ns);
+                ok = ok && mbar_wait(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p.timeout_ns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    failed = true;
+                    break;
+                }
+                unaligned_rows_place(smem_u32(sB + stage * Cfg::kBStageBytes),
+                                     raw0 + static_cast<uint32_t>(slot * kRawStageBytes), p.B, p.ldb,
+                                     n0, (kb0 + placed) * kBK, p.N, p.K, w4, lane);
+                // generic stores -> the MMA's operand reads; generic reads of the raw
+                // slot -> the next bulk copy into it
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                __syncwarp();
+                if (issued < nkb) issue(issued++);
+            }
+            if (failed) {
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                // Bulk copies already issued must land before the shared memory goes away.
+                const volatile int never = 0;
+                for (int j = placed; j < issued; ++j)
+                    mbar_wait(smem_u32(&rawfull[(j % RAW) * 4 + w4]),
+                              static_cast<uint32_t>(j / RAW) & 1u, &never, 50000000ull);
+            }
+        }
         const int q = warp & 3;                       // TMEM lane quadrant of this warp
-        const bool direct = p.c_type == kOutF32 && p.c_vec;   // the same in every thread
         if (q * 32 < MS) {
-            const int r = q * 32 + lane;              // row of C (TMEM lane)
+            const int r = q * 32 + lane;              // row of the tile (TMEM lane)
+            const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             bool ok = mbar_wait(smem_u32(tfull), 0u, abort_flag, p.timeout_ns);
             // tcgen05.ld is warp-collective: one decision per warp.
             ok = __all_sync(0xffffffffu, ok);
+            // 1. The peer's half of the columns goes to the peer in one bulk copy
+            // through this CTA's now idle operand ring, laid out [4 columns][row]
+            // as float4 (a warp writes 512 contiguous bytes).  The producer warp,
+            // idle once the K loop is issued, sends it (step 1b below), so that no
+            // epilogue thread has a copy of its own in flight.
             if (ok) {
                 tc_fence_after();
-                const uint32_t trow = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-                // 1. The peer's half of the columns goes to the peer's exchange buffer.
-                const uint32_t x_remote =
-                    mapa_shared(smem_u32(sX) + static_cast<uint32_t>(r * Cfg::kXPitch * 4), peer);
+                fence_proxy_async_smem();   // the ring was last used by TMA and the MMAs
 #pragma unroll 1
                 for (int c = 0; c < Cfg::kHalf; c += 32) {
                     uint32_t v[32];
@@ -196,43 +282,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     if (r < MS) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            st_cluster_v4_b32(x_remote + static_cast<uint32_t>((c + 4 * j) * 4),
-                                              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                                                         v[4 * j + 3]));
+                            sSend[(c / 4 + j) * MS + r] =
+                                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     }
                 }
-                if (r < MS) mbar_arrive_cluster(mapa_shared(smem_u32(xfull), peer));
-                // This thread touches the peer's shared memory no more: its arrival on
-                // the closing cluster barrier can go now.
-                cluster_arrive_release();
-                arrived = true;
-                // 2. This CTA's half: own partial + the peer's.  With 16-byte stores of
-                // fp32 C each thread writes its own row straight away; otherwise the
-                // sums go back into the exchange buffer and step 3 writes them out.
-                const bool got = mbar_wait_cluster(smem_u32(xfull), 0u, abort_flag, p.timeout_ns);
-                if (!got) {
-                    *abort_flag = 1;
-                    if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                fence_proxy_async_smem();
+            } else {
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+            }
+            named_bar_arrive(4, 32 * Cfg::kEpiWarps + 32);
+            // 2. The peer's half of this CTA's columns.  A wait that runs out claims
+            // the exchange slot so that the peer sends nothing afterwards; if the
+            // peer had already claimed it, its copy is on the way and is waited
+            // for (with a long bound) before this CTA may leave.
+            bool got = mbar_wait_cluster(smem_u32(xfull), 0u, abort_flag, p.timeout_ns);
+            if (!got) {
+                if (atom_cas_shared_cluster(smem_u32(xstate), 0, 2) == 1) {
+                    const volatile int never = 0;
+                    mbar_wait_cluster(smem_u32(xfull), 0u, &never, 100000000ull);
                 }
-                if (__all_sync(0xffffffffu, got) && direct) {
-                    const float* xrow = sX + r * Cfg::kXPitch;
-                    const int col_base = n0 + static_cast<int>(rank) * Cfg::kHalf;
-                    const int row = m0 + r;
+                *abort_flag = 1;
+                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+            }
+            // Nothing more arrives in this CTA's shared memory once the peer's copy
+            // has landed, and this thread touches no other CTA's memory: the closing
+            // arrival can go now, without release semantics.
+            cluster_arrive_relaxed();
+            arrived = true;
+            got = __all_sync(0xffffffffu, got) && ok;
+            // 3. This CTA's half: own partial + the peer's (a + b, one rounding, the
+            // same bits whichever CTA adds), then C through the chunk epilogue
+            // (tensor-memory-access stores where C allows them).
+            const uint32_t ebuf =
+                smem_u32(smem) + Cfg::kEpiOffset + static_cast<uint32_t>((warp - 1) * kEpiWarpBytes);
+            uint32_t eseq = 0;
+            const int col_base = n0 + static_cast<int>(rank) * Cfg::kHalf;
+            const int row0 = m0 + q * 32;
+            if (p.c_type == kOutF32 || Cfg::kHalf % 64 == 0) {
+                if (got) {
+                    const int cw = epi_chunk_cols(p.c_type);
 #pragma unroll 1
-                    for (int c = 0; c < Cfg::kHalf; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(trow + rank * Cfg::kHalf + c, v);
-                        tmem_ld_wait(v);
-                        const int col = col_base + c;
-                        if (r < MS && row < p.M && col < p.N) {
+                    for (int c = 0; c < Cfg::kHalf; c += cw) {
+                        uint32_t lo[32], hi[32];
+                        tmem_ld_32x32b_x32(trow + rank * Cfg::kHalf + c, lo);
+                        if (cw == 64) tmem_ld_32x32b_x32(trow + rank * Cfg::kHalf + c + 32, hi);
+                        tmem_ld_wait(lo);
+                        if (cw == 64) tmem_ld_wait(hi);
+                        const int rx = r < MS ? r : 0;   // rows beyond a short strip: masked at M
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                v[j] = __float_as_uint(__uint_as_float(v[j]) + xrow[c + j]);
-                            store_c32(p, static_cast<int64_t>(row) * p.ldc + col, v, p.N - col);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 x = sX[(c / 4 + j) * MS + rx];
+                            lo[4 * j] = __float_as_uint(__uint_as_float(lo[4 * j]) + x.x);
+                            lo[4 * j + 1] = __float_as_uint(__uint_as_float(lo[4 * j + 1]) + x.y);
+                            lo[4 * j + 2] = __float_as_uint(__uint_as_float(lo[4 * j + 2]) + x.z);
+                            lo[4 * j + 3] = __float_as_uint(__uint_as_float(lo[4 * j + 3]) + x.w);
                         }
+                        if (cw == 64) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 x = sX[(c / 4 + 8 + j) * MS + rx];
+                                hi[4 * j] = __float_as_uint(__uint_as_float(hi[4 * j]) + x.x);
+                                hi[4 * j + 1] = __float_as_uint(__uint_as_float(hi[4 * j + 1]) + x.y);
+                                hi[4 * j + 2] = __float_as_uint(__uint_as_float(hi[4 * j + 2]) + x.z);
+                                hi[4 * j + 3] = __float_as_uint(__uint_as_float(hi[4 * j + 3]) + x.w);
+                            }
+                        }
+                        epi_store_chunk(p, &mapC, ebuf, eseq, lane, row0, col_base + c, lo, hi);
                     }
-                } else if (__all_sync(0xffffffffu, got)) {
-                    float* xrow = sX + r * Cfg::kXPitch;
+                    // The tensor-memory-access stores must have read their buffers
+                    // before the shared memory goes away.
+                    if (lane == 0 && p.c_tma) bulk_wait_group0();
+                }
+            } else {
+                // 16-bit C with 96 columns per CTA (not whole 64-column chunks): the
+                // sums go back into the exchange buffer and are written row by row.
+                if (got) {
 #pragma unroll 1
                     for (int c = 0; c < Cfg::kHalf; c += 32) {
                         uint32_t v[32];
@@ -240,35 +366,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         tmem_ld_wait(v);
                         if (r < MS) {
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4) {
-                                float4* x4 = reinterpret_cast<float4*>(xrow + c + j);
-                                float4 t = *x4;
-                                t.x += __uint_as_float(v[j]);
-                                t.y += __uint_as_float(v[j + 1]);
-                                t.z += __uint_as_float(v[j + 2]);
-                                t.w += __uint_as_float(v[j + 3]);
-                                *x4 = t;
+                            for (int j = 0; j < 8; ++j) {
+                                float4& x = sX[(c / 4 + j) * MS + r];
+                                x.x += __uint_as_float(v[4 * j]);
+                                x.y += __uint_as_float(v[4 * j + 1]);
+                                x.z += __uint_as_float(v[4 * j + 2]);
+                                x.w += __uint_as_float(v[4 * j + 3]);
                             }
                         }
                     }
                 }
-            } else {
-                *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
-            }
-            // 3. (Not direct) C from the exchange buffer, row by row: every row of
-            // this CTA's half is complete once all epilogue warps holding rows have
-            // passed the barrier; each warp store covers contiguous columns of a row.
-            if (!direct) named_bar_sync(3, 32 * Cfg::kEpiWarps);
-            if (!direct && *abort_flag == 0) {
-                const int col_base = n0 + static_cast<int>(rank) * Cfg::kHalf;
-                for (int rr = q; rr < MS && m0 + rr < p.M; rr += Cfg::kEpiWarps) {
-                    const float* xr = sX + rr * Cfg::kXPitch;
-                    const int64_t off = static_cast<int64_t>(m0 + rr) * p.ldc;
+                // Every warp holding rows passes this barrier, whatever its waits gave.
+                if (named_bar_and(3, 32 * Cfg::kEpiWarps, got)) {
+                    const float* xs = reinterpret_cast<const float*>(sX);
+                    for (int rr = q; rr < MS && m0 + rr < p.M; rr += Cfg::kEpiWarps) {
+                        const int64_t off = static_cast<int64_t>(m0 + rr) * p.ldc;
 #pragma unroll 4
-                    for (int cc = lane; cc < Cfg::kHalf; cc += 32) {
-                        const int col = col_base + cc;
-                        if (col < p.N) store_c1(p, off + col, xr[cc]);
+                        for (int cc = lane; cc < Cfg::kHalf; cc += 32) {
+                            const int col = col_base + cc;
+                            if (col < p.N)
+                                store_c1(p, off + col, xs[((cc >> 2) * MS + rr) * 4 + (cc & 3)]);
+                        }
                     }
                 }
             }
@@ -287,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             // and the first loads after the wait then find their lines in L2.
             for (int kb = kb0; kb < kb1 && kb < kb0 + p.prefetch_kb; ++kb) {
                 tma_prefetch_2d_hint(&mapA, kb * kBK, m0, pol_keep);
-                prefetch_operand_hint<B_MN>(&mapB, n0, kb * kBK, BN, pol_stream);
+                if (!B_GEN) prefetch_operand_hint<B_MN>(&mapB, n0, kb * kBK, BN, pol_stream);
             }
             griddep_wait();                   // A and B may be written by the previous grid
             for (int kb = kb0; kb < kb1; ++kb) {
@@ -296,12 +414,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     break;
                 }
                 const uint32_t fb = smem_u32(&full[stage]);
-                mbar_arrive_expect_tx(
-                    fb, static_cast<uint32_t>(Cfg::kAStageBytes + Cfg::kBStageBytes));
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(B_GEN ? Cfg::kAStageBytes
+                                                                      : Cfg::kAStageBytes +
+                                                                            Cfg::kBStageBytes));
                 tma_load_2d_hint(smem_u32(sA + stage * Cfg::kAStageBytes), &mapA, fb, kb * kBK, m0,
                                  pol_keep);
-                load_operand_hint<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb, n0,
-                                        kb * kBK, BN, pol_stream);
+                if (!B_GEN)
+                    load_operand_hint<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb,
+                                            n0, kb * kBK, BN, pol_stream);
                 ++armed;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -328,7 +448,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
         }
         __syncwarp();
-        cluster_wait_acquire();
+        cluster_wait_acquire();             // the peer's barriers exist
+        // 1b. Once the epilogue warps holding rows have written the peer's half
+        // (named barrier 4), claim the peer's exchange slot and send the half.
+        // A peer that has given up (a bounded wait ran out) has claimed the slot
+        // first, and then nothing is sent; nor is anything after a wait of this
+        // CTA gave up (the abort flag).
+        named_bar_sync(4, 32 * Cfg::kEpiWarps + 32);
+        if (lane == 0) {
+            if (*abort_flag == 0 &&
+                atom_cas_shared_cluster(mapa_shared(smem_u32(xstate), peer), 0, 1) == 0) {
+                bulk_copy_s2s_cluster(mapa_shared(smem_u32(sX), peer), smem_u32(sSend),
+                                      static_cast<uint32_t>(Cfg::kXBytes),
+                                      mapa_shared(smem_u32(xfull), peer));
+            } else {
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -350,23 +487,39 @@ namespace {
 template <int MS, int BN>
 constexpr int stages_for() {
     constexpr int per = MS * kBK * 2 + BN * kBK * 2;
-    constexpr int fixed = 1024 + MS * (BN / 2 + 4) * 4 + 8 * 40 + 16;
+    constexpr int fixed = 1024 + MS * (BN / 2) * 4 + 8 * 40 + 16;
     constexpr int s = (232448 - fixed) / per;
     return s > 8 ? 8 : s;
 }
 
-template <int MS, int BN, bool B_MN>
+// B read in place: a shallower operand ring next to the raw rows.
+constexpr int kSplitPairGenStages = 4;
+
+template <int MS, int BN, bool B_GEN>
+constexpr int stages_of() {
+    return B_GEN ? kSplitPairGenStages : stages_for<MS, BN>();
+}
+
+template <int MS, int BN, bool B_GEN>
+constexpr int smem_of() {
+    return SplitPairCfg<MS, BN, stages_of<MS, BN, B_GEN>(), B_GEN ? kSplitPairRawStages : 0>::kSmemBytes;
+}
+
+template <int MS, int BN, bool B_MN, bool B_GEN = false>
 cudaError_t set_attr_one() {
-    constexpr int S = stages_for<MS, BN>();
-    return cudaFuncSetAttribute(gemm_splitpair_kernel<MS, BN, S, B_MN>,
+    constexpr int S = stages_of<MS, BN, B_GEN>();
+    return cudaFuncSetAttribute(gemm_splitpair_kernel<MS, BN, S, B_MN, B_GEN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SplitPairCfg<MS, BN, S>::kSmemBytes);
+                                smem_of<MS, BN, B_GEN>());
 }
 
 template <int MS, int BN>
 cudaError_t set_attrs_bn() {
     cudaError_t e = set_attr_one<MS, BN, true>();
     if (e == cudaSuccess) e = set_attr_one<MS, BN, false>();
+    if constexpr (MS == 128 && BN == 128) {
+        if (e == cudaSuccess) e = set_attr_one<MS, BN, true, true>();
+    }
     return e;
 }
 
@@ -383,8 +536,9 @@ cudaError_t set_attrs_ms() {
 // Launched as a programmatic dependent of the previous work in the stream (the
 // kernel waits for it before touching global memory).
 template <int MS, int BN>
-cudaError_t launch_bn(bool b_mn, const CUtensorMap& a, const CUtensorMap& b, const Params& p,
-                      uint32_t idesc, int grid, cudaStream_t s) {
+cudaError_t launch_bn(bool b_mn, bool b_gen, const CUtensorMap& a, const CUtensorMap& b,
+                      const CUtensorMap& c, const Params& p, uint32_t idesc, int grid,
+                      cudaStream_t s) {
     constexpr int S = stages_for<MS, BN>();
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -396,19 +550,32 @@ cudaError_t launch_bn(bool b_mn, const CUtensorMap& a, const CUtensorMap& b, con
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (b_mn) return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, true>, a, b, p, idesc);
-    return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, false>, a, b, p, idesc);
+    if constexpr (MS == 128 && BN == 128) {
+        if (b_gen) {
+            constexpr int SG = stages_of<MS, BN, true>();
+            cfg.dynamicSmemBytes = smem_of<MS, BN, true>();
+            return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, SG, true, true>, a, b, c,
+                                      p, idesc);
+        }
+    }
+    if (b_gen) return cudaErrorInvalidValue;
+    if (b_mn)
+        return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, true, false>, a, b, c, p,
+                                  idesc);
+    return cudaLaunchKernelEx(&cfg, gemm_splitpair_kernel<MS, BN, S, false, false>, a, b, c, p,
+                              idesc);
 }
 
 template <int MS>
-cudaError_t launch_ms(int bn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
-                      const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
+cudaError_t launch_ms(int bn, bool b_mn, bool b_gen, const CUtensorMap& a, const CUtensorMap& b,
+                      const CUtensorMap& c, const Params& p, uint32_t idesc, int grid,
+                      cudaStream_t s) {
     if constexpr (MS == 128) {
-        return launch_bn<MS, 128>(b_mn, a, b, p, idesc, grid, s);
+        return launch_bn<MS, 128>(b_mn, b_gen, a, b, c, p, idesc, grid, s);
     } else {
-        if (bn == 128) return launch_bn<MS, 128>(b_mn, a, b, p, idesc, grid, s);
-        if (bn == 192) return launch_bn<MS, 192>(b_mn, a, b, p, idesc, grid, s);
-        return launch_bn<MS, 256>(b_mn, a, b, p, idesc, grid, s);
+        if (bn == 128) return launch_bn<MS, 128>(b_mn, b_gen, a, b, c, p, idesc, grid, s);
+        if (bn == 192) return launch_bn<MS, 192>(b_mn, b_gen, a, b, c, p, idesc, grid, s);
+        return launch_bn<MS, 256>(b_mn, b_gen, a, b, c, p, idesc, grid, s);
     }
 }
 
@@ -427,7 +594,7 @@ int max_clusters_one() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_splitpair_kernel<MS, BN, S, true>, &cfg) !=
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_splitpair_kernel<MS, BN, S, true, false>, &cfg) !=
         cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -436,7 +603,8 @@ int max_clusters_one() {
 }
 }  // namespace
 
-int splitpair_stages(int ms, int bn) {
+int splitpair_stages(int ms, int bn, bool b_gen) {
+    if (b_gen) return kSplitPairGenStages;
     if (ms == 16) return bn == 128 ? stages_for<16, 128>() : (bn == 192 ? stages_for<16, 192>() : stages_for<16, 256>());
     if (ms == 32) return bn == 128 ? stages_for<32, 128>() : (bn == 192 ? stages_for<32, 192>() : stages_for<32, 256>());
     if (ms == 128) return stages_for<128, 128>();
@@ -454,13 +622,14 @@ cudaError_t splitpair_prepare() {
 // All (MS, BN) instantiations hold one CTA per SM, so one query serves them.
 int splitpair_max_clusters() { return max_clusters_one<64, 256>(); }
 
-cudaError_t launch_splitpair(int ms, int bn, bool b_mn, const CUtensorMap& mapA,
-                          const CUtensorMap& mapB, const Params& p, uint32_t idesc, int grid,
-                          cudaStream_t stream) {
-    if (ms == 16) return launch_ms<16>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
-    if (ms == 32) return launch_ms<32>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
-    if (ms == 128) return launch_ms<128>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
-    return launch_ms<64>(bn, b_mn, mapA, mapB, p, idesc, grid, stream);
+cudaError_t launch_splitpair(int ms, int bn, bool b_mn, bool b_gen, const CUtensorMap& mapA,
+                             const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
+                             uint32_t idesc, int grid, cudaStream_t stream) {
+    if (ms == 16) return launch_ms<16>(bn, b_mn, b_gen, mapA, mapB, mapC, p, idesc, grid, stream);
+    if (ms == 32) return launch_ms<32>(bn, b_mn, b_gen, mapA, mapB, mapC, p, idesc, grid, stream);
+    if (ms == 128)
+        return launch_ms<128>(bn, b_mn, b_gen, mapA, mapB, mapC, p, idesc, grid, stream);
+    return launch_ms<64>(bn, b_mn, b_gen, mapA, mapB, mapC, p, idesc, grid, stream);
 }
 
 }  // namespace dg

@@ -190,6 +190,20 @@ __device__ __forceinline__ void bulk_load_g2s(uint32_t dst, const void* src, uin
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared by this thread (both addresses
+// 16-byte aligned), bypassing L1.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has completed
+// (the arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -374,6 +388,18 @@ __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 
+// Arrival without release semantics, for a thread whose memory accesses the
+// other CTAs do not depend on.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+// Arrive on named barrier `id` without waiting for it (the other participants
+// of a bar.sync with the same id and count wait for this arrival).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -401,6 +427,29 @@ __device__ __forceinline__ void st_cluster_v4_b32(uint32_t cluster_addr, uint4 v
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr),
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory into the shared memory of a CTA of the cluster
+// (dst and bar from mapa_shared); completion is counted on that CTA's barrier.
+// The source must have been made visible to the async proxy (fence_proxy_async_smem).
+__device__ __forceinline__ void bulk_copy_s2s_cluster(uint32_t dst_cluster, uint32_t src,
+                                                      uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst_cluster), "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+
+// Compare-and-swap on a 32-bit word in the shared memory of a CTA of the
+// cluster (address from mapa_shared, or this CTA's own); returns the old value.
+__device__ __forceinline__ int atom_cas_shared_cluster(uint32_t addr, int compare, int value) {
+    int old;
+    asm volatile("atom.shared::cluster.cas.b32 %0, [%1], %2, %3;"
+                 : "=r"(old)
+                 : "r"(addr), "r"(compare), "r"(value)
+                 : "memory");
+    return old;
 }
 
 // Arrive on an mbarrier that may live in another CTA of the cluster.

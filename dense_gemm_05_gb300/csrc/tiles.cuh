@@ -216,6 +216,51 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
         return;
     }
     __syncwarp();
+    if (p.c_type == kOutF32 && col + 32 <= p.N) {
+        // fp32 C whose rows are only 4-byte aligned, chunk wholly inside N.  A
+        // warp store costs about the same whatever its width, so the chunk is
+        // written with as few stores as the alignment allows: first every
+        // 16-byte slot that lies inside a row (7 or 8 per row: 8 stores of
+        // float4 across the warp), then each row's head and tail (the 1-3
+        // floats before its first and after its last aligned slot) with at
+        // most four 4- and 8-byte stores, one row per lane.
+        float* cbase = static_cast<float*>(p.C);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int i = lane + 32 * t;
+            const int rr = i >> 3, k = i & 7;
+            const int r = row0 + rr;
+            const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
+            const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
+            if (r < p.M && h + 4 * k + 4 <= 32) {
+                const int e = h + 4 * k;
+                const uint32_t rowb = buf + static_cast<uint32_t>(rr * 128);
+                float4 v;
+                v.x = __uint_as_float(ld_shared_b32(rowb + (static_cast<uint32_t>(((e >> 2) ^ (rr & 7))) << 4) + (e & 3) * 4));
+                v.y = __uint_as_float(ld_shared_b32(rowb + (static_cast<uint32_t>((((e + 1) >> 2) ^ (rr & 7))) << 4) + ((e + 1) & 3) * 4));
+                v.z = __uint_as_float(ld_shared_b32(rowb + (static_cast<uint32_t>((((e + 2) >> 2) ^ (rr & 7))) << 4) + ((e + 2) & 3) * 4));
+                v.w = __uint_as_float(ld_shared_b32(rowb + (static_cast<uint32_t>((((e + 3) >> 2) ^ (rr & 7))) << 4) + ((e + 3) & 3) * 4));
+                *reinterpret_cast<float4*>(cbase + off + e) = v;
+            }
+        }
+        const int r = row0 + lane;
+        const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
+        const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
+        if (r < p.M && h != 0) {
+            const uint32_t rowb = buf + static_cast<uint32_t>(lane * 128);
+            auto elem = [&](int e) {
+                return __uint_as_float(ld_shared_b32(
+                    rowb + (static_cast<uint32_t>(((e >> 2) ^ (lane & 7))) << 4) + (e & 3) * 4));
+            };
+            // h = 3: head e0 (4 B) + e1..2 (8 B), tail e31 (4 B); h = 2: head e0..1,
+            // tail e30..31 (8 B each); h = 1: head e0 (4 B), tail e29..30 (8 B) + e31.
+            if (h & 1) cbase[off] = elem(0);
+            if (h >= 2) *reinterpret_cast<float2*>(cbase + off + h - 2) = make_float2(elem(h - 2), elem(h - 1));
+            if (h <= 2) *reinterpret_cast<float2*>(cbase + off + 28 + h) = make_float2(elem(28 + h), elem(29 + h));
+            if (h & 1) cbase[off + 31] = elem(31);
+        }
+        return;
+    }
     // Lane l reads 32-bit word l of each 128-byte row (in 16-byte piece l / 4).
     const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
 #pragma unroll 4
@@ -281,6 +326,159 @@ __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorM
         tmem_ld_wait(lo);
         if (ch == nchunks - 1) release();
         epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * cw, lo, hi);
+    }
+}
+
+// ---------------------------------------------------------------- unaligned MN-major rows
+// A 64 (K) x 128 (M/N) MN-major operand tile from a matrix whose rows are only
+// 2-byte aligned (e.g. a K x N operand with an odd leading dimension, which
+// TMA cannot address), for the 4 warps of a warpgroup: warp w4 takes K rows
+// w4, w4 + 4, ..., 60 + w4.  The 16-byte-aligned span around each row's 256
+// bytes (at most 17 pieces of 16 bytes) is copied by asynchronous 16-byte
+// copies (cp.async) into a raw row slot of 272 bytes -- many copies in flight
+// per SM, no registers held -- and the elements are then moved into the
+// 128-byte-swizzled tile at their 2-byte offset.  A row whose aligned span
+// would leave the matrix's footprint [base, base + (K - 1) * ld + MN) -- row 0
+// of a base that is not 16-byte aligned, the last row -- is read element by
+// element instead.  Elements beyond K or MN are written as zeros.
+constexpr int kRawRowBytes = 272;
+constexpr int kRawStageBytes = 64 * kRawRowBytes;
+
+struct RowSpan {
+    uintptr_t a;      // byte address of the row's first element
+    uint32_t d;       // a - (a rounded down to 16 bytes)
+    uint32_t pieces;  // 16-byte pieces of the aligned span to copy (0: element-wise or beyond K)
+};
+
+// Row k0 + w4 + 4 i of the warp's 16 (i = 0..15).
+__device__ __forceinline__ RowSpan unaligned_row_span(const uint16_t* base, int64_t ld, int mn0,
+                                                      int k, int mn_total, int k_total) {
+    RowSpan r{0, 0, 0};
+    if (k >= k_total) return r;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t hi =
+        reinterpret_cast<uintptr_t>(base + (static_cast<int64_t>(k_total) - 1) * ld + mn_total);
+    const int ncols = mn_total - mn0 < 128 ? mn_total - mn0 : 128;
+    r.a = reinterpret_cast<uintptr_t>(base + static_cast<int64_t>(k) * ld + mn0);
+    const uintptr_t a16 = r.a & ~static_cast<uintptr_t>(15);
+    r.d = static_cast<uint32_t>(r.a - a16);
+    const uintptr_t e16 = (r.a + 2u * static_cast<uintptr_t>(ncols) + 15u) & ~static_cast<uintptr_t>(15);
+    if (a16 >= lo && e16 <= hi) r.pieces = static_cast<uint32_t>(e16 - a16) >> 4;
+    return r;
+}
+
+// Whether every one of the tile's 64 rows at K offset k0 has its whole aligned
+// span inside the footprint: no row 0 of a misaligned base, no last row, no
+// row beyond K, and rows at least 8 elements apart (so that the up to 14 bytes
+// a span reaches past a row lie in the next or previous row).  Such a stage
+// takes the fast paths below.
+__device__ __forceinline__ bool unaligned_stage_interior(const uint16_t* base, int64_t ld, int mn0,
+                                                         int k0, int k_total) {
+    const bool first_ok = k0 > 0 || mn0 > 0 || (reinterpret_cast<uintptr_t>(base) & 15u) == 0u;
+    return first_ok && ld >= 8 && k0 + 64 < k_total;   // rows k0 .. k0 + 63 below the last
+}
+
+// Issue this warp's copies of its 16 rows of the tile at K offset k0 into the
+// raw stage at `raw` (row kk at kk * kRawRowBytes); every lane then arrives on
+// `bar` (32 expected arrivals) when its copies have landed.  Half-warp h takes
+// rows i = h, h + 2, ..., h + 14 (K rows w4 + 4 i), lane c of it the 16-byte
+// piece c of each (lane 0 also piece 16): a warp instruction copies two rows'
+// 256 contiguous bytes.  All rows of a half-warp sit at the same offset from a
+// 16-byte boundary (their distance, 16 ld bytes, is a multiple of 16), so on
+// an interior stage one row's span serves all eight.
+__device__ __forceinline__ void unaligned_rows_issue(uint32_t raw, uint32_t bar,
+                                                     const uint16_t* base, int64_t ld, int mn0,
+                                                     int k0, int mn_total, int k_total, int w4,
+                                                     int lane) {
+    const int h = lane >> 4, c = lane & 15;
+    if (unaligned_stage_interior(base, ld, mn0, k0, k_total)) {
+        const RowSpan r0 = unaligned_row_span(base, ld, mn0, k0 + w4 + 4 * h, mn_total, k_total);
+        const uintptr_t a16 = r0.a - r0.d;
+        const uintptr_t step = static_cast<uintptr_t>(16 * ld);       // 8 K rows, in bytes
+        const uint32_t dst0 = raw + static_cast<uint32_t>((w4 + 4 * h) * kRawRowBytes);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t dst = dst0 + static_cast<uint32_t>(j * 8 * kRawRowBytes);
+            const uintptr_t src = a16 + static_cast<uintptr_t>(j) * step;
+            if (static_cast<uint32_t>(c) < r0.pieces)
+                cp_async_16(dst + 16u * c, reinterpret_cast<const void*>(src + 16u * c));
+            if (c == 0 && r0.pieces > 16)
+                cp_async_16(dst + 256u, reinterpret_cast<const void*>(src + 256u));
+        }
+    } else {
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+            const int kk = w4 + 4 * (h + 2 * j);
+            const RowSpan r = unaligned_row_span(base, ld, mn0, k0 + kk, mn_total, k_total);
+            const uintptr_t a16 = r.a - r.d;
+            const uint32_t dst = raw + static_cast<uint32_t>(kk * kRawRowBytes);
+            if (static_cast<uint32_t>(c) < r.pieces)
+                cp_async_16(dst + 16u * c, reinterpret_cast<const void*>(a16 + 16u * c));
+            if (c == 0 && r.pieces > 16)
+                cp_async_16(dst + 256u, reinterpret_cast<const void*>(a16 + 256u));
+        }
+    }
+    cp_async_arrive(bar);
+}
+
+// Move this warp's 16 rows from the raw stage into the swizzled tile at `dst`:
+// lane c of half-warp h takes the 16-byte chunk c (elements mn0 + 8c ..) of
+// rows h, h + 2, ..., h + 14.
+__device__ __forceinline__ void unaligned_rows_place(uint32_t dst, uint32_t raw,
+                                                     const uint16_t* base, int64_t ld, int mn0,
+                                                     int k0, int mn_total, int k_total, int w4,
+                                                     int lane) {
+    const int h = lane >> 4, c = lane & 15;
+    const int n = mn0 + 8 * c;
+    uint32_t keep[4];                              // masks of the elements below MN
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        keep[e] = (n + 2 * e < mn_total ? 0x0000FFFFu : 0u) | (n + 2 * e + 1 < mn_total ? 0xFFFF0000u : 0u);
+    const int kk0 = w4 + 4 * h;                    // rows kk0 + 8 j: same swizzle phase (kk & 7)
+    if (unaligned_stage_interior(base, ld, mn0, k0, k_total)) {
+        const RowSpan r0 = unaligned_row_span(base, ld, mn0, k0 + kk0, mn_total, k_total);
+        const uint32_t d = r0.d;                   // the same for the eight rows
+        const uint32_t src0 = raw + static_cast<uint32_t>(kk0 * kRawRowBytes) + 16u * c + (d & ~3u);
+        const uint32_t dst0 = dst + chunk_offset<true>(kk0, c);
+        const uint32_t sh = 8u * (d & 3u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            // bytes [d + 16c, d + 16c + 16) of the raw row (d even); bytes past the
+            // copied span are masked below
+            const uint32_t src = src0 + static_cast<uint32_t>(j * 8 * kRawRowBytes);
+            uint32_t x[5];
+#pragma unroll
+            for (int t = 0; t < 5; ++t) x[t] = ld_shared_b32(src + 4u * t);
+            uint32_t w[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = __funnelshift_r(x[t], x[t + 1], sh) & keep[t];
+            st_shared_v4_b32(dst0 + static_cast<uint32_t>(j * 8 * 128), make_uint4(w[0], w[1], w[2], w[3]));
+        }
+        return;
+    }
+#pragma unroll 1
+    for (int j = 0; j < 8; ++j) {
+        const int kk = kk0 + 8 * j;
+        const int k = k0 + kk;
+        const RowSpan r = unaligned_row_span(base, ld, mn0, k, mn_total, k_total);
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (r.pieces) {
+            const uint32_t src = raw + static_cast<uint32_t>(kk * kRawRowBytes) + 16u * c + (r.d & ~3u);
+            uint32_t x[5];
+#pragma unroll
+            for (int t = 0; t < 5; ++t) x[t] = ld_shared_b32(src + 4u * t);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) w[t] = __funnelshift_r(x[t], x[t + 1], 8u * (r.d & 3u));
+        } else if (k < k_total) {
+            const uint16_t* row = base + static_cast<int64_t>(k) * ld;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (n + e < mn_total)
+                    w[e >> 1] |= static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row + n + e)))
+                                 << (16 * (e & 1));
+        }
+        st_shared_v4_b32(dst + chunk_offset<true>(kk, c),
+                         make_uint4(w[0] & keep[0], w[1] & keep[1], w[2] & keep[2], w[3] & keep[3]));
     }
 }
 

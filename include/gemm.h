@@ -111,7 +111,9 @@ typedef struct {
     int32_t tiles;        /* work units: output tiles, or stream-K shares for SKINNY */
     int32_t shares;       /* SKINNY: equal contiguous shares of the (tile, K block) iterations;
                              PAIR: shares (one per cluster) of the stream-K phase, 0 = none */
-    int32_t staged;       /* operands copied to 16-byte-aligned rows first: 1 = A, 2 = B, 3 = both */
+    int32_t staged;       /* bit 1: A copied to 16-byte-aligned rows first; bit 2: B copied;
+                             bit 4: B (stored K x N, not 16-byte aligned) read in place by the
+                             SPLIT_PAIR kernel's own copies, no staging pass */
 } gemm_config_t;
 
 /*
@@ -137,7 +139,10 @@ GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t *out, int device);
  * with rows padded to 16 bytes, when it fits (both together when both are),
  * and the tensor-memory-access kernels read the copy; larger ones are read in
  * place by the generic kernel.  Consecutive calls on one plan reuse the buffer
- * in stream order.
+ * in stream order.  A misaligned B too large for the buffer, with an aligned A,
+ * in a problem that goes to the SPLIT_PAIR kernel with 128 x 128 tiles (M >
+ * 64), is read in place by that kernel instead of the generic kernel
+ * (gemm_config_t.staged bit 4; see also gemm_plan_set_staging).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA (launch failure), TIMEOUT (only in
  * debug-sync mode).  Nothing is launched when an error is returned, except
  * for CUDA/TIMEOUT, which report a failure of the launched work itself.
@@ -240,6 +245,17 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  */
 GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
                                        int32_t block_n);
+
+/*
+ * Turn the staging of misaligned operands on (1, the default) or off (0) for
+ * the next gemm_run calls on this plan.  With staging off, an operand whose
+ * base or row pitch is not a multiple of 16 bytes is never copied: a K x N B
+ * with an aligned A in a SPLIT_PAIR-sized problem (M > 64) is read in place by
+ * that kernel, anything else by the generic kernel.  For tests, tuning, and
+ * callers that want no extra pass over their operands.
+ * Errors: INVALID_ARG (null plan, enabled not 0 or 1).
+ */
+GEMM_API gemm_status_t gemm_plan_set_staging(gemm_plan_t plan, int32_t enabled);
 
 /*
  * The scheduler's tile order, evaluated on the host by the same function the

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 SHAPES = [
     (16, 4096, 4864, torch.bfloat16, 0, 0),      # swap-AB stream-K, split tiles
     (4096, 4096, 4096, torch.bfloat16, 0, 0),    # pair tiles with a stream-K phase
-    (1023, 1000, 1029, torch.float16, 0, 0),     # B staged (ldb = 1029 halves)
+    (1023, 640, 1029, torch.float16, 0, 0),      # B staged (ldb = 1029 halves; 10 K blocks)
     (600, 1000, 1104, torch.float16, 3, 0),      # A staged (lda = 1003 halves)
 ]
 

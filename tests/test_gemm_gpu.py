@@ -94,7 +94,7 @@ def test_workload_ragged_f16_full(plan):
     """M=1023 K=1000 N=1029: ldb = 1029 halves is not a 16-byte pitch -> B is staged
     into 16-byte rows and the TMA-fed kernels read the copy: automatically the
     split-K cluster kernel (72 tiles of 128 x 128 on 144 SMs), and the one-CTA
-    kernel when forced."""
+    kernel when forced; with staging off the cluster kernel reads B in place."""
     w = workloads.WORKLOADS["ragged1023x1000x1029_f16"]
     A, B = workloads.make_inputs(w)
     dev = torch.device("cuda:0")
@@ -107,6 +107,13 @@ def test_workload_ragged_f16_full(plan):
     got = run(plan, A, B, w.M, w.N, w.K, kernel=g.GEMM_KERNEL_TMA, expect=g.GEMM_KERNEL_TMA)
     assert_guards(got, w.M, w.N)
     assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " one-CTA tiles")
+    plan.set_staging(False)
+    try:
+        got = run(plan, A, B, w.M, w.N, w.K, expect=g.GEMM_KERNEL_SPLIT_PAIR)
+    finally:
+        plan.set_staging(True)
+    assert_guards(got, w.M, w.N)
+    assert_close(got[:w.M, :w.N], A, B, w.M, w.N, w.K, w.name + " B in place")
 
 
 def test_workload_ragged_f16_generic_in_place(plan):
@@ -535,7 +542,7 @@ def test_ragged_sweep_generic_in_place(plan, M, N, K):
 
 @pytest.mark.parametrize("M,N,K,lda,ldb,staged", [
     (300, 520, 1001, 1001, 520, 1),      # A rows of 1001 halves
-    (300, 517, 1000, 1000, 517, 2),      # B rows of 517 halves
+    (300, 517, 640, 640, 517, 2),        # B rows of 517 halves (10 K blocks: one-CTA tiles)
     (1000, 1300, 777, 779, 1301, 3),     # both, with padding beyond K and N
     (40, 3000, 1003, 1003, 3000, 1),     # skinny M with A staged
 ])
@@ -567,11 +574,83 @@ def test_staged_misaligned_base_and_integer_exact(plan):
 
 
 def test_too_large_to_stage_uses_generic(plan):
-    M, K, N = 200, 4096, 4100
+    # B of 33.6 MB (more than the staging buffer) and 528 tiles (too many for the
+    # split-pair kernel): the generic kernel reads both operands in place.
+    M, K, N = 1100, 4096, 4100
     A, B = workloads.custom(M, K, N, "bf16", seed=3, dist="normal", ldb=4101)
     got = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_GENERIC)
     assert_guards(got, M, N)
     assert_close(got[:M, :N], A, B, M, N, K, "unstaged generic")
+
+
+# ---------------------------------------------------------------- B read in place
+# A K x N B whose base or pitch is not a multiple of 16 bytes, with an aligned
+# A, in a problem the split-pair kernel takes with 128 x 128 tiles, read in
+# place (staging off, or a B too large for the staging buffer): the kernel's
+# four epilogue warps copy each row's 16-byte-aligned span during the K loop
+# and shift it into the swizzled stage.  Pitches with various 2-byte residues
+# modulo 16, bases 1-3 elements past a 16-byte boundary (row 0's aligned span
+# then starts before B: read element by element), K and N not multiples of
+# the tile.
+
+@pytest.mark.parametrize("M,N,K,ldb,b_off", [
+    (1023, 1029, 1000, 1029, 0),         # the ragged workload's shape
+    (300, 517, 1000, 517, 0),
+    (129, 250, 776, 251, 1),             # K = 776, 2000: ragged, with A's pitch aligned
+    (200, 1000, 2000, 1003, 2),
+    (513, 381, 768, 390, 3),
+    (1000, 1000, 4096, 1001, 0),
+    (65, 130, 768, 133, 1),              # one tile row, ragged N
+])
+def test_b_in_place_integer_exact(plan, M, N, K, ldb, b_off):
+    A, B = int_inputs(M, K, N, "f16" if (M + N) % 2 else "bf16", seed=M + N + K + ldb)
+    dev = torch.device("cuda:0")
+    td = A.dtype
+    a = A.to(dev)
+    bbuf = torch.full((K * ldb + b_off + 8,), float("nan"), dtype=td, device=dev)
+    b = bbuf[b_off:b_off + K * ldb].view(K, ldb)
+    b[:, :N].copy_(B.to(dev))
+    cbuf = torch.full((M + 2, N + 3), SENTINEL, dtype=torch.float32, device=dev)
+    plan.set_staging(False)
+    try:
+        cfg = plan.query(a, b, cbuf, M, N, K)
+        assert cfg["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and cfg["staged"] == 4, cfg
+        plan.run(a, b, cbuf, M, N, K)
+        torch.cuda.synchronize()
+    finally:
+        plan.set_staging(True)
+    got = cbuf.cpu().double().numpy()
+    assert_guards(got, M, N)
+    ref = oracle.gemm(A, B)
+    assert np.array_equal(got[:M, :N], ref), f"max diff {np.abs(got[:M, :N] - ref).max()}"
+
+
+def test_b_in_place_large_b_within_tolerance(plan):
+    # B of 35 MB (larger than the staging buffer): read in place, N(0,1) inputs
+    M, K, N = 130, 16000, 1100
+    A, B = workloads.custom(M, K, N, "bf16", seed=7, dist="normal", ldb=1103)
+    got = run(plan, A, B, M, N, K, expect=g.GEMM_KERNEL_SPLIT_PAIR)
+    assert_guards(got, M, N)
+    assert_close(got[:M, :N], A, B, M, N, K, "split pair, B in place")
+
+
+def test_b_in_place_16bit_output(plan):
+    M, K, N = 700, 1000, 517
+    A, B = int_inputs(M, K, N, "bf16", seed=11, ldb=521)
+    dev = torch.device("cuda:0")
+    a, b = A.to(dev), B.to(dev)[:, :N]
+    c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
+    plan.set_staging(False)
+    try:
+        cfg = plan.query_ex(a, b, c)
+        assert cfg["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and cfg["staged"] == 4, cfg
+        plan.run_ex(a, b, c)
+        torch.cuda.synchronize()
+    finally:
+        plan.set_staging(True)
+    ref = oracle.gemm(A[:, :K], B[:, :N])
+    want = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(c.cpu().double().numpy(), want)
 
 
 @pytest.mark.parametrize("M,N,K", [(129, 257, 130), (17, 128, 63), (255, 15, 1000)])
@@ -666,7 +745,7 @@ def test_kernel_selection(plan):
     assert q(8192, 8192, 8192)["block_n"] == 256
     r = q(1023, 1000, 1029)                     # odd ldb: B staged, then TMA-fed split pairs
     assert r["kernel"] == g.GEMM_KERNEL_SPLIT_PAIR and r["staged"] == 2, r
-    r = q(200, 4096, 4100, ldb=4101)            # a 33.6 MB B does not fit the staging buffer
+    r = q(1100, 4096, 4100, ldb=4101)           # a 33.6 MB B does not fit the staging buffer
     assert r["kernel"] == g.GEMM_KERNEL_GENERIC and r["staged"] == 0, r
     s = q(16, 4096, 14336)
     # 56 strips of 256 columns, K halved over the two CTAs of each cluster.

@@ -105,9 +105,43 @@ def test_staging_decisions(model):
     assert r["staged"] == 3 and r["kernel"] != g.GEMM_KERNEL_GENERIC, r
     # a misaligned base pointer is staged too
     assert q(model, 1000, 1000, 1000, a_off=2)["staged"] == 1
-    # a 33.6 MB B does not fit: the generic kernel reads both in place
-    r = q(model, 200, 4100, 4096, ldb=4101)
+    # a 33.6 MB B does not fit, and 528 tiles are too many for the split-pair
+    # kernel: the generic kernel reads both in place
+    r = q(model, 2000, 4100, 4096, ldb=4101)
     assert r["kernel"] == g.GEMM_KERNEL_GENERIC and r["staged"] == 0, r
+    # with 66 tiles the split-pair kernel takes it and reads B in place
+    r = q(model, 200, 4100, 4096, ldb=4101)
+    assert (r["kernel"], r["staged"]) == (g.GEMM_KERNEL_SPLIT_PAIR, 4), r
+    # split-pair-sized problems (M > 64, one wave of 128 x 128 tiles, K >= 768) with
+    # an aligned A: a misaligned B that fits the buffer is staged ...
+    r = q(model, 1000, 1000, 4096, ldb=1001, dtype=g.GEMM_F16)
+    assert (r["kernel"], r["staged"]) == (g.GEMM_KERNEL_SPLIT_PAIR, 2), r
+    # ... one that does not is read in place
+    r = q(model, 300, 1100, 20000, ldb=1103)           # B of 44 MB
+    assert (r["kernel"], r["staged"]) == (g.GEMM_KERNEL_SPLIT_PAIR, 4), r
+    # never with a misaligned A, small M or a transposed B
+    r = q(model, 300, 1100, 20000, lda=20001, ldb=1103)
+    assert r["staged"] & 4 == 0, r
+    assert q(model, 64, 4100, 4096, ldb=4101)["staged"] & 4 == 0
+    r = g.gemm_query_ex(model, g.GEMM_OP_N, g.GEMM_OP_T, A_ADDR, 4096, B_ADDR, 4097, C_ADDR,
+                        1000, g.GEMM_OUT_F32, 1000, 1000, 4096, g.GEMM_BF16)
+    assert r["staged"] & 4 == 0, r
+
+
+def test_staging_off(model):
+    # with staging off nothing is copied: the split-pair kernel reads B in place
+    # where it can, the generic kernel takes the rest
+    assert g.gemm_plan_set_staging(model, 0) == g.GEMM_OK
+    try:
+        r = q(model, 1023, 1029, 1000, dtype=g.GEMM_F16)
+        assert (r["kernel"], r["staged"]) == (g.GEMM_KERNEL_SPLIT_PAIR, 4), r
+        r = q(model, 1000, 1000, 1000, lda=1001, ldb=1003, dtype=g.GEMM_F16)
+        assert (r["kernel"], r["staged"]) == (g.GEMM_KERNEL_GENERIC, 0), r
+    finally:
+        assert g.gemm_plan_set_staging(model, 1) == g.GEMM_OK
+    assert q(model, 1023, 1029, 1000, dtype=g.GEMM_F16)["staged"] == 2
+    assert g.gemm_plan_set_staging(model, 2) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan_set_staging(None, 1) == g.GEMM_ERR_INVALID_ARG
 
 
 def test_forcing(model):
