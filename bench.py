@@ -161,33 +161,23 @@ class ClockSampler:
                 "window": "timed region" if inside else "whole run (no sample inside the timed region)"}
 
 
-def oracle_sample(w, A, B, budget_s: float) -> tuple[int, int, int]:
-    """(rows, cols, threads): a block C[0:rows, 0:cols] of the workload that the
-    oracle, as it stands, computes in about `budget_s` seconds on all host cores.
-    Rows are split across threads, so a sample has at least one row per thread."""
+# The oracle's bounded sample of the headline workload, the same for the CPU
+# baseline leg and every step of the reference arm: whole rows C[0:R, :] of the
+# 8192^3 product (about 4 s of fp64 work on 16 host cores).
+SAMPLE_ROWS = 2048
+
+
+def cpu_baseline(w, A, B, passes: int = 3) -> dict:
+    """The oracle, as it stands, timed on the fixed row sample (`passes` times)."""
     import oracle
     cores = oracle.max_threads()
-    cal_cols = min(w.N, 2048)
+    rows = min(SAMPLE_ROWS, w.M)
+    As = A[:rows]
     t0 = time.perf_counter()
-    oracle.gemm(A[:cores], B, N=cal_cols)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    rate = 2.0 * cores * cal_cols * w.K / dt
-    flops = rate * budget_s
-    cols = int(flops / (2.0 * cores * w.K))
-    if cols >= w.N:
-        rows = int(flops / (2.0 * w.N * w.K)) // cores * cores
-        return max(cores, min(w.M, rows)), w.N, cores
-    return min(cores, w.M), max(16, min(w.N, cols // 16 * 16)), cores
-
-
-def cpu_baseline(w, A, B, budget_s: float = 12.0) -> dict:
-    """The oracle, as it stands, timed on a bounded block of the workload."""
-    import oracle
-    rows, cols, cores = oracle_sample(w, A, B, budget_s)
-    t0 = time.perf_counter()
-    oracle.gemm(A[:rows], B, N=cols)
+    for _ in range(passes):
+        oracle.gemm(As, B)
     dt = time.perf_counter() - t0
-    fl = 2.0 * rows * cols * w.K
+    fl = 2.0 * rows * w.N * w.K * passes
     # the same oracle on one core: whole rows, as many as about 3 s allow
     rate1 = fl / dt / cores
     rows1 = max(1, min(w.M, int(rate1 * 3.0 / (2.0 * w.N * w.K))))
@@ -195,10 +185,18 @@ def cpu_baseline(w, A, B, budget_s: float = 12.0) -> dict:
     oracle.gemm(A[:rows1], B, nthreads=1)
     dt1 = time.perf_counter() - t1
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"C[0:{rows}, 0:{cols}] of {w.name} (K = {w.K}; fp64 i-k-j loop, "
-                      f"{cores} threads), {dt:.1f} s",
+            "sample": f"C[0:{rows}, 0:{w.N}] of {w.name} (K = {w.K}; fp64 i-k-j loop, "
+                      f"{cores} threads), {passes} passes in {dt:.1f} s",
             "one_core": {"value": 2.0 * rows1 * w.N * w.K / dt1 / 1e12, "unit": "TFLOP/s",
                          "cores": 1, "sample": f"C[0:{rows1}, 0:{w.N}] of {w.name}, {dt1:.1f} s"}}
+
+
+def headline_config(w, world: int) -> dict:
+    """The `config` of both arms' JSON lines (identical by construction)."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
+            "dtype_in": "bf16", "output": "fp32", "accumulate": "fp32",
+            "l2": "inputs larger than L2 (A+B = 268 MB > 129 MB), no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -212,26 +210,26 @@ def run_reference(args, rank: int, world: int) -> None:
     import workloads
     w = workloads.WORKLOADS[HEADLINE]
     A, B = workloads.make_inputs(w)
-    budget = 120.0 / max(1, args.steps + args.warmup)
-    rows, cols, cores = oracle_sample(w, A, B, budget)
+    cores = oracle.max_threads()
+    rows = min(SAMPLE_ROWS, w.M)
     As = A[:rows]
     for _ in range(args.warmup):
-        oracle.gemm(As, B, N=cols)
+        oracle.gemm(As, B)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.gemm(As, B, N=cols)
+        oracle.gemm(As, B)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * cols * w.K * args.steps
+    flops = 2.0 * rows * w.N * w.K * args.steps
     v = flops / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1)/sqrt(K) bf16, widened exactly to f64)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
-                   "sample_per_step": f"C[0:{rows}, 0:{cols}]"},
+        "config": headline_config(w, 1),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"C[0:{rows}, 0:{cols}] of {w.name} per step (K = {w.K})"},
+                         "sample": f"C[0:{rows}, 0:{w.N}] of {w.name} per step (K = {w.K}; "
+                                   f"fp64 i-k-j loop, {cores} threads)"},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -336,7 +334,9 @@ def run_ours(args, rank: int, world: int, dist) -> None:
 
     also = {}
     if rank == 0 and not args.quick:
-        also = secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src)
+        also["sustained_" + w.name] = sustained_leg(torch, step, w, stream, peaks, peak_src,
+                                                 args.sustained_s, local)
+        also.update(secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src))
 
     e2e = None
     if not args.no_e2e:
@@ -353,17 +353,76 @@ def run_ours(args, rank: int, world: int, dist) -> None:
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1)/sqrt(K) bf16)",
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
-                       "output": "fp32", "accumulate": "fp32",
-                       "l2": "inputs larger than L2 (A+B = 268 MB > 129 MB), no flush",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "kernel": cfg},
+            "config": headline_config(w, world), "kernel": cfg,
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps, "clocks": clocks, "also": also,
         }
         print(json.dumps(line), flush=True)
+        if also:
+            # The secondary figures again, as one short line that the end of the
+            # output keeps whole.
+            print(json.dumps({"secondary": summary(also)}), flush=True)
     plan.close()
+
+
+def sustained_leg(torch, step, w, stream, peaks, peak_src, seconds, device_index) -> dict:
+    """The headline GEMM back to back for `seconds` (power-capped steady state),
+    with clocks sampled inside the timed region; against the sustained peak."""
+    # one launch's time, to size the run
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(5):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    per = max(e0.elapsed_time(e1) / 5 / 1e3, 1e-5)
+    n = max(10, int(seconds / per))
+    sampler = ClockSampler(device_index)
+    sampler.start()
+    torch.cuda.synchronize()
+    sampler.mark_begin()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    t = e0.elapsed_time(e1) / 1e3
+    tf = w.flops * n / t / 1e12
+    return {"tflops": tf, "launches": n, "seconds": t,
+            "frac_of_sustained_peak": tf / peaks["bf16_tflops_sustained"],
+            "peak": peaks["bf16_tflops_sustained"], "peak_source": f"{peak_src} bf16 sustained",
+            "clocks": clocks}
+
+
+def summary(also: dict) -> dict:
+    """The figures of `also` that carry a target or a comparison, rounded."""
+    r = lambda x, n=1: None if x is None else round(x, n)  # noqa: E731
+    out = {}
+    for k, v in also.items():
+        if k.startswith("sustained_"):
+            c = v.get("clocks") or {}
+            out[k] = {"tflops": r(v["tflops"]), "frac_sustained": r(v["frac_of_sustained_peak"], 3),
+                      "s": r(v["seconds"], 2), "sm_mhz": c.get("sm_mhz"),
+                      "clock_samples": c.get("samples"), "reasons": c.get("reasons")}
+        elif "gbs" in v:
+            out[k] = {"gbs": r(v["gbs"], 0), "pct_hbm": r(v["pct_of_hbm_peak"])}
+            for extra in ("torch_matmul_gbs", "torch_softmax_gbs"):
+                if extra in v:
+                    out[k][extra.split("_")[1]] = r(v[extra], 0)
+        elif "gpu_us_per_launch" in v:
+            out[k] = {"us": r(v["gpu_us_per_launch"], 2), "floor_us": r(v.get("launch_floor_us"), 2),
+                      "roofline_frac": r(v["roofline_frac"], 3), "single_call_us": r(v["single_call_us"])}
+        elif "tflops" in v:
+            out[k] = {"tflops": r(v["tflops"]), "pct_peak": r(v["pct_of_peak"])}
+            for extra in ("torch_matmul_tflops", "torch_sdpa_tflops"):
+                if extra in v:
+                    out[k][extra.split("_")[1]] = r(v[extra])
+    return out
 
 
 def secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> dict:
@@ -482,6 +541,7 @@ def small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> 
     enqueue plus launch latency, from the call until the stream has finished --
     reported separately, as the launch overhead dominates at these sizes."""
     out = {}
+    floors = {}
     for name in ("gemm256_f16", "ragged1023x1000x1029_f16"):
         w = workloads.WORKLOADS[name]
         A, B = workloads.make_inputs(w)
@@ -509,6 +569,28 @@ def small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> 
         torch.cuda.synchronize()
         ms = sorted(e0.elapsed_time(e1) / per_graph for e0, e1 in ev)
         t = ms[len(ms) // 2] / 1e3
+        # The launch floor: a kernel with no work, launched as this GEMM's kernel is
+        # (its grid and cluster size, programmatic dependent launch), in the same
+        # kind of replayed graph.
+        key = (cfg["grid"], cfg["cluster"])
+        if key not in floors:
+            fgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(fgraph):
+                cap = torch.cuda.current_stream()
+                for _ in range(per_graph):
+                    if g.gemm_noop_launch(cfg["grid"], cfg["cluster"], cap.cuda_stream) != 0:
+                        raise RuntimeError("gemm_noop_launch failed")
+            fgraph.replay()
+            torch.cuda.synchronize()
+            fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(15)]
+            for e0, e1 in fev:
+                e0.record()
+                fgraph.replay()
+                e1.record()
+            torch.cuda.synchronize()
+            fms = sorted(e0.elapsed_time(e1) / per_graph for e0, e1 in fev)
+            floors[key] = fms[len(fms) // 2] / 1e3
         # one call at a time: from the call until the stream is idle again
         walls = []
         for _ in range(50):
@@ -522,6 +604,9 @@ def small_secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src) -> 
         out[name] = {"tflops": w.flops / t / 1e12, "gpu_us_per_launch": t * 1e6,
                      "single_call_us": wall * 1e6, "launch_overhead_us": (wall - t) * 1e6,
                      "roofline_us": roof * 1e6, "roofline_frac": roof / t,
+                     "launch_floor_us": floors[key] * 1e6,
+                     "launch_floor": f"graph of {per_graph} empty kernels, grid {key[0]}, "
+                                     f"cluster {key[1]}, programmatic dependent launch",
                      "timing": f"CUDA graph of {per_graph} launches replayed 15 times (median); "
                                "single call = host enqueue to stream idle, median of 50",
                      "kernel": cfg["kernel_name"], "staged": cfg["staged"]}
@@ -707,6 +792,8 @@ def main() -> None:
     ap.add_argument("--case", default=None,
                     help="profiling: run only this workload's GEMM (or softmax) --launches times")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--sustained-s", type=float, default=2.5,
+                    help="seconds of the back-to-back headline leg with clocks inside it")
     args = ap.parse_args()
     if args.case:
         run_case(args)

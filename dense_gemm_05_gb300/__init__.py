@@ -54,7 +54,8 @@ ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_stat
                  "gemm_query", "gemm_plan_set_group", "gemm_plan_force", "gemm_tile_coord",
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
                  "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
-                 "gemm_plan_create_model", "gemm_noop_launch", "gemm_plan_set_staging")
+                 "gemm_plan_create_model", "gemm_noop_launch", "gemm_plan_set_staging",
+                 "gemm_plan_set_debug")
 
 SOFTMAX_PATH_NONE = 0
 SOFTMAX_PATH_WARP = 1
@@ -139,6 +140,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_plan_force.restype = i32
         L.gemm_plan_set_staging.argtypes = [vp, i32]
         L.gemm_plan_set_staging.restype = i32
+        L.gemm_plan_set_debug.argtypes = [vp, i32, ctypes.c_uint64]
+        L.gemm_plan_set_debug.restype = i32
         L.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
                                       ctypes.POINTER(i64)]
         L.gemm_tile_coord.restype = i32
@@ -237,6 +240,12 @@ def gemm_plan_set_group(plan: int, group: int) -> int:
 
 def gemm_plan_force(plan: int, kernel: int = 0, split_k: int = 0, block_n: int = 0) -> int:
     return int(lib().gemm_plan_force(plan, kernel, split_k, block_n))
+
+
+def gemm_plan_set_debug(plan: int, sync: int, timeout_ns: int = 0) -> int:
+    """Debug-sync mode (gemm_run waits and reports device-side give-ups) and the
+    limit of every bounded device wait (0 = the default)."""
+    return int(lib().gemm_plan_set_debug(plan, int(sync), int(timeout_ns)))
 
 
 def gemm_plan_set_staging(plan: int, enabled: bool) -> int:
@@ -359,6 +368,11 @@ class Plan:
         st = gemm_plan_set_group(self.handle, group)
         if st != GEMM_OK:
             raise GemmError(st, "gemm_plan_set_group")
+
+    def set_debug(self, sync: bool, timeout_ns: int = 0):
+        st = gemm_plan_set_debug(self.handle, int(bool(sync)), timeout_ns)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_plan_set_debug")
 
     def set_staging(self, enabled: bool):
         st = gemm_plan_set_staging(self.handle, enabled)

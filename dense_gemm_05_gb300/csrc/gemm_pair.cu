@@ -32,9 +32,9 @@ struct PairCfg {
     static constexpr int kStageBytes = kAStageBytes + kBStageBytes;   // per CTA
     static constexpr int kTmemCols = 2 * BN;                    // two 128 x BN fp32 accumulators
     static constexpr int kThreads = 192;
-    static constexpr int kNumBars = 2 * STAGES + 5;
+    static constexpr int kNumBars = 2 * STAGES + 6;
     static constexpr int kSmemBytes =
-        1024 + STAGES * kStageBytes + kEpiSmemBytes + 8 * kNumBars + 16;
+        1024 + STAGES * kStageBytes + kEpiSmemBytes + 8 * kNumBars + 32;
     static_assert(kBHalf % kSubN == 0, "B half must be whole 64-column sub-tiles");
     static_assert(kSmemBytes <= 232448, "shared memory");
 };
@@ -132,9 +132,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* final_bar = drain + 1;   // after an abort: the last multicast commit of CTA 0
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = abort_flag + 1;   // "this CTA sums a stream-K tile"
+    volatile int* n_issued = last_flag + 1;     // K-block stages this CTA's producer issued
+    volatile int* n_consumed = n_issued + 1;    // CTA 0: stages whose full barrier the MMA passed
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -151,8 +154,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             mbar_init(smem_u32(&tempty[a]), 256u);
         }
         mbar_init(smem_u32(drain), 1u);
+        mbar_init(smem_u32(final_bar), 1u);
         *abort_flag = 0;
         *last_flag = 0;
+        *n_issued = 0;
+        *n_consumed = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -183,6 +189,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
+            int consumed = 0;
             PairWalker walk(p, cid, ncl);
             PairSeg sg;
             while (!failed && walk.next(sg)) {
@@ -198,6 +205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         failed = true;
                         break;
                     }
+                    ++consumed;
                     tc_fence_after();
                     const uint32_t a_base = smem_u32(sA + stage * kAStageBytes);
                     const uint32_t b_base = smem_u32(sB + stage * Cfg::kBStageBytes);
@@ -219,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     acc_phase ^= 1u;
                 }
             }
+            *n_consumed = consumed;
             if (failed) {
                 *abort_flag = 1;
                 if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
@@ -411,6 +420,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             bool failed = false;
             int stage = 0;
             uint32_t phase = 0;
+            int issued = 0;
             PairWalker walk(p, cid, ncl);
             PairSeg sg;
             while (!failed && walk.next(sg)) {
@@ -431,6 +441,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                                             kb * kBK, kBM);
                     load_operand_pair<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb,
                                             b_col, kb * kBK, Cfg::kBHalf);
+                    ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -452,14 +463,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                 }
             }
+            *n_issued = issued;
             if (failed) {
                 *abort_flag = 1;
                 if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
-                // Copies already issued complete on CTA 0's barriers, which this CTA
-                // cannot observe: give them a bounded 2 ms to land before leaving.
-                const uint64_t t0 = global_timer_ns();
-                while (global_timer_ns() - t0 < 2000000ull) {
-                }
             }
         }
         __syncwarp();
@@ -469,7 +476,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (warp >= 1 && warp <= 4 && lane == 0 && p.c_tma) bulk_wait_group0();
     tc_fence_before();
     __syncthreads();
-    cluster_sync();      // neither CTA leaves while its peer may still signal it
+    cluster_sync();      // #1: no role of either CTA issues anything any more
+    // After a wait gave up in either CTA, copies may still be on their way into
+    // both CTAs' shared memory, and those of CTA 1 complete on CTA 0's barriers,
+    // which CTA 1 cannot observe.  CTA 0 therefore brings every stage that either
+    // producer issued but the MMA did not consume to completion -- arming the
+    // ones only CTA 1 issued, cancelling the bytes of CTA 1's half where only
+    // CTA 0 issued -- and waits for each (bounded); the second cluster barrier
+    // then keeps both CTAs until they have landed.  (At most STAGES stages are
+    // outstanding: a producer issues stage i only after the MMA freed i - STAGES.)
+    // Multicast commits of CTA 0's MMA issuer (the empty and tfull arrivals) may
+    // also still be on their way into CTA 1 when a role that waited for them gave
+    // up: a last commit to both CTAs, which arrives after every earlier one, is
+    // waited for by both.
+    const uint32_t peer = rank ^ 1u;
+    if ((leader && warp == 5 && lane == 0) || (warp == 0 && lane == 0)) {
+        const bool any_abort =
+            *abort_flag != 0 ||
+            ld_shared_cluster_s32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), peer)) != 0;
+        if (any_abort && warp == 0) {
+            const volatile int never = 0;
+            if (leader) tc_commit_pair_mc(smem_u32(final_bar), 0x3);
+            mbar_wait(smem_u32(final_bar), 0u, &never, 100000000ull);
+        }
+        if (any_abort && warp == 5) {
+            const int n0 = *n_issued;
+            const int n1 = ld_shared_cluster_s32(mapa_shared(smem_u32(const_cast<int*>(n_issued)), 1));
+            const int c = *n_consumed;
+            const int n = n0 > n1 ? n0 : n1;
+            const volatile int never = 0;
+            for (int i = c; i < n; ++i) {
+                const uint32_t fb = smem_u32(&full[i % STAGES]);
+                if (i >= n0)
+                    mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
+                else if (i >= n1)
+                    mbar_complete_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
+                mbar_wait(fb, static_cast<uint32_t>(i / STAGES) & 1u, &never, 100000000ull);
+            }
+        }
+    }
+    cluster_sync();      // #2: neither CTA leaves while a copy or commit may still land in it
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);

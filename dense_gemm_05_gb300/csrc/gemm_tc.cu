@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
 namespace {
 constexpr int kTmaStages256 = 4;
 constexpr int kTmaStages128 = 6;
+constexpr int kTmaStages64 = 6;
 constexpr int kGenericStages = 4;
 
 template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
@@ -389,15 +390,19 @@ cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap
 
 int tma_smem_bytes(int bn) {
     return bn == 256 ? TcCfg<256, kTmaStages256, false>::kSmemBytes
-                     : TcCfg<128, kTmaStages128, false>::kSmemBytes;
+                     : (bn == 64 ? TcCfg<64, kTmaStages64, false>::kSmemBytes
+                                 : TcCfg<128, kTmaStages128, false>::kSmemBytes);
 }
 
-int tma_stages(int bn) { return bn == 256 ? kTmaStages256 : kTmaStages128; }
+int tma_stages(int bn) {
+    return bn == 256 ? kTmaStages256 : (bn == 64 ? kTmaStages64 : kTmaStages128);
+}
 
 cudaError_t tma_prepare() {
     cudaError_t e = set_attrs<256, kTmaStages256, false>();
-    if (e != cudaSuccess) return e;
-    return set_attrs<128, kTmaStages128, false>();
+    if (e == cudaSuccess) e = set_attrs<128, kTmaStages128, false>();
+    if (e == cudaSuccess) e = set_attrs<64, kTmaStages64, false>();
+    return e;
 }
 
 cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
@@ -406,6 +411,9 @@ cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
     if (bn == 256)
         return launch<256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
                                                  stream);
+    if (bn == 64)
+        return launch<64, kTmaStages64, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                               stream);
     return launch<128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
                                              stream);
 }

@@ -28,6 +28,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Count `bytes` as arrived on the barrier's transaction count (for bytes that
+// were announced with expect_tx but will never be copied).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -44,11 +51,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, suspending the thread (while the phase is incomplete) for at
+// most about `hint_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// Longest suspension of one poll of a bounded wait, and how many polls pass
+// between checks of the clock and the abort flag: a wait gives up at most a few
+// microseconds after its limit, so limits far below a kernel's run time work.
+constexpr uint32_t kPollSuspendNs = 1000;
+constexpr uint32_t kPollCheckMask = 3;
 
 // Bounded wait for the completion of the barrier phase with parity `parity`.
 // Gives up (returns false) when `abort_flag` becomes non-zero, after
@@ -56,11 +83,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // comes first, so no wait can spin forever.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort_flag, uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, kPollSuspendNs)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 127u) == 0u) {
+        if (mbar_try_wait_hint(bar, parity, kPollSuspendNs)) return true;
+        if ((it & kPollCheckMask) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) return false;
         }
@@ -422,6 +449,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
+// 32-bit load from the shared memory of a CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ int ld_shared_cluster_s32(uint32_t cluster_addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 // 16-byte store into the shared memory of a CTA of the cluster (address from mapa_shared).
 __device__ __forceinline__ void st_cluster_v4_b32(uint32_t cluster_addr, uint4 v) {
     asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr),
@@ -470,16 +504,29 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_try_wait_acq_cluster_hint(uint32_t bar, uint32_t parity,
+                                                               uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait (as mbar_wait) whose completion also acquires what other CTAs
 // of the cluster released when they arrived.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort_flag,
                                                   uint64_t timeout_ns) {
-    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    if (mbar_try_wait_acq_cluster_hint(bar, parity, kPollSuspendNs)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-        if ((it & 127u) == 0u) {
+        if (mbar_try_wait_acq_cluster_hint(bar, parity, kPollSuspendNs)) return true;
+        if ((it & kPollCheckMask) == 0u) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) return false;
         }

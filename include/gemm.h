@@ -122,8 +122,10 @@ typedef struct {
  * count, sets kernel attributes and allocates the plan's workspace (64 MiB of
  * split-K / stream-K partials, tile counters, a status word) and its 32 MiB
  * staging buffer.
- * Errors: INVALID_ARG (out == NULL), UNSUPPORTED (not sm_103), CUDA, OOM.
- * On error *out is set to NULL.
+ * Errors: INVALID_ARG (out == NULL), UNSUPPORTED (not sm_103), CUDA, OOM (an
+ * allocation failed; whatever was allocated is freed again).  On error *out is
+ * set to NULL.  For tests, GEMM_TEST_FAIL_ALLOC=k in the environment makes the
+ * k-th of the four allocations fail as if the device were out of memory.
  */
 GEMM_API gemm_status_t gemm_plan_create(gemm_plan_t *out, int device);
 
@@ -245,6 +247,22 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  */
 GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
                                        int32_t block_n);
+
+/*
+ * Debug settings of the plan's next gemm_run calls.  sync = 1: gemm_run waits
+ * for its kernels and returns GEMM_ERR_TIMEOUT when a bounded device-side wait
+ * gave up (the device status word is then cleared, and so are the plan's tile
+ * counters, which a kernel that stopped early may leave non-zero); sync = 0:
+ * no waiting (the default, unless GEMM_DEBUG_SYNC=1 was set when the plan was
+ * created).  timeout_ns: the limit of every bounded wait in the kernels, 0 =
+ * the default of 2 s (GEMM_WAIT_TIMEOUT_MS at plan creation also sets it).  A
+ * wait that gives up stops its CTA and the others it works with after their
+ * copies and MMAs in flight have landed; C is then incomplete.  A limit far
+ * below a kernel's run time makes real launches give up: the tests use that to
+ * exercise the path, and the context stays usable afterwards.
+ * Errors: INVALID_ARG (null plan, sync not 0 or 1).
+ */
+GEMM_API gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint64_t timeout_ns);
 
 /*
  * Turn the staging of misaligned operands on (1, the default) or off (0) for

@@ -761,7 +761,7 @@ def test_kernel_selection(plan):
                             ((1536, 1536, 1536), g.GEMM_KERNEL_TMA, 128),
                             ((128, 8192, 8192), g.GEMM_KERNEL_SPLIT_PAIR, 128),
                             ((1024, 8192, 1024), g.GEMM_KERNEL_SPLIT_PAIR, 128),
-                            ((1024, 512, 1024), g.GEMM_KERNEL_TMA, 128)]:
+                            ((1024, 512, 1024), g.GEMM_KERNEL_TMA, 64)]:
         r = q(*shape)
         assert r["kernel"] == kern and r["block_n"] == bn, (shape, r)
     assert q(4096, 1024, 4096)["shares"] == 0       # 16 K blocks: no stream-K phase

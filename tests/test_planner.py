@@ -43,8 +43,8 @@ def test_the_five_workloads(model):
     r = q(model, 16, 14336, 4096)
     assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["split_k"], r["tiles"]) == \
         (g.GEMM_KERNEL_SPLIT_PAIR, 16, 256, 112, 2, 56), r
-    r = q(model, 256, 256, 256, dtype=g.GEMM_F16)
-    assert (r["kernel"], r["block_n"], r["grid"], r["tiles"]) == (g.GEMM_KERNEL_TMA, 128, 4, 4), r
+    r = q(model, 256, 256, 256, dtype=g.GEMM_F16)       # 128 x 64 tiles: 8 CTAs
+    assert (r["kernel"], r["block_n"], r["grid"], r["tiles"]) == (g.GEMM_KERNEL_TMA, 64, 8, 8), r
     r = q(model, 1023, 1029, 1000, dtype=g.GEMM_F16)      # tight pitches: ldb = 1029 halves
     assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["staged"]) == \
         (g.GEMM_KERNEL_SPLIT_PAIR, 128, 128, 144, 2), r
