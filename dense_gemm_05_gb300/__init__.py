@@ -55,7 +55,11 @@ ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_stat
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
                  "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
                  "gemm_plan_create_model", "gemm_noop_launch", "gemm_plan_set_staging",
-                 "gemm_plan_set_debug")
+                 "gemm_plan_set_debug", "gemm_partition", "gemm_run_slice")
+
+GEMM_SPLIT_AUTO = -1
+GEMM_SPLIT_M = 0
+GEMM_SPLIT_N = 1
 
 SOFTMAX_PATH_NONE = 0
 SOFTMAX_PATH_WARP = 1
@@ -84,6 +88,15 @@ class GemmConfig(ctypes.Structure):
         d = {n: int(getattr(self, n)) for n, _ in self._fields_}
         d["kernel_name"] = KERNEL_NAMES.get(d["kernel"], "?")
         return d
+
+
+class GemmSlice(ctypes.Structure):
+    _fields_ = [("axis", ctypes.c_int32), ("rank", ctypes.c_int32), ("world", ctypes.c_int32),
+                ("row0", ctypes.c_int64), ("rows", ctypes.c_int64),
+                ("col0", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
 
 
 class SoftmaxConfig(ctypes.Structure):
@@ -142,6 +155,11 @@ def lib() -> ctypes.CDLL:
         L.gemm_plan_set_staging.restype = i32
         L.gemm_plan_set_debug.argtypes = [vp, i32, ctypes.c_uint64]
         L.gemm_plan_set_debug.restype = i32
+        L.gemm_partition.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(GemmSlice)]
+        L.gemm_partition.restype = i32
+        L.gemm_run_slice.argtypes = [vp, ctypes.POINTER(GemmSlice), vp, i64, vp, i64, vp, i64,
+                                     i64, i64, i64, i32, vp]
+        L.gemm_run_slice.restype = i32
         L.gemm_tile_coord.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64),
                                       ctypes.POINTER(i64)]
         L.gemm_tile_coord.restype = i32
@@ -246,6 +264,24 @@ def gemm_plan_set_debug(plan: int, sync: int, timeout_ns: int = 0) -> int:
     """Debug-sync mode (gemm_run waits and reports device-side give-ups) and the
     limit of every bounded device wait (0 = the default)."""
     return int(lib().gemm_plan_set_debug(plan, int(sync), int(timeout_ns)))
+
+
+def gemm_partition(M: int, N: int, K: int, world: int, rank: int,
+                   axis: int = GEMM_SPLIT_AUTO) -> dict:
+    """The slice of C = A @ B (rows or columns) that `rank` of `world` computes."""
+    sl = GemmSlice()
+    st = lib().gemm_partition(M, N, K, world, rank, axis, ctypes.byref(sl))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_partition")
+    return sl.as_dict()
+
+
+def gemm_run_slice(plan: int, sl: dict, A: int, lda: int, B: int, ldb: int, C: int, ldc: int,
+                   M: int, N: int, K: int, dtype: int, stream: int = 0) -> int:
+    """One slice of C = A @ B on the whole matrices' layouts (raw pointers); returns the status."""
+    s = GemmSlice(**sl)
+    return int(lib().gemm_run_slice(plan, ctypes.byref(s), A, lda, B, ldb, C, ldc, M, N, K,
+                                    dtype, stream))
 
 
 def gemm_plan_set_staging(plan: int, enabled: bool) -> int:
@@ -433,6 +469,20 @@ class Plan:
         return gemm_query_ex(self.handle, op_a, op_b, a.data_ptr(), lda, b.data_ptr(), ldb,
                              c.data_ptr(), _ld(c), _out_code(c), M, N, K, _dtype_code(a))
 
+    def run_slice(self, a, b, c, sl: dict, stream=None) -> None:
+        """The slice `sl` (from gemm_partition) of c = a @ b, all three the whole
+        matrices (row-major fp16/bf16 a, b; fp32 c); raises GemmError on failure."""
+        import torch
+        if a.dtype != b.dtype:
+            raise TypeError("A and B must have the same dtype")
+        M, K = a.shape
+        N = b.shape[1]
+        s = (torch.cuda.current_stream(a.device) if stream is None else stream).cuda_stream
+        st = gemm_run_slice(self.handle, sl, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                            c.data_ptr(), _ld(c), M, N, K, _dtype_code(a), s)
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_run_slice")
+
     def matmul(self, a, b, out_dtype=None):
         """C = a @ b (fp32 by default); a and b may be transposed views."""
         import torch
@@ -511,4 +561,27 @@ def attention(q, k, v, causal: bool = False, out=None, out_dtype=None, stream=No
                        hs, ldo, hso, int(bool(causal)), _dtype_code(q), _out_code(out), s)
     if st != GEMM_OK:
         raise GemmError(st, "attention_fwd")
+    return out
+
+
+def gather_c(c_local, M: int, N: int, K: int, axis: int = GEMM_SPLIT_AUTO, group=None):
+    """All of C on every rank, from each rank's slice `c_local` (rows x cols of
+    its gemm_partition slice, any device torch.distributed's backend handles):
+    the slices are padded to the largest one, all-gathered, and placed.  This is
+    the one collective of the partitioned GEMM, and only for callers that need
+    all of C on every device; the slices themselves need no exchange."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    slices = [gemm_partition(M, N, K, world, r, axis) for r in range(world)]
+    rows = max(sl["rows"] for sl in slices)
+    cols = max(sl["cols"] for sl in slices)
+    padded = torch.zeros(rows, cols, dtype=c_local.dtype, device=c_local.device)
+    padded[:c_local.shape[0], :c_local.shape[1]] = c_local
+    parts = [torch.empty_like(padded) for _ in range(world)]
+    dist.all_gather(parts, padded, group=group)
+    out = torch.empty(M, N, dtype=c_local.dtype, device=c_local.device)
+    for sl, part in zip(slices, parts):
+        out[sl["row0"]:sl["row0"] + sl["rows"], sl["col0"]:sl["col0"] + sl["cols"]] = \
+            part[:sl["rows"], :sl["cols"]]
     return out

@@ -1066,6 +1066,60 @@ gemm_status_t gemm_run_ex(gemm_plan_t plan, gemm_op_t op_a, gemm_op_t op_b, cons
     return run_impl(plan, a, reinterpret_cast<cudaStream_t>(stream_handle));
 }
 
+gemm_status_t gemm_partition(int64_t M, int64_t N, int64_t K, int32_t world, int32_t rank,
+                             int32_t axis, gemm_slice_t* out) {
+    if (out == nullptr || M < 0 || N < 0 || K < 0 || world < 1 || rank < 0 || rank >= world)
+        return GEMM_ERR_INVALID_ARG;
+    if (axis != GEMM_SPLIT_AUTO && axis != GEMM_SPLIT_M && axis != GEMM_SPLIT_N)
+        return GEMM_ERR_INVALID_ARG;
+    if (axis == GEMM_SPLIT_AUTO) axis = M <= 64 ? GEMM_SPLIT_N : GEMM_SPLIT_M;
+    constexpr int64_t kUnit = 128;
+    const int64_t extent = axis == GEMM_SPLIT_M ? M : N;
+    const int64_t units = cdiv(extent, kUnit);
+    const int64_t u0 = static_cast<int64_t>(rank) * units / world;
+    const int64_t u1 = static_cast<int64_t>(rank + 1) * units / world;
+    const int64_t lo = std::min(extent, u0 * kUnit), hi = std::min(extent, u1 * kUnit);
+    gemm_slice_t sl{};
+    sl.axis = axis;
+    sl.rank = rank;
+    sl.world = world;
+    if (axis == GEMM_SPLIT_M) {
+        sl.row0 = lo;
+        sl.rows = hi - lo;
+        sl.col0 = 0;
+        sl.cols = N;
+    } else {
+        sl.row0 = 0;
+        sl.rows = M;
+        sl.col0 = lo;
+        sl.cols = hi - lo;
+    }
+    *out = sl;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run_slice(gemm_plan_t plan, const gemm_slice_t* slice, const void* A,
+                             int64_t lda, const void* B, int64_t ldb, float* C, int64_t ldc,
+                             int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                             struct CUstream_st* stream_handle) {
+    if (plan == nullptr || slice == nullptr) return GEMM_ERR_INVALID_ARG;
+    const gemm_slice_t& sl = *slice;
+    if ((sl.axis != GEMM_SPLIT_M && sl.axis != GEMM_SPLIT_N) || sl.row0 < 0 || sl.rows < 0 ||
+        sl.col0 < 0 || sl.cols < 0 || M < 0 || N < 0 || sl.row0 > M || sl.col0 > N ||
+        sl.rows > M - sl.row0 || sl.cols > N - sl.col0)
+        return GEMM_ERR_INVALID_ARG;
+    // The whole problem's arguments must be valid on their own.
+    const Args whole{A, lda, B, ldb, C, ldc, M, N, K, dtype};
+    gemm_status_t st = check_args(whole);
+    if (st != GEMM_OK) return st;
+    if (sl.rows == 0 || sl.cols == 0) return GEMM_OK;
+    const auto* a16 = static_cast<const uint16_t*>(A);
+    const auto* b16 = static_cast<const uint16_t*>(B);
+    const Args part{K == 0 ? A : a16 + sl.row0 * lda, lda, K == 0 ? B : b16 + sl.col0, ldb,
+                    C + sl.row0 * ldc + sl.col0, ldc, sl.rows, sl.cols, K, dtype};
+    return run_impl(plan, part, reinterpret_cast<cudaStream_t>(stream_handle));
+}
+
 gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_st* stream_handle) {
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
     int* d = nullptr;

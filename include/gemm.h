@@ -257,9 +257,11 @@ GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t
  * created).  timeout_ns: the limit of every bounded wait in the kernels, 0 =
  * the default of 2 s (GEMM_WAIT_TIMEOUT_MS at plan creation also sets it).  A
  * wait that gives up stops its CTA and the others it works with after their
- * copies and MMAs in flight have landed; C is then incomplete.  A limit far
- * below a kernel's run time makes real launches give up: the tests use that to
- * exercise the path, and the context stays usable afterwards.
+ * copies and MMAs in flight have landed; C is then incomplete.  A wait gives
+ * up a few to a few tens of microseconds after its limit (its polls suspend
+ * the thread for up to about a microsecond each, on the hardware's schedule).
+ * A limit far below a kernel's run time makes real launches give up: the
+ * tests use that to exercise the path, and the context stays usable afterwards.
  * Errors: INVALID_ARG (null plan, sync not 0 or 1).
  */
 GEMM_API gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint64_t timeout_ns);
@@ -307,6 +309,63 @@ GEMM_API gemm_status_t gemm_wait_selftest(uint32_t timeout_us, struct CUstream_s
  * multiple of cluster), CUDA (launch failure).
  */
 GEMM_API gemm_status_t gemm_noop_launch(int32_t grid, int32_t cluster, struct CUstream_st *stream);
+
+/*
+ * ---------------------------------------------------------------- partitioned GEMM
+ * C = A @ B split over `world` devices by output rows or columns, the "rank
+ * offset" of "How to hand-write Triton kernels for matmul and Flash Attention"
+ * (engineering advice: each device takes different output blocks).  The
+ * slices need no exchange of data to compute: by rows, rank r multiplies its
+ * rows of A by all of B into its rows of C; by columns, all of A by its
+ * columns of B into its columns of C.  (Gathering C onto every device, where
+ * that is wanted, is the caller's collective; the Python binding has one.)
+ */
+typedef enum {
+    GEMM_SPLIT_AUTO = -1,   /* rows, or columns when M <= 64 (B is then the large operand) */
+    GEMM_SPLIT_M = 0,       /* rows of A and C */
+    GEMM_SPLIT_N = 1        /* columns of B and C */
+} gemm_split_t;
+
+typedef struct {
+    int32_t axis;           /* GEMM_SPLIT_M or GEMM_SPLIT_N */
+    int32_t rank, world;
+    int64_t row0, rows;     /* rows [row0, row0 + rows) of A and C */
+    int64_t col0, cols;     /* columns [col0, col0 + cols) of B and C */
+} gemm_slice_t;
+
+/*
+ * The slice of the M x N output that rank `rank` of `world` computes: the
+ * split axis is cut into units of 128 (the kernels' tile edge), U units in
+ * all, and rank r takes units [floor(r U / world), floor((r + 1) U / world)),
+ * clipped to the matrix -- contiguous, disjoint, in rank order, covering the
+ * axis, their sizes differing by at most one unit, every boundary but the
+ * matrix's end a multiple of 128 (so operand offsets keep their alignment).
+ * A rank may get an empty slice (rows or cols 0) when U < world.  The other
+ * axis is whole.  Pure host arithmetic; no device is touched.
+ * Errors: INVALID_ARG (null out, negative sizes, world < 1, rank outside
+ * [0, world), unknown axis).
+ */
+GEMM_API gemm_status_t gemm_partition(int64_t M, int64_t N, int64_t K, int32_t world,
+                                      int32_t rank, int32_t axis, gemm_slice_t *out);
+
+/*
+ * Compute one slice of C = A @ B: C[row0 : row0 + rows, col0 : col0 + cols] =
+ * A[row0 : row0 + rows, :] @ B[:, col0 : col0 + cols], with A, B and C given
+ * as the whole matrices' layouts (the pointers and leading dimensions of
+ * gemm_run; the slice must lie inside M x N).  It is gemm_run on the offset
+ * pointers, with the same asynchrony, ownership and errors; an empty slice is
+ * a no-op.  Running every rank's slice (on one device one after another, or on
+ * each rank's own device with its own copies) writes all of C, bit for bit as
+ * one gemm_run would where the kernel choice is the same.
+ * Errors: INVALID_ARG (null plan or slice, a slice outside M x N or with an
+ * unknown axis) and those of gemm_run.
+ */
+GEMM_API gemm_status_t gemm_run_slice(gemm_plan_t plan, const gemm_slice_t *slice,
+                                      const void *A, int64_t lda,
+                                      const void *B, int64_t ldb,
+                                      float *C, int64_t ldc,
+                                      int64_t M, int64_t N, int64_t K,
+                                      gemm_dtype_t dtype, struct CUstream_st *stream);
 
 /*
  * gemm_run_noalloc -- C = A @ B for small M without a plan and without any
