@@ -3,7 +3,10 @@
 Argument marshalling only: every step of ``C = A @ B`` runs in the CUDA
 kernels of ``_build/libgemm.so``.  PyTorch supplies device memory and streams.
 There is no fallback: if the library has not been built, importing the
-binding functions raises.
+binding functions raises.  With ``DG_GEMM_CHECKED=1`` in the environment the
+binding loads (and ``build()`` makes) the checked build
+``_build/libgemm_checked.so`` instead: the same ABI, with every ordinary
+global access of the kernels tested against its matrix (``include/gemm.h``).
 
     plan = gemm_plan_create(0)
     gemm_run(plan, A.data_ptr(), lda, B.data_ptr(), ldb, C.data_ptr(), ldc, M, N, K,
@@ -19,7 +22,25 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH, build  # noqa: F401  (re-exported for __graft_entry__)
+from .build import CHECKED_LIB_PATH, LIB_PATH, build_all  # noqa: F401  (for __graft_entry__)
+from .build import build as _build_one
+
+
+def checked_requested() -> bool:
+    """Whether DG_GEMM_CHECKED=1 asks for the checked build."""
+    v = os.environ.get("DG_GEMM_CHECKED", "")
+    return v not in ("", "0")
+
+
+def lib_path() -> str:
+    return CHECKED_LIB_PATH if checked_requested() else LIB_PATH
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          checked: bool | None = None) -> str:
+    """Build the library the binding loads (the checked one under DG_GEMM_CHECKED=1)."""
+    return _build_one(force, verbose, ptxas_info,
+                      checked_requested() if checked is None else checked)
 
 GEMM_F16 = 0
 GEMM_BF16 = 1
@@ -30,6 +51,7 @@ GEMM_ERR_UNSUPPORTED = 2
 GEMM_ERR_CUDA = 3
 GEMM_ERR_OOM = 4
 GEMM_ERR_TIMEOUT = 5
+GEMM_ERR_BOUNDS = 6
 
 GEMM_OP_N = 0
 GEMM_OP_T = 1
@@ -55,7 +77,8 @@ ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_stat
                  "gemm_wait_selftest", "gemm_run_noalloc", "gemm_run_ex", "gemm_query_ex",
                  "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
                  "gemm_plan_create_model", "gemm_noop_launch", "gemm_plan_set_staging",
-                 "gemm_plan_set_debug", "gemm_partition", "gemm_run_slice")
+                 "gemm_plan_set_debug", "gemm_partition", "gemm_run_slice",
+                 "gemm_build_checked", "gemm_plan_device_status")
 
 GEMM_SPLIT_AUTO = -1
 GEMM_SPLIT_M = 0
@@ -128,11 +151,12 @@ def lib() -> ctypes.CDLL:
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(LIB_PATH):
+        path = lib_path()
+        if not os.path.exists(path):
             raise RuntimeError(
-                f"{LIB_PATH} is missing: run dense_gemm_05_gb300.build() (or "
+                f"{path} is missing: run dense_gemm_05_gb300.build() (or "
                 "__graft_entry__.build()) first; there is no fallback implementation")
-        L = ctypes.CDLL(LIB_PATH)
+        L = ctypes.CDLL(path)
         vp, i64, i32, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32
         L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), ctypes.c_int]
         L.gemm_plan_create.restype = i32
@@ -155,6 +179,10 @@ def lib() -> ctypes.CDLL:
         L.gemm_plan_set_staging.restype = i32
         L.gemm_plan_set_debug.argtypes = [vp, i32, ctypes.c_uint64]
         L.gemm_plan_set_debug.restype = i32
+        L.gemm_build_checked.argtypes = []
+        L.gemm_build_checked.restype = i32
+        L.gemm_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+        L.gemm_plan_device_status.restype = i32
         L.gemm_partition.argtypes = [i64, i64, i64, i32, i32, i32, ctypes.POINTER(GemmSlice)]
         L.gemm_partition.restype = i32
         L.gemm_run_slice.argtypes = [vp, ctypes.POINTER(GemmSlice), vp, i64, vp, i64, vp, i64,
@@ -264,6 +292,20 @@ def gemm_plan_set_debug(plan: int, sync: int, timeout_ns: int = 0) -> int:
     """Debug-sync mode (gemm_run waits and reports device-side give-ups) and the
     limit of every bounded device wait (0 = the default)."""
     return int(lib().gemm_plan_set_debug(plan, int(sync), int(timeout_ns)))
+
+
+def gemm_build_checked() -> int:
+    """1 when the loaded library is the checked build."""
+    return int(lib().gemm_build_checked())
+
+
+def gemm_plan_device_status(plan: int) -> int:
+    """The device status word the plan's last debug-sync gemm_run read."""
+    w = ctypes.c_int32(0)
+    st = int(lib().gemm_plan_device_status(plan, ctypes.byref(w)))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan_device_status")
+    return int(w.value)
 
 
 def gemm_partition(M: int, N: int, K: int, world: int, rank: int,
@@ -409,6 +451,9 @@ class Plan:
         st = gemm_plan_set_debug(self.handle, int(bool(sync)), timeout_ns)
         if st != GEMM_OK:
             raise GemmError(st, "gemm_plan_set_debug")
+
+    def device_status(self) -> int:
+        return gemm_plan_device_status(self.handle)
 
     def set_staging(self, enabled: bool):
         st = gemm_plan_set_staging(self.handle, enabled)

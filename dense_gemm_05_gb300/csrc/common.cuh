@@ -15,8 +15,51 @@ constexpr int kAStageBytes = kBM * kBK * 2;
 constexpr int kSubN = 64;                // columns of one MN-major swizzle sub-tile (128 B)
 constexpr int kSubTileBytes = kSubN * kBK * 2;   // 8 KB: 64 K-rows of 128 B
 
-// Status word written by a kernel whose bounded wait gave up.
+// Status word bits.  kDevTimeout: a bounded wait gave up.  kDevBounds: a
+// checked build (below) skipped an access outside its matrix or buffer; the
+// kChk* bits say which kind of access it was.
 constexpr int kDevTimeout = 1;
+constexpr int kDevBounds = 2;
+constexpr int kChkC = 1 << 8;         // a store of C outside rows [0, M) x columns [0, N)
+constexpr int kChkA = 1 << 9;         // a load of A outside its stored rectangle
+constexpr int kChkB = 1 << 10;        // a load of B outside its stored rectangle
+constexpr int kChkWs = 1 << 11;       // a partial-sum access outside the plan's workspace
+constexpr int kChkCounter = 1 << 12;  // a tile-counter access outside the counter array
+constexpr int kChkStage = 1 << 13;    // the staging copy outside its source or destination
+
+// Checked builds.  Compiled with DG_CHECKED=1 (the library libgemm_checked.so),
+// every ordinary global load and store of the kernels first tests the range it
+// touches against the matrix or buffer it belongs to -- the rectangle of rows x
+// columns the caller passed, or the plan's workspace -- and is skipped when the
+// test fails, which sets kDevBounds and the access's bit in the status word (a
+// debug-sync gemm_run reports it).  TMA copies are not tested: their tensor
+// maps bound them in hardware (elements outside read as zeros, stores are
+// clipped).  In the normal build the tests are the constant true.
+#ifndef DG_CHECKED
+#define DG_CHECKED 0
+#endif
+
+// Elements [c, c + n) of row r lie inside a rows x cols rectangle (n >= 1).
+__host__ __device__ __forceinline__ bool span_inside(int64_t r, int64_t c, int64_t n, int64_t rows,
+                                                     int64_t cols) {
+    return r >= 0 && r < rows && c >= 0 && n >= 1 && c <= cols - n;
+}
+
+// Bytes [a, a + n) lie inside [lo, hi).
+__host__ __device__ __forceinline__ bool bytes_inside(uintptr_t a, uintptr_t n, uintptr_t lo,
+                                                      uintptr_t hi) {
+    return a >= lo && a <= hi && n <= hi - a;
+}
+
+#if DG_CHECKED
+__device__ __forceinline__ bool check_record(int* status, int kind, bool ok) {
+    if (!ok && status != nullptr) atomicOr(status, kDevBounds | kind);
+    return ok;
+}
+#define DG_CHECK(status, kind, cond) ::dg::check_record((status), (kind), (cond))
+#else
+#define DG_CHECK(status, kind, cond) true
+#endif
 
 struct Params {
     const uint16_t* A;
@@ -34,9 +77,11 @@ struct Params {
     int32_t c_vec;          // 16-byte vector stores of C are legal
     int32_t c_tma;          // the epilogue writes C with TMA stores (mapC is valid)
     int32_t prefetch_kb;    // split pair, skinny: K blocks per CTA warmed in L2 before the grid wait
-    float* ws;              // skinny: split-K partial sums
-    int* counters;          // skinny: per-tile arrival counters (zero between launches)
-    int* status;            // device error word (kDevTimeout on a wait that gave up)
+    float* ws;              // skinny, pair: split-K partial sums
+    int* counters;          // skinny, pair: per-tile arrival counters (zero between launches)
+    int64_t ws_len;         // floats at ws (the range a checked build tests against)
+    int64_t counters_len;   // ints at counters
+    int* status;            // device error word (kDev* bits)
     uint64_t timeout_ns;    // limit of every device-side wait
 };
 
@@ -209,7 +254,8 @@ cudaError_t launch_splitpair(int ms, int bn, bool b_mn, bool b_gen, const CUtens
 // Copy a rows x cols 16-bit matrix (pitch lds) into dst with pitch ldd (a multiple
 // of 8 elements, dst 16-byte aligned), zero-filling columns [cols, ldd).
 cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
-                              int64_t rows, int64_t cols, int num_sms, cudaStream_t stream);
+                              int64_t rows, int64_t cols, int* status, int num_sms,
+                              cudaStream_t stream);
 
 // Wait self-test: one block waits on a barrier nobody completes.
 cudaError_t launch_wait_selftest(int* out, uint64_t timeout_ns, cudaStream_t stream);

@@ -49,6 +49,7 @@ struct gemm_plan_s {
     int pair_clusters[2] = {0, 0};   // co-resident 2-CTA clusters for pair tiles of 128 / 256
     int splitpair_clusters = 0;         // co-resident 2-CTA clusters of the small-M cluster kernel
     bool debug_sync = false;
+    int last_device_status = 0;      // status word seen by the last debug-sync gemm_run
     bool model = false;              // a device model for gemm_query only (no device, no memory)
     uint64_t timeout_ns = 2000000000ull;   // limit of every bounded device-side wait
 };
@@ -523,18 +524,24 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c, bool b_g
         const int ncl = c->units < clusters ? c->units : clusters;
         c->grid = 2 * ncl;
         // Stream-K phase: when the last wave of tiles leaves at least half of the
-        // clusters idle, that partial wave is cut into one equal K share per
-        // cluster, taken first; the rest are whole tiles.  A wave that is more than
-        // half full costs less idle time than the split's slower streaming and
-        // fix-ups, and with fewer than two full waves the fix-ups have too little
-        // whole-tile work to hide behind (both measured).  If the shares would be
+        // clusters idle (or at least 30% of them, behind five or more full waves),
+        // that partial wave is cut into one equal K share per cluster, taken first;
+        // the rest are whole tiles.  A fuller last wave costs less idle time than
+        // the split's slower streaming and fix-ups, and with few full waves the
+        // fix-ups have too little whole-tile work to hide behind (all measured:
+        // 6144^3, 58% full behind 7 waves, gains 1.5%; 3584^3, 58% behind 2,
+        // loses 11%; 5376^3, 80% behind 5, loses 0.7%).  If the shares would be
         // shorter than kPairMinShareKb K blocks, one full wave joins the split
         // tiles.  Also skipped when the partial tiles would not fit the workspace,
         // with fewer than kPairMinSkKb K blocks per tile (the fix-ups then cost
         // more than the idle time they save; measured at K = 1024), or when
         // forced off (split_k = 1).
-        if (plan->force_split != 1 && units % ncl != 0 && 2 * (units % ncl) <= ncl &&
-            units / ncl >= 2 && c->num_kb >= kPairMinSkKb) {
+        // split_k = 3 forces the phase for any partial last wave (tuning).
+        const bool sk_forced = plan->force_split == 3;
+        const int64_t rem = units % ncl, waves = units / ncl;
+        const bool sk_pays = (2 * rem <= ncl && waves >= 2) || (10 * rem <= 7 * ncl && waves >= 5);
+        if (plan->force_split != 1 && rem != 0 && (sk_forced || sk_pays) &&
+            c->num_kb >= kPairMinSkKb) {
             int64_t sk = units % ncl;
             if (sk * c->num_kb / ncl < kPairMinShareKb) sk += ncl;
             const int64_t share_kb = sk * c->num_kb / ncl;
@@ -658,6 +665,7 @@ const char* gemm_status_string(gemm_status_t s) {
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
         case GEMM_ERR_OOM: return "GEMM_ERR_OOM";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        case GEMM_ERR_BOUNDS: return "GEMM_ERR_BOUNDS";
     }
     return "GEMM_ERR_UNKNOWN";
 }
@@ -798,6 +806,14 @@ gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t split_k,
     return GEMM_OK;
 }
 
+int32_t gemm_build_checked(void) { return DG_CHECKED ? 1 : 0; }
+
+gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int32_t* word) {
+    if (plan == nullptr || word == nullptr) return GEMM_ERR_INVALID_ARG;
+    *word = plan->last_device_status;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint64_t timeout_ns) {
     if (plan == nullptr || (sync != 0 && sync != 1)) return GEMM_ERR_INVALID_ARG;
     plan->debug_sync = sync != 0;
@@ -880,12 +896,14 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
         if (sg.a)
             err = dg::launch_stage_rows(static_cast<const uint16_t*>(a_in.A), a_in.lda,
                                         const_cast<uint16_t*>(static_cast<const uint16_t*>(a.A)),
-                                        a.lda, a_in.a_rows(), a_in.a_cols(), plan->num_sms,
+                                        a.lda, a_in.a_rows(), a_in.a_cols(), plan->status,
+                                        plan->num_sms,
                                         stream);
         if (err == cudaSuccess && sg.b)
             err = dg::launch_stage_rows(static_cast<const uint16_t*>(a_in.B), a_in.ldb,
                                         const_cast<uint16_t*>(static_cast<const uint16_t*>(a.B)),
-                                        a.ldb, a_in.b_rows(), a_in.b_cols(), plan->num_sms,
+                                        a.ldb, a_in.b_rows(), a_in.b_cols(), plan->status,
+                                        plan->num_sms,
                                         stream);
         if (err != cudaSuccess) {
             (void)cudaGetLastError();
@@ -926,6 +944,8 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
                       : 0;
         p.ws = plan->ws;
         p.counters = plan->counters;
+        p.ws_len = static_cast<int64_t>(plan->ws_bytes / sizeof(float));
+        p.counters_len = plan->counters_len;
         p.status = plan->status;
         p.timeout_ns = plan->timeout_ns;
         const bool bf16 = a.dtype == GEMM_BF16;
@@ -1017,10 +1037,11 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
         if (cudaMemcpy(&dev_status, plan->status, sizeof(int), cudaMemcpyDeviceToHost) !=
             cudaSuccess)
             return GEMM_ERR_CUDA;
+        plan->last_device_status = dev_status;
         if (dev_status != 0) {
             (void)cudaMemset(plan->status, 0, sizeof(int));
             (void)cudaMemset(plan->counters, 0, sizeof(int) * plan->counters_len);
-            return GEMM_ERR_TIMEOUT;
+            return (dev_status & dg::kDevBounds) ? GEMM_ERR_BOUNDS : GEMM_ERR_TIMEOUT;
         }
     }
     return GEMM_OK;

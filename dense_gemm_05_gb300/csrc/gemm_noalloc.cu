@@ -231,6 +231,8 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
     p.c_vec = 0;
     p.ws = reinterpret_cast<float*>(s->scratch);
     p.counters = counters;
+    p.ws_len = kScratchWsBytes / static_cast<int64_t>(sizeof(float));
+    p.counters_len = kScratchCounters;
     p.status = status;
     p.timeout_ns = 2000000000ull;
     const int grid = shares < s->num_sms ? static_cast<int>(shares) : s->num_sms;
@@ -248,6 +250,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, int64_t lda, const void
             (void)cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
+        if (dev_status & dg::kDevBounds) return GEMM_ERR_BOUNDS;
         if (dev_status != 0) return GEMM_ERR_TIMEOUT;
     }
     return GEMM_OK;

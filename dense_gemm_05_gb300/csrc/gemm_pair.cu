@@ -230,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             *n_consumed = consumed;
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 const volatile int never = 0;
                 tc_commit_pair_mc(smem_u32(drain), 0x1);
                 mbar_wait(smem_u32(drain), 0u, &never, 100000000ull);
@@ -254,12 +254,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         while (walk.next(sg)) {
             int tm, tn;
             tile_coord32(sg.tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
-            const bool ok =
+            const bool waited =
                 mbar_wait(smem_u32(&tfull[acc]), acc_phase, abort_flag, p.timeout_ns);
+            if (!waited && p.status != nullptr) atomicOr(p.status, kDevTimeout);
+            bool in_range = true;
+#if DG_CHECKED
+            // A checked build tests a partial tile's counter and workspace parts
+            // first; a failure stops the cluster like a wait that gave up.
+            if (sg.kb0 != 0 || sg.kb1 != num_kb) {
+                const int64_t f = share_of(int64_t(sg.tile) * num_kb, walk.t_sk, walk.g);
+                const int64_t l = share_of(int64_t(sg.tile + 1) * num_kb - 1, walk.t_sk, walk.g);
+                in_range = DG_CHECK(p.status, kChkCounter,
+                                    span_inside(0, int64_t(sg.tile) * 2 + rank, 1, 1, p.counters_len));
+                for (int64_t sh = f; sh <= l && in_range; ++sh)
+                    in_range = DG_CHECK(
+                        p.status, kChkWs,
+                        span_inside(0, ((sh * 2 + walk.slot_of(sh, sg.tile)) * 2 + rank) * (BN * 128),
+                                    BN * 128, 1, p.ws_len));
+            }
+#endif
             // One decision for all 128 epilogue threads: they share named barriers below.
-            if (!named_bar_and(1, 128, ok)) {
+            if (!named_bar_and(1, 128, waited && in_range)) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
                 break;
             }
             tc_fence_after();
@@ -466,7 +482,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             *n_issued = issued;
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
             }
         }
         __syncwarp();

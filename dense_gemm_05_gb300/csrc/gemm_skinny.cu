@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 const volatile int never = 0;
                 tc_commit(smem_u32(drain));
                 mbar_wait(smem_u32(drain), 0u, &never, 100000000ull);
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(192, 1)
             // One decision for all 128 epilogue threads: they share named barriers below.
             if (!named_bar_and(1, 128, ok)) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 break;
             }
             tc_fence_after();
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (n < p.N) {
 #pragma unroll
                     for (int m = 0; m < MS; ++m)
-                        if (m < p.M) store_c1(p, static_cast<int64_t>(m) * p.ldc + n, v[m]);
+                        if (m < p.M) store_c1(p, m, n, v[m]);
                 }
                 continue;
             }
@@ -258,6 +258,15 @@ __global__ void __launch_bounds__(192, 1)
             const int64_t last = share_of(int64_t(sg.tile + 1) * num_kb - 1, T, p.shares);
             const int nslots = static_cast<int>(last - first + 1);
             const int slot = static_cast<int>(walk.share - first);
+            // A checked build tests the tile's slots and counter first: the same
+            // answer on every epilogue thread, so all of them skip the tile together
+            // (its C is then not written).
+            if (!DG_CHECK(p.status, kChkWs,
+                          nslots <= p.max_slots &&
+                              span_inside(0, static_cast<int64_t>(sg.tile) * p.max_slots * (MS * 128),
+                                          static_cast<int64_t>(nslots) * (MS * 128), 1, p.ws_len)) ||
+                !DG_CHECK(p.status, kChkCounter, span_inside(0, sg.tile, 1, 1, p.counters_len)))
+                continue;
             float* tile_ws = p.ws + static_cast<int64_t>(sg.tile) * p.max_slots * (MS * 128);
             float* mine = tile_ws + static_cast<int64_t>(slot) * (MS * 128) + r;
 #pragma unroll
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(192, 1)
                 if (n < p.N) {
 #pragma unroll
                     for (int m = 0; m < MS; ++m)
-                        if (m < p.M) store_c1(p, static_cast<int64_t>(m) * p.ldc + n, s[m]);
+                        if (m < p.M) store_c1(p, m, n, s[m]);
                 }
                 if (et == 0) store_relaxed_gpu(&p.counters[sg.tile], 0);
             }
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 const volatile int never = 0;
                 const int64_t rounds = armed / STAGES;
                 for (int s = 0; s < STAGES; ++s) {

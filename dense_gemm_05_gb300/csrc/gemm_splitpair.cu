@@ -191,7 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 tc_commit(smem_u32(tfull));
             } else {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 const volatile int never = 0;
                 tc_commit(smem_u32(drain));
                 mbar_wait(smem_u32(drain), 0u, &never, 100000000ull);
@@ -220,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 const int slot = j % RAW;
                 unaligned_rows_issue(raw0 + static_cast<uint32_t>(slot * kRawStageBytes),
                                      smem_u32(&rawfull[slot * 4 + w4]), p.B, p.ldb, n0,
-                                     (kb0 + j) * kBK, p.N, p.K, w4, lane);
+                                     (kb0 + j) * kBK, p.N, p.K, w4, lane, p.status, kChkB);
             };
             for (; issued < RAW && issued < nkb; ++issued) issue(issued);
             bool failed = false;
@@ -237,7 +237,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 }
                 unaligned_rows_place(smem_u32(sB + stage * Cfg::kBStageBytes),
                                      raw0 + static_cast<uint32_t>(slot * kRawStageBytes), p.B, p.ldb,
-                                     n0, (kb0 + placed) * kBK, p.N, p.K, w4, lane);
+                                     n0, (kb0 + placed) * kBK, p.N, p.K, w4, lane, p.status,
+                                     kChkB);
                 // generic stores -> the MMA's operand reads; generic reads of the raw
                 // slot -> the next bulk copy into it
                 fence_proxy_async_smem();
@@ -251,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 // Bulk copies already issued must land before the shared memory goes away.
                 const volatile int never = 0;
                 for (int j = placed; j < issued; ++j)
@@ -290,7 +291,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 fence_proxy_async_smem();
             } else {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
             }
             named_bar_arrive(4, 32 * Cfg::kEpiWarps + 32);
             // 2. The peer's half of this CTA's columns.  A wait that runs out claims
@@ -304,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     mbar_wait_cluster(smem_u32(xfull), 0u, &never, 100000000ull);
                 }
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
             }
             // Nothing more arrives in this CTA's shared memory once the peer's copy
             // has landed, and this thread touches no other CTA's memory: the closing
@@ -380,12 +381,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                 if (named_bar_and(3, 32 * Cfg::kEpiWarps, got)) {
                     const float* xs = reinterpret_cast<const float*>(sX);
                     for (int rr = q; rr < MS && m0 + rr < p.M; rr += Cfg::kEpiWarps) {
-                        const int64_t off = static_cast<int64_t>(m0 + rr) * p.ldc;
 #pragma unroll 4
                         for (int cc = lane; cc < Cfg::kHalf; cc += 32) {
                             const int col = col_base + cc;
                             if (col < p.N)
-                                store_c1(p, off + col, xs[((cc >> 2) * MS + rr) * 4 + (cc & 3)]);
+                                store_c1(p, m0 + rr, col, xs[((cc >> 2) * MS + rr) * 4 + (cc & 3)]);
                         }
                     }
                 }
@@ -430,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             }
             if (failed) {
                 *abort_flag = 1;
-                if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+                if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
                 // Copies already issued must land before the shared memory goes away.
                 const volatile int never = 0;
                 const int rounds = armed / STAGES;

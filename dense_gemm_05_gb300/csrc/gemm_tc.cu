@@ -44,20 +44,29 @@ struct TcCfg {
 
 __device__ __forceinline__ void raise_abort(const Params& p, volatile int* abort_flag) {
     *abort_flag = 1;
-    if (p.status != nullptr) atomicExch(p.status, kDevTimeout);
+    if (p.status != nullptr) atomicOr(p.status, kDevTimeout);
 }
 
-// Eight consecutive 16-bit elements starting at base[off]; elements at or
-// beyond `remaining`, or the whole chunk when !row_ok, read as zero.
-__device__ __forceinline__ uint4 load8(const uint16_t* base, int64_t off, bool row_ok,
-                                       int remaining, int vec) {
+// Eight consecutive 16-bit elements of a stored rows x cols matrix (pitch ld),
+// from (row, col) on; elements beyond cols, or all of them when row >= rows,
+// read as zero.  In a checked build each load is tested against the rectangle
+// first (`kind`: the operand's status bit).
+__device__ __forceinline__ uint4 load8(const uint16_t* base, int64_t ld, int row, int col,
+                                       int rows, int cols, int vec, int* status, int kind) {
     uint4 r = make_uint4(0u, 0u, 0u, 0u);
-    if (!row_ok || remaining <= 0) return r;
-    const uint16_t* ptr = base + off;
-    if (vec && remaining >= 8) return __ldg(reinterpret_cast<const uint4*>(ptr));
+    const int remaining = cols - col;
+    if (row >= rows || remaining <= 0) return r;
+    const uint16_t* ptr = base + static_cast<int64_t>(row) * ld + col;
+    if (vec && remaining >= 8) {
+        if (!DG_CHECK(status, kind, span_inside(row, col, 8, rows, cols))) return r;
+        return __ldg(reinterpret_cast<const uint4*>(ptr));
+    }
     uint32_t e[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) e[i] = (i < remaining) ? static_cast<uint32_t>(__ldg(ptr + i)) : 0u;
+    for (int i = 0; i < 8; ++i)
+        e[i] = (i < remaining && DG_CHECK(status, kind, span_inside(row, col + i, 1, rows, cols)))
+                   ? static_cast<uint32_t>(__ldg(ptr + i))
+                   : 0u;
     r.x = e[0] | (e[1] << 16);
     r.y = e[2] | (e[3] << 16);
     r.z = e[4] | (e[5] << 16);
@@ -72,7 +81,7 @@ __device__ __forceinline__ uint4 load8(const uint16_t* base, int64_t off, bool r
 template <bool MN_MAJOR, int ROWS>
 __device__ __forceinline__ void load_tile_generic(uint32_t dst, const uint16_t* base, int64_t ld,
                                                   int mn0, int k0, int mn_total, int k_total,
-                                                  int vec, int pt) {
+                                                  int vec, int pt, int* status, int kind) {
     constexpr int kChunks = ROWS * kBK / 8;      // 16-byte chunks in the tile
     constexpr int kPer = kChunks / 128;
     constexpr int kRowChunks = MN_MAJOR ? ROWS / 8 : kBK / 8;
@@ -82,11 +91,9 @@ __device__ __forceinline__ void load_tile_generic(uint32_t dst, const uint16_t* 
         const int q = pt + i * 128;
         const int r = q / kRowChunks, c = q % kRowChunks;
         if constexpr (MN_MAJOR) {
-            const int k = k0 + r, mn = mn0 + c * 8;
-            v[i] = load8(base, static_cast<int64_t>(k) * ld + mn, k < k_total, mn_total - mn, vec);
+            v[i] = load8(base, ld, k0 + r, mn0 + c * 8, k_total, mn_total, vec, status, kind);
         } else {
-            const int mn = mn0 + r, k = k0 + c * 8;
-            v[i] = load8(base, static_cast<int64_t>(mn) * ld + k, mn < mn_total, k_total - k, vec);
+            v[i] = load8(base, ld, mn0 + r, k0 + c * 8, mn_total, k_total, vec, status, kind);
         }
     }
 #pragma unroll
@@ -233,7 +240,6 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                                      mbar_arrive(tempty_bar);
                                  });
             } else {
-                const int64_t row_off = static_cast<int64_t>(row) * p.ldc + col0;
                 const bool row_ok = row < p.M;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                         tc_fence_before();
                         mbar_arrive(tempty_bar);
                     }
-                    if (row_ok) store_c32(p, row_off + c * 32, v, p.N - (col0 + c * 32));
+                    if (row_ok) store_c32(p, row, col0 + c * 32, v);
                 }
             }
             if (++acc == 2) {
@@ -315,9 +321,11 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     break;
                 }
                 load_tile_generic<A_MN, kBM>(smem_u32(sA + stage * kAStageBytes), p.A, p.lda,
-                                             tm * kBM, kb * kBK, p.M, p.K, p.a_vec, pt);
+                                             tm * kBM, kb * kBK, p.M, p.K, p.a_vec, pt, p.status,
+                                             kChkA);
                 load_tile_generic<B_MN, BN>(smem_u32(sB + stage * Cfg::kBStageBytes), p.B, p.ldb,
-                                            tn * BN, kb * kBK, p.N, p.K, p.b_vec, pt);
+                                            tn * BN, kb * kBK, p.N, p.K, p.b_vec, pt, p.status,
+                                            kChkB);
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full[stage]));
                 if (++stage == STAGES) {

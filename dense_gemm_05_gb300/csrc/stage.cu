@@ -12,7 +12,7 @@ namespace {
 
 __global__ void __launch_bounds__(256)
     stage_rows_kernel(const uint16_t* __restrict__ src, int64_t lds, uint16_t* __restrict__ dst,
-                      int64_t ldd, int64_t rows, int64_t cols) {
+                      int64_t ldd, int64_t rows, int64_t cols, int* status) {
     griddep_wait();        // src may be written, dst still read, by the previous grid
     griddep_launch_dependents();
     const int64_t pieces = (cols + 7) / 8;          // per row; ldd >= 8 * pieces
@@ -25,23 +25,29 @@ __global__ void __launch_bounds__(256)
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const uint32_t lo = (c0 + 2 * e < cols) ? s[2 * e] : 0u;
-            const uint32_t hi = (c0 + 2 * e + 1 < cols) ? s[2 * e + 1] : 0u;
+            const uint32_t lo = (c0 + 2 * e < cols &&
+                                 DG_CHECK(status, kChkStage, span_inside(r, c0 + 2 * e, 1, rows, cols)))
+                                    ? s[2 * e] : 0u;
+            const uint32_t hi = (c0 + 2 * e + 1 < cols &&
+                                 DG_CHECK(status, kChkStage, span_inside(r, c0 + 2 * e + 1, 1, rows, cols)))
+                                    ? s[2 * e + 1] : 0u;
             w[e] = lo | (hi << 16);
         }
-        *reinterpret_cast<uint4*>(dst + r * ldd + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (DG_CHECK(status, kChkStage, span_inside(r, c0, 8, rows, ldd)))
+            *reinterpret_cast<uint4*>(dst + r * ldd + c0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_stage_rows(const uint16_t* src, int64_t lds, uint16_t* dst, int64_t ldd,
-                              int64_t rows, int64_t cols, int num_sms, cudaStream_t stream) {
+                              int64_t rows, int64_t cols, int* status, int num_sms,
+                              cudaStream_t stream) {
     const int64_t total = rows * ((cols + 7) / 8);
     const int64_t blocks = (total + 255) / 256;
     const int64_t cap = int64_t(num_sms) * 8;
     return launch_pdl(stage_rows_kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)),
-                      dim3(256), 0, stream, src, lds, dst, ldd, rows, cols);
+                      dim3(256), 0, stream, src, lds, dst, ldd, rows, cols, status);
 }
 
 }  // namespace dg

@@ -108,12 +108,17 @@ __device__ __forceinline__ uint32_t pack_out(float a, float b, int type) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Store 32 consecutive accumulator values of one C row starting at element
-// `off` (= row * ldc + col), the first `ncols` of them in range, converting to
-// the output type with round-to-nearest-even.  `vec`: the row start is
-// 16-byte aligned (C base and ldc allow 16-byte stores).
-__device__ __forceinline__ void store_c32(const Params& p, int64_t off, const uint32_t (&v)[32],
-                                          int ncols) {
+// Store 32 consecutive accumulator values of C row `row` from column `col` on,
+// those below N, converting to the output type with round-to-nearest-even.
+// `vec`: the row start is 16-byte aligned (C base and ldc allow 16-byte
+// stores).  A checked build tests the row's range first.
+__device__ __forceinline__ void store_c32(const Params& p, int row, int col,
+                                          const uint32_t (&v)[32]) {
+    const int ncols = p.N - col;
+    if (ncols <= 0 ||
+        !DG_CHECK(p.status, kChkC, span_inside(row, col, ncols < 32 ? ncols : 32, p.M, p.N)))
+        return;
+    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
     if (p.c_type == kOutF32) {
         float* dst = static_cast<float*>(p.C) + off;
         if (p.c_vec && ncols >= 32) {
@@ -232,7 +237,8 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
             const int r = row0 + rr;
             const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
             const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
-            if (r < p.M && h + 4 * k + 4 <= 32) {
+            if (r < p.M && h + 4 * k + 4 <= 32 &&
+                DG_CHECK(p.status, kChkC, span_inside(r, col + h + 4 * k, 4, p.M, p.N))) {
                 const int e = h + 4 * k;
                 const uint32_t rowb = buf + static_cast<uint32_t>(rr * 128);
                 float4 v;
@@ -246,7 +252,7 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
         const int r = row0 + lane;
         const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
         const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
-        if (r < p.M && h != 0) {
+        if (r < p.M && h != 0 && DG_CHECK(p.status, kChkC, span_inside(r, col, 32, p.M, p.N))) {
             const uint32_t rowb = buf + static_cast<uint32_t>(lane * 128);
             auto elem = [&](int e) {
                 return __uint_as_float(ld_shared_b32(
@@ -273,12 +279,15 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
         const int64_t off = static_cast<int64_t>(r) * p.ldc;
         if (p.c_type == kOutF32) {
             const int c = col + lane;
-            if (c < p.N) static_cast<float*>(p.C)[off + c] = __uint_as_float(w);
+            if (c < p.N && DG_CHECK(p.status, kChkC, span_inside(r, c, 1, p.M, p.N)))
+                static_cast<float*>(p.C)[off + c] = __uint_as_float(w);
         } else {
             const int c = col + 2 * lane;
             uint16_t* dst = static_cast<uint16_t*>(p.C) + off;
-            if (c < p.N) dst[c] = static_cast<uint16_t>(w & 0xFFFFu);
-            if (c + 1 < p.N) dst[c + 1] = static_cast<uint16_t>(w >> 16);
+            if (c < p.N && DG_CHECK(p.status, kChkC, span_inside(r, c, 1, p.M, p.N)))
+                dst[c] = static_cast<uint16_t>(w & 0xFFFFu);
+            if (c + 1 < p.N && DG_CHECK(p.status, kChkC, span_inside(r, c + 1, 1, p.M, p.N)))
+                dst[c + 1] = static_cast<uint16_t>(w >> 16);
         }
     }
 }
@@ -389,8 +398,24 @@ __device__ __forceinline__ bool unaligned_stage_interior(const uint16_t* base, i
 __device__ __forceinline__ void unaligned_rows_issue(uint32_t raw, uint32_t bar,
                                                      const uint16_t* base, int64_t ld, int mn0,
                                                      int k0, int mn_total, int k_total, int w4,
-                                                     int lane) {
+                                                     int lane, int* status, int kind) {
     const int h = lane >> 4, c = lane & 15;
+#if DG_CHECKED
+    // A checked build tests every 16-byte copy against the matrix's footprint.
+    const uintptr_t foot_lo = reinterpret_cast<uintptr_t>(base);
+    const uintptr_t foot_hi =
+        reinterpret_cast<uintptr_t>(base + (static_cast<int64_t>(k_total) - 1) * ld + mn_total);
+    auto copy16 = [&](uint32_t dst, uintptr_t src) {
+        if (DG_CHECK(status, kind, bytes_inside(src, 16u, foot_lo, foot_hi)))
+            cp_async_16(dst, reinterpret_cast<const void*>(src));
+    };
+#else
+    (void)status;
+    (void)kind;
+    auto copy16 = [&](uint32_t dst, uintptr_t src) {
+        cp_async_16(dst, reinterpret_cast<const void*>(src));
+    };
+#endif
     if (unaligned_stage_interior(base, ld, mn0, k0, k_total)) {
         const RowSpan r0 = unaligned_row_span(base, ld, mn0, k0 + w4 + 4 * h, mn_total, k_total);
         const uintptr_t a16 = r0.a - r0.d;
@@ -400,10 +425,8 @@ __device__ __forceinline__ void unaligned_rows_issue(uint32_t raw, uint32_t bar,
         for (int j = 0; j < 8; ++j) {
             const uint32_t dst = dst0 + static_cast<uint32_t>(j * 8 * kRawRowBytes);
             const uintptr_t src = a16 + static_cast<uintptr_t>(j) * step;
-            if (static_cast<uint32_t>(c) < r0.pieces)
-                cp_async_16(dst + 16u * c, reinterpret_cast<const void*>(src + 16u * c));
-            if (c == 0 && r0.pieces > 16)
-                cp_async_16(dst + 256u, reinterpret_cast<const void*>(src + 256u));
+            if (static_cast<uint32_t>(c) < r0.pieces) copy16(dst + 16u * c, src + 16u * c);
+            if (c == 0 && r0.pieces > 16) copy16(dst + 256u, src + 256u);
         }
     } else {
 #pragma unroll 1
@@ -412,10 +435,8 @@ __device__ __forceinline__ void unaligned_rows_issue(uint32_t raw, uint32_t bar,
             const RowSpan r = unaligned_row_span(base, ld, mn0, k0 + kk, mn_total, k_total);
             const uintptr_t a16 = r.a - r.d;
             const uint32_t dst = raw + static_cast<uint32_t>(kk * kRawRowBytes);
-            if (static_cast<uint32_t>(c) < r.pieces)
-                cp_async_16(dst + 16u * c, reinterpret_cast<const void*>(a16 + 16u * c));
-            if (c == 0 && r.pieces > 16)
-                cp_async_16(dst + 256u, reinterpret_cast<const void*>(a16 + 256u));
+            if (static_cast<uint32_t>(c) < r.pieces) copy16(dst + 16u * c, a16 + 16u * c);
+            if (c == 0 && r.pieces > 16) copy16(dst + 256u, a16 + 256u);
         }
     }
     cp_async_arrive(bar);
@@ -427,7 +448,7 @@ __device__ __forceinline__ void unaligned_rows_issue(uint32_t raw, uint32_t bar,
 __device__ __forceinline__ void unaligned_rows_place(uint32_t dst, uint32_t raw,
                                                      const uint16_t* base, int64_t ld, int mn0,
                                                      int k0, int mn_total, int k_total, int w4,
-                                                     int lane) {
+                                                     int lane, int* status, int kind) {
     const int h = lane >> 4, c = lane & 15;
     const int n = mn0 + 8 * c;
     uint32_t keep[4];                              // masks of the elements below MN
@@ -473,7 +494,8 @@ __device__ __forceinline__ void unaligned_rows_place(uint32_t dst, uint32_t raw,
             const uint16_t* row = base + static_cast<int64_t>(k) * ld;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                if (n + e < mn_total)
+                if (n + e < mn_total &&
+                    DG_CHECK(status, kind, span_inside(k, n + e, 1, k_total, mn_total)))
                     w[e >> 1] |= static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row + n + e)))
                                  << (16 * (e & 1));
         }
@@ -482,8 +504,10 @@ __device__ __forceinline__ void unaligned_rows_place(uint32_t dst, uint32_t raw,
     }
 }
 
-// Store one accumulator value (skinny epilogue, scattered columns).
-__device__ __forceinline__ void store_c1(const Params& p, int64_t off, float x) {
+// Store one accumulator value at C[row, col] (scattered columns).
+__device__ __forceinline__ void store_c1(const Params& p, int row, int col, float x) {
+    if (!DG_CHECK(p.status, kChkC, span_inside(row, col, 1, p.M, p.N))) return;
+    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
     if (p.c_type == kOutF32)
         static_cast<float*>(p.C)[off] = x;
     else

@@ -60,7 +60,9 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED = 2,   /* unknown dtype, not an sm_103 device, size beyond 2^31-1 */
     GEMM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch error etc.) */
     GEMM_ERR_OOM = 4,           /* workspace allocation failed */
-    GEMM_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (debug-sync mode) */
+    GEMM_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up (debug-sync mode) */
+    GEMM_ERR_BOUNDS = 6         /* checked build, debug-sync mode: a kernel skipped an access
+                                   outside its matrix or buffer (gemm_build_checked) */
 } gemm_status_t;
 
 /* Storage of an operand for gemm_run_ex (the operation is always C = A @ B):
@@ -234,7 +236,8 @@ GEMM_API gemm_status_t gemm_plan_set_group(gemm_plan_t plan, int32_t group);
  * (0 = automatic); for PAIR, `split_k` = 1 turns off the stream-K phase that
  * otherwise splits the last, partial wave of pair tiles (plus one full wave)
  * by K across all clusters, `split_k` = 2 splits every tile's K loop over all
- * clusters (whole-problem stream-K), any other value = automatic -- and `block_n`
+ * clusters (whole-problem stream-K), `split_k` = 3 runs the stream-K phase for any
+ * partial last wave, any other value = automatic -- and `block_n`
  * tile columns for TMA/PAIR (128 or 256) or strip columns for SPLIT_PAIR (128,
  * 192 or 256; 0 = automatic).  For tests and tuning.
  * gemm_run returns UNSUPPORTED when the forced kernel cannot run the given
@@ -265,6 +268,33 @@ GEMM_API gemm_status_t gemm_plan_force(gemm_plan_t plan, int32_t kernel, int32_t
  * Errors: INVALID_ARG (null plan, sync not 0 or 1).
  */
 GEMM_API gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint64_t timeout_ns);
+
+/*
+ * Checked builds.  The same sources compiled with DG_CHECKED=1 give a second
+ * library, libgemm_checked.so, with this same ABI.  In it every ordinary
+ * (non-TMA) global load and store of the kernels first tests the range it
+ * touches against the matrix or buffer it belongs to: A, B and C against the
+ * rows x columns rectangles the caller passed (so a row's padding between N and
+ * ldc counts as outside), the staging copy against its source and destination,
+ * split-K partials and tile counters against the plan's workspace.  An access
+ * that fails the test is skipped -- it never reaches memory -- and sets a bit
+ * of the plan's device status word: 2 (out of range) plus one bit per kind of
+ * access, 1<<8 C store, 1<<9 A load, 1<<10 B load, 1<<11 workspace,
+ * 1<<12 tile counter, 1<<13 staging copy.  A debug-sync gemm_run (see
+ * gemm_plan_set_debug) then returns GEMM_ERR_BOUNDS; without debug-sync the
+ * word is cleared unread by the next debug-sync call.  A partial tile whose
+ * workspace range fails stops its kernel as a wait that gave up does.  TMA copies
+ * are not tested: their tensor maps bound them in hardware (elements outside
+ * read as zeros, stores are clipped).  There is no counterpart in the pages;
+ * the checked build stands in for a memory checker, and runs slower.
+ *
+ * gemm_build_checked: 1 in the checked library, 0 in the normal one.
+ * gemm_plan_device_status: the status word the plan's last debug-sync gemm_run
+ * read (0: none; 1 = a wait gave up; 2 and the bits above = out of range).
+ * Errors: INVALID_ARG (null plan or word).
+ */
+GEMM_API int32_t gemm_build_checked(void);
+GEMM_API gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int32_t* word);
 
 /*
  * Turn the staging of misaligned operands on (1, the default) or off (0) for

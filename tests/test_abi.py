@@ -42,6 +42,7 @@ def test_status_strings():
     assert g.status_string(0) == "GEMM_OK"
     assert g.status_string(1) == "GEMM_ERR_INVALID_ARG"
     assert g.status_string(5) == "GEMM_ERR_TIMEOUT"
+    assert g.status_string(6) == "GEMM_ERR_BOUNDS"
     assert g.status_string(99) == "GEMM_ERR_UNKNOWN"
 
 

@@ -40,6 +40,10 @@ def test_the_five_workloads(model):
     assert r["shares"] == 76 and r["split_k"] >= 2, r      # stream-K phase for the partial wave
     r = q(model, 4096, 4096, 4096)
     assert r["kernel"] == g.GEMM_KERNEL_PAIR and r["block_n"] == 256 and r["shares"] == 76, r
+    # the stream-K phase by last-wave fill and full waves (576, 196, 441 tiles on 76 pairs)
+    assert q(model, 6144, 6144, 6144)["shares"] == 76        # 58% full behind 7 waves
+    assert q(model, 3584, 3584, 3584)["shares"] == 0         # 58% behind 2
+    assert q(model, 5376, 5376, 5376)["shares"] == 0         # 80% behind 5
     r = q(model, 16, 14336, 4096)
     assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["split_k"], r["tiles"]) == \
         (g.GEMM_KERNEL_SPLIT_PAIR, 16, 256, 112, 2, 56), r
