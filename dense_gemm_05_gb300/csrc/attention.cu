@@ -5,31 +5,36 @@
 // to hand-write Triton kernels for matmul and Flash Attention": each block of
 // 128 queries of one head walks the key/value blocks (128 keys each)
 // and keeps, per query row, a running maximum m, a running sum l and an
-// accumulator O that are rescaled by alpha = exp(m_old - m_new) whenever m
+// accumulator O that are rescaled by alpha = exp(m_old - m_new) when m
 // grows; O / l is written once at the end.  Causal: key j takes part in row i
 // only if j <= i, so query block t needs key blocks 0..t, and only block t is
-// masked element by element.
+// masked element by element.  Unlike the page's loop, the maximum the weights
+// are taken against moves (and O is rescaled) only when the running maximum
+// has grown by more than 2^8 in weight (kRescaleLog2): O / l is the same for
+// any reference maximum, and weights up to 2^8 fit every type involved.
 //
-// GB300 mapping: one CTA per SM holds two query tiles of one head (A, B)
-// that share every K/V block (512 TMEM columns, ~130 KiB of shared memory):
-//   warp 0      TMA producer: both Q tiles once, then K and V blocks into a
+// GB300 mapping: one CTA per SM holds one (d = 128) or two (d = 64, tiles A
+// and B sharing every K/V block) query tiles of one head; TMEM per tile: the
+// score buffers S (two at d = 128, one at d = 64), P and O:
+//   warp 0      TMA producer: the Q tiles once, then K and V blocks into a
 //               3-stage ring (3-D tensor maps over [BH, seq, d]).
-//   warps 1, 2  one MMA issuer per tile (warp 1 also owns TMEM):
-//               S_t(j+1) = Q_t K^T (M 128, N 128, K 64) into the tile's TMEM
-//               score buffer as soon as the tile's softmax has read S_t(j),
-//               then O_t += P_t(j) V_j (M 128, N 64, K 128) with P_t(j) read
-//               from TMEM once the softmax has stored it there; a K/V stage
-//               is refilled when every tile that used it has committed its
-//               release.
-//   warps 3..10 two softmax warpgroups, one per tile, one thread per query
-//               row (= TMEM lane): read S_t(j) from TMEM, mask, row max,
+//   warp 1      S issuer (also owns TMEM): S_t(j) = Q_t K_j^T (M 128, N 128,
+//               K d) into score buffer j % kSBufs of tile t once K_j has
+//               landed and the tile's softmax has read that buffer.
+//   warp 2      P V issuer: O_t += P_t(j) V_j (M 128, N d, K 128) with P_t(j)
+//               read from TMEM once the softmax has stored it there; a K/V
+//               stage is refilled when every tile that used it has committed
+//               its release.  With the two kinds on separate warps neither
+//               waits behind the other.
+//   warps 3..   one softmax warpgroup per tile, one thread per query row
+//               (= TMEM lane): read S_t(j) from TMEM, mask, row max,
 //               p = 2^(s*c - m*c) with c = log2(e)/sqrt(d), row sum, P_t(j)
 //               rounded to the input type into TMEM (the A operand of the
-//               second MMA), and the rescale of O_t in TMEM
-//               (load, multiply by alpha, store) after P_t(j-1) V_{j-1} has
-//               finished.  At the end O_t / l goes to global memory.  The two
-//               warpgroups interleave on the SM's exponential units and issue
-//               slots while the tensor cores work on the other tile.
+//               second MMA), and when the reference maximum moves the rescale
+//               of O_t in TMEM (load, multiply by alpha, store) after
+//               P_t(j-1) V_{j-1} has finished.  At the end O_t / l goes to
+//               global memory.  At d = 64 the two warpgroups interleave on the
+//               SM's exponential units and issue slots.
 // Every mbarrier wait is bounded; a role that gives up raises the CTA's abort
 // flag and records the failure in a device status word.
 #include <cmath>
@@ -54,28 +59,36 @@ constexpr int kBKV = 128;                 // keys per block
 constexpr int kStages = 3;                // K/V ring depth
 constexpr int kAtomBytes = 128 * 128;     // 128 rows x 64 elements of a K-major operand (16 KiB)
 constexpr int kSubBytes = 64 * 128;       // 64 keys x 64 d of the MN-major V operand (8 KiB)
-constexpr uint32_t kTmemCols = 512;       // per tile t at 256 t: S (128 columns of fp32),
-constexpr uint32_t kTmemP = 128;          //   P (64 columns, two 16-bit values each),
-constexpr uint32_t kTmemO = 192;          //   O (d columns of fp32)
-constexpr uint32_t kTmemTile = 256;
+constexpr uint32_t kTmemCols = 512;       // per tile t at 256 t: kSBufs score buffers S
+constexpr uint32_t kTmemS = 128;          //   (128 columns of fp32 each), then P (64 columns,
+constexpr uint32_t kTmemTile = 256;       //   two 16-bit values each), then O (d columns of fp32)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-// Sizes for head dimension D (64 or 128).  Rows of D elements are D/64 K-major
-// atoms of 128 B; with D = 64 two query tiles share each K/V block (TMEM: two
-// tiles of S + P + O = 2 x 256 columns), with D = 128 one (128 + 64 + 128).
+// Lazy rescaling: a row keeps the maximum its weights are taken against until
+// the running maximum exceeds it by more than 2^kRescaleLog2 in weight, so
+// weights stay <= 2^8 (exact in fp32, and in range for 16-bit P) and O is
+// rescaled only on the blocks where some row of the warp crossed that margin.
+constexpr float kRescaleLog2 = 8.0f;
+
 template <int D>
 struct AttnCfg {
     static constexpr int kD = D;
     static constexpr int kAtoms = D / 64;
     static constexpr int kTiles = D == 64 ? 2 : 1;
+    // Score buffers per tile: with one tile there is room for two, so that the
+    // MMA can compute S(j+2) while the softmax still works on S(j+1) and the
+    // P V product of block j is queued.
+    static constexpr int kSBufs = kTiles == 1 ? 2 : 1;
+    static constexpr uint32_t kTmemP = kSBufs * kTmemS;
+    static constexpr uint32_t kTmemO = kTmemP + 64;
     static constexpr int kQBytes = kBQ * D * 2;       // per tile: kAtoms atoms
     static constexpr int kKBytes = kBKV * D * 2;      // kAtoms atoms, N = keys
     static constexpr int kVBytes = kBKV * D * 2;      // [64-key half][64-d sub-tile]
-    static constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + 5 * kTiles;
+    static constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + kTiles * (2 * kSBufs + 2) + 2;
     static constexpr int kSmemBytes =
         1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
-    static constexpr int kThreads = 32 * (1 + kTiles + 4 * kTiles);   // producer, MMA warp,
-                                                                      // softmax warpgroups
+    static constexpr int kThreads = 32 * (3 + 4 * kTiles);   // producer, two MMA warps,
+                                                              // softmax warpgroups
     static_assert(D == 64 || D == 128, "head dimension");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kTmemO + D <= kTmemTile || kTiles == 1, "TMEM per tile");
@@ -104,6 +117,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     constexpr int kD = D;
     constexpr int kAtoms = Cfg::kAtoms;
     constexpr int kTiles = Cfg::kTiles;
+    constexpr int kSBufs = Cfg::kSBufs;
     constexpr int kQBytes = Cfg::kQBytes;
     constexpr int kKBytes = Cfg::kKBytes;
     constexpr int kVBytes = Cfg::kVBytes;
@@ -118,11 +132,11 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     uint64_t* k_full = q_full + 1;
     uint64_t* v_full = k_full + kStages;
     uint64_t* kv_empty = v_full + kStages;               // [tile][stage]
-    uint64_t* s_full = kv_empty + kTiles * kStages;      // [tile]
-    uint64_t* s_empty = s_full + kTiles;
-    uint64_t* p_full = s_empty + kTiles;
+    uint64_t* s_full = kv_empty + kTiles * kStages;      // [tile][score buffer]
+    uint64_t* s_empty = s_full + kTiles * kSBufs;
+    uint64_t* p_full = s_empty + kTiles * kSBufs;
     uint64_t* pv_done = p_full + kTiles;
-    uint64_t* drain = pv_done + kTiles;                  // [tile]
+    uint64_t* drain = pv_done + kTiles;                  // [MMA warp]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kTiles);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -157,12 +171,14 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
         }
         for (int s = 0; s < kTiles * kStages; ++s) dg::mbar_init(dg::smem_u32(&kv_empty[s]), 1u);
         for (int t = 0; t < kTiles; ++t) {
-            dg::mbar_init(dg::smem_u32(&s_full[t]), 1u);
-            dg::mbar_init(dg::smem_u32(&s_empty[t]), 128u);
+            for (int b = 0; b < kSBufs; ++b) {
+                dg::mbar_init(dg::smem_u32(&s_full[t * kSBufs + b]), 1u);
+                dg::mbar_init(dg::smem_u32(&s_empty[t * kSBufs + b]), 128u);
+            }
             dg::mbar_init(dg::smem_u32(&p_full[t]), 128u);
             dg::mbar_init(dg::smem_u32(&pv_done[t]), 1u);
         }
-        for (int t = 0; t < kTiles; ++t) dg::mbar_init(dg::smem_u32(&drain[t]), 1u);
+        for (int w = 0; w < 2; ++w) dg::mbar_init(dg::smem_u32(&drain[w]), 1u);
         *abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -225,95 +241,108 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp <= kTiles) {
+    } else if (warp <= 2) {
         // ------------------------------------------------------------ MMA issuers
-        // One warp per query tile, so that neither tile's pace holds up the
-        // other: S_t(j+1) as soon as the tile's softmax has read S_t(j) out of
-        // TMEM and K_{j+1} has landed, then P_t(j) V_j once P_t(j) is in
-        // shared memory; each softmax warpgroup finds its next scores ready
-        // when it finishes a block.
-        const int t = warp - 1;
+        // Warp 1 issues every tile's S_t(j) = Q_t K_j^T, warp 2 every tile's
+        // O_t += P_t(j) V_j, so that neither kind waits behind the other: an S
+        // MMA waiting for its K block or for its score buffer to be read never
+        // holds up a P V MMA whose P is ready, and back.  S_t(j) goes into
+        // score buffer j % kSBufs once the tile's softmax has read that buffer's
+        // previous scores; P_t(j) V_j once P_t(j) is in TMEM and V_j has landed.
+        const bool s_role = warp == 1;
         if (lane == 0) {
             constexpr uint32_t idesc_s = dg::idesc_f16(BF16, false, false, kBQ, kBKV);
             constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
-            const int n = nkv[t];
-            const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
-            const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile;
-            const uint32_t p_tmem = s_tmem + kTmemP;
-            const uint32_t o_tmem = s_tmem + kTmemO;
-            bool ok = n == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
-            auto issue_s = [&](int jj) -> bool {
-                // K_jj landed, and the tile's score buffer was read (jj-th use).
-                if (!dg::mbar_wait(dg::smem_u32(&k_full[jj % kStages]),
-                                   static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
-                                   p.timeout_ns) ||
-                    !dg::mbar_wait(dg::smem_u32(&s_empty[t]), (static_cast<uint32_t>(jj) & 1u) ^ 1u,
-                                   abort_flag, p.timeout_ns))
-                    return false;
-                dg::tc_fence_after();
-                const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
+            bool ok = true;
+            if (s_role) {
+                ok = nkv_max == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
+                for (int jj = 0; ok && jj < nkv_max; ++jj) {
+                    const int b = jj % kSBufs;
+                    ok = dg::mbar_wait(dg::smem_u32(&k_full[jj % kStages]),
+                                       static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
+                                       p.timeout_ns);
+                    const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
 #pragma unroll
-                for (int k16 = 0; k16 < kD / 16; ++k16)
-                    dg::tc_mma_f16(s_tmem,
-                                   dg::operand_desc<false>(q_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
-                                   dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
-                                   idesc_s, k16 > 0 ? 1u : 0u);
-                dg::tc_commit(dg::smem_u32(&s_full[t]));
-                return true;
-            };
-            if (ok && n > 0) ok = issue_s(0);
-            for (int j = 0; ok && j < n; ++j) {
-                const int st = j % kStages;
-                if (j + 1 < n && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                if (!dg::mbar_wait(dg::smem_u32(&v_full[st]), static_cast<uint32_t>(j / kStages) & 1u,
-                                   abort_flag, p.timeout_ns) ||
-                    !dg::mbar_wait(dg::smem_u32(&p_full[t]), static_cast<uint32_t>(j) & 1u,
-                                   abort_flag, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                dg::tc_fence_after();
-                const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
-                // P_t(j) from TMEM (8 columns = 16 keys per MMA), V_j from shared memory.
+                    for (int t = 0; t < kTiles; ++t) {
+                        if (!ok || jj >= nkv[t]) continue;
+                        // the buffer's (jj / kSBufs)-th use: its previous scores were read
+                        ok = dg::mbar_wait(dg::smem_u32(&s_empty[t * kSBufs + b]),
+                                           (static_cast<uint32_t>(jj / kSBufs) & 1u) ^ 1u, abort_flag,
+                                           p.timeout_ns);
+                        if (!ok) break;
+                        dg::tc_fence_after();
+                        const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
+                        const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile +
+                                                static_cast<uint32_t>(b) * kTmemS;
 #pragma unroll
-                for (int k16 = 0; k16 < kBKV / 16; ++k16)
-                    dg::tc_mma_f16_ts(o_tmem, p_tmem + static_cast<uint32_t>(k16 * 8),
-                                      dg::operand_desc<true>(v_addr + (k16 >> 2) * (kVBytes / 2),
-                                                             k16 & 3),
-                                      idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);   // N = d: kAtoms
-                                                                                 // sub-tiles 8 KiB apart
-                dg::tc_commit(dg::smem_u32(&pv_done[t]));
-                dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
+                        for (int k16 = 0; k16 < kD / 16; ++k16)
+                            dg::tc_mma_f16(s_tmem,
+                                           dg::operand_desc<false>(q_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                           dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                           idesc_s, k16 > 0 ? 1u : 0u);
+                        dg::tc_commit(dg::smem_u32(&s_full[t * kSBufs + b]));
+                    }
+                }
+            } else {
+                for (int j = 0; ok && j < nkv_max; ++j) {
+                    const int st = j % kStages;
+                    ok = dg::mbar_wait(dg::smem_u32(&v_full[st]), static_cast<uint32_t>(j / kStages) & 1u,
+                                       abort_flag, p.timeout_ns);
+                    const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
+#pragma unroll
+                    for (int t = 0; t < kTiles; ++t) {
+                        if (!ok || j >= nkv[t]) continue;
+                        ok = dg::mbar_wait(dg::smem_u32(&p_full[t]), static_cast<uint32_t>(j) & 1u,
+                                           abort_flag, p.timeout_ns);
+                        if (!ok) break;
+                        dg::tc_fence_after();
+                        const uint32_t tile_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile;
+                        // P_t(j) from TMEM (8 columns = 16 keys per MMA), V_j from
+                        // shared memory (N = d: kAtoms sub-tiles 8 KiB apart).
+#pragma unroll
+                        for (int k16 = 0; k16 < kBKV / 16; ++k16)
+                            dg::tc_mma_f16_ts(tile_tmem + Cfg::kTmemO,
+                                              tile_tmem + Cfg::kTmemP + static_cast<uint32_t>(k16 * 8),
+                                              dg::operand_desc<true>(v_addr + (k16 >> 2) * (kVBytes / 2),
+                                                                     k16 & 3),
+                                              idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);
+                        dg::tc_commit(dg::smem_u32(&pv_done[t]));
+                        // K_j and V_j of this stage are free once this tile is done
+                        // with them (its S_t(j) finished before P_t(j) existed).
+                        dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
+                    }
+                }
             }
             if (!ok) fail();
             // Every MMA this thread issued must have completed (and signalled its
             // barriers) before the CTA's shared memory and TMEM go away.
             const volatile int never = 0;
-            dg::tc_commit(dg::smem_u32(&drain[t]));
-            dg::mbar_wait(dg::smem_u32(&drain[t]), 0u, &never, 100000000ull);
+            uint64_t* my_drain = &drain[warp - 1];
+            dg::tc_commit(dg::smem_u32(my_drain));
+            dg::mbar_wait(dg::smem_u32(my_drain), 0u, &never, 100000000ull);
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int t = (warp - 1 - kTiles) >> 2;         // query tile of this warpgroup
+        const int t = (warp - 3) >> 2;                  // query tile of this warpgroup
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;              // query row in the tile == TMEM lane
         const int qrow = (pair * kTiles + t) * kBQ + r;
         const int qt = pair * kTiles + t;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        const uint32_t s_addr = lane_addr + static_cast<uint32_t>(t) * kTmemTile;
-        const uint32_t p_addr = s_addr + kTmemP;
-        const uint32_t o_addr = s_addr + kTmemO;
+        const uint32_t tile_addr = lane_addr + static_cast<uint32_t>(t) * kTmemTile;
+        const uint32_t p_addr = tile_addr + Cfg::kTmemP;
+        const uint32_t o_addr = tile_addr + Cfg::kTmemO;
         const int ptype = BF16 ? dg::kOutBF16 : dg::kOutF16;
         const int n = nkv[t];
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const bool got = dg::mbar_wait(dg::smem_u32(&s_full[t]), static_cast<uint32_t>(j) & 1u,
-                                           abort_flag, p.timeout_ns);
+            const int sb = j % kSBufs;                      // score buffer of block j
+            const uint32_t s_addr = tile_addr + static_cast<uint32_t>(sb) * kTmemS;
+            const bool got = dg::mbar_wait(dg::smem_u32(&s_full[t * kSBufs + sb]),
+                                           static_cast<uint32_t>(j / kSBufs) & 1u, abort_flag,
+                                           p.timeout_ns);
             if (!__all_sync(0xffffffffu, got)) {   // tcgen05.ld is warp-collective
                 ok = false;
                 break;
@@ -331,7 +360,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             dg::tmem_ld_wait(v2);
             dg::tmem_ld_wait(v3);
             dg::tc_fence_before();
-            dg::mbar_arrive(dg::smem_u32(&s_empty[t]));     // the MMA may write S_t(j+1)
+            dg::mbar_arrive(dg::smem_u32(&s_empty[t * kSBufs + sb]));   // S_t(j + kSBufs) may come
             float x[kBKV];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -355,8 +384,13 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             for (int i = 0; i < kBKV; i += 2) mx[(i >> 1) & 3] = dg::fmax3(mx[(i >> 1) & 3], x[i], x[i + 1]);
             const float mb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
             const float m_new = fmaxf(m, mb);
-            const float mc = m_new * p.c;
-            const float alpha = dg::ex2_approx(m * p.c - mc);   // 0 on the first block
+            // The reference maximum moves to m_new (and O is rescaled) only when
+            // some row of the warp would otherwise get weights above 2^8.
+            const bool move = m == -INFINITY || (m_new - m) * p.c > kRescaleLog2;
+            const bool rescale = __any_sync(0xffffffffu, move);
+            const float m_ref = rescale ? m_new : m;
+            const float mc = m_ref * p.c;
+            const float alpha = rescale ? dg::ex2_approx(m * p.c - mc) : 1.0f;   // 0 on the first block
             // p = 2^(s*c - m*c), two scores per packed fp32 multiply-add and add,
             // summed in fp32 and packed two per 32-bit word (rounded to the input
             // type) as they are made.
@@ -397,8 +431,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                 dg::tmem_st_32x32b_x32(p_addr + 32u, w1);
             }
             dg::tmem_st_wait();
-            if (j > 0 && !__all_sync(0xffffffffu, alpha == 1.0f)) {
-                // Rescale O_t to the new maximum before P_t(j) V_j is added.
+            if (j > 0 && rescale) {
+                // Rescale O_t to the new reference maximum before P_t(j) V_j is added.
 #pragma unroll
                 for (int ch = 0; ch < kD / 32; ++ch) {
                     uint32_t v[32];
@@ -414,7 +448,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             }
             dg::tc_fence_before();
             dg::mbar_arrive(dg::smem_u32(&p_full[t]));
-            m = m_new;
+            m = m_ref;
         }
         if (ok && n > 0) {
             const bool done = dg::mbar_wait(dg::smem_u32(&pv_done[t]),
