@@ -16,16 +16,17 @@
 // GB300 mapping: one CTA per SM holds one (d = 128) or two (d = 64, tiles A
 // and B sharing every K/V block) query tiles of one head; TMEM per tile: the
 // score buffers S (two at d = 128, one at d = 64), P and O:
-//   warp 0      TMA producer: the Q tiles once, then K and V blocks into a
-//               3-stage ring (3-D tensor maps over [BH, seq, d]).
+//   warp 0      TMA producers: lane 0 the Q tiles once, then K blocks, lane 1
+//               V blocks, each into a 3-stage ring (3-D tensor maps over
+//               [BH, seq, d]).
 //   warp 1      S issuer (also owns TMEM): S_t(j) = Q_t K_j^T (M 128, N 128,
 //               K d) into score buffer j % kSBufs of tile t once K_j has
 //               landed and the tile's softmax has read that buffer.
 //   warp 2      P V issuer: O_t += P_t(j) V_j (M 128, N d, K 128) with P_t(j)
-//               read from TMEM once the softmax has stored it there; a K/V
-//               stage is refilled when every tile that used it has committed
-//               its release.  With the two kinds on separate warps neither
-//               waits behind the other.
+//               read from TMEM once the softmax has stored it there.  With
+//               the two kinds on separate warps neither waits behind the
+//               other.  A K stage is refilled when every tile's S MMAs that
+//               read it have completed, a V stage when its P V MMAs have.
 //   warps 3..   one softmax warpgroup per tile, one thread per query row
 //               (= TMEM lane): read S_t(j) from TMEM, mask, row max,
 //               p = 2^(s*c - m*c) with c = log2(e)/sqrt(d), row sum, P_t(j)
@@ -84,11 +85,23 @@ struct AttnCfg {
     static constexpr int kQBytes = kBQ * D * 2;       // per tile: kAtoms atoms
     static constexpr int kKBytes = kBKV * D * 2;      // kAtoms atoms, N = keys
     static constexpr int kVBytes = kBKV * D * 2;      // [64-key half][64-d sub-tile]
-    static constexpr int kNumBars = 1 + 2 * kStages + kTiles * kStages + kTiles * (2 * kSBufs + 2) + 2;
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * kTiles * kStages + kTiles * (2 * kSBufs + 2) + 2;
     static constexpr int kSmemBytes =
         1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
-    static constexpr int kThreads = 32 * (3 + 4 * kTiles);   // producer, two MMA warps,
-                                                              // softmax warpgroups
+    // Warpgroup 0: the producer, the two MMA warps and one idle warp; then one
+    // softmax warpgroup per tile (warpgroup-aligned, for the register split).
+    static constexpr int kThreads = 32 * (4 + 4 * kTiles);
+    // With two tiles (384 threads) the launch allows at most 168 registers a
+    // thread, fewer than a softmax thread's 128 scores and 64 packed weights
+    // need: warpgroup 0 gives registers back (setmaxnreg.dec to kRegsLow) and
+    // the softmax warpgroups take them (setmaxnreg.inc to kRegsHigh).  The
+    // increase waits until the decrease has freed enough, so the split needs
+    // 128 kRegsLow + 256 kRegsHigh <= 384 x the launch's registers a thread,
+    // i.e. at least kRegsMinLaunch; the launcher checks that before launching.
+    static constexpr bool kRegSplit = kTiles == 2;
+    static constexpr int kRegsLow = 40;
+    static constexpr int kRegsHigh = 208;
+    static constexpr int kRegsMinLaunch = (128 * kRegsLow + 256 * kRegsHigh + 383) / 384;
     static_assert(D == 64 || D == 128, "head dimension");
     static_assert(kSmemBytes <= 232448, "shared memory");
     static_assert(kTmemO + D <= kTmemTile || kTiles == 1, "TMEM per tile");
@@ -131,13 +144,14 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     uint64_t* q_full = bars;
     uint64_t* k_full = q_full + 1;
     uint64_t* v_full = k_full + kStages;
-    uint64_t* kv_empty = v_full + kStages;               // [tile][stage]
-    uint64_t* s_full = kv_empty + kTiles * kStages;      // [tile][score buffer]
+    uint64_t* k_empty = v_full + kStages;                // [tile][stage]
+    uint64_t* v_empty = k_empty + kTiles * kStages;      // [tile][stage]
+    uint64_t* s_full = v_empty + kTiles * kStages;       // [tile][score buffer]
     uint64_t* s_empty = s_full + kTiles * kSBufs;
     uint64_t* p_full = s_empty + kTiles * kSBufs;
     uint64_t* pv_done = p_full + kTiles;
     uint64_t* drain = pv_done + kTiles;                  // [MMA warp]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kTiles);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -169,7 +183,10 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             dg::mbar_init(dg::smem_u32(&k_full[s]), 1u);
             dg::mbar_init(dg::smem_u32(&v_full[s]), 1u);
         }
-        for (int s = 0; s < kTiles * kStages; ++s) dg::mbar_init(dg::smem_u32(&kv_empty[s]), 1u);
+        for (int s = 0; s < kTiles * kStages; ++s) {
+            dg::mbar_init(dg::smem_u32(&k_empty[s]), 1u);
+            dg::mbar_init(dg::smem_u32(&v_empty[s]), 1u);
+        }
         for (int t = 0; t < kTiles; ++t) {
             for (int b = 0; b < kSBufs; ++b) {
                 dg::mbar_init(dg::smem_u32(&s_full[t * kSBufs + b]), 1u);
@@ -202,16 +219,29 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
         *abort_flag = 1;
         atomicExch(&g_attn_status, 1);
     };
+    if constexpr (Cfg::kRegSplit) {
+        if (warp < 4)
+            dg::setmaxnreg_dec<Cfg::kRegsLow>();
+        else
+            dg::setmaxnreg_inc<Cfg::kRegsHigh>();
+    }
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint32_t qb = dg::smem_u32(q_full);
-            dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
-            for (int t = 0; t < kTiles; ++t)
-                for (int a = 0; a < kAtoms; ++a)
-                    dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes + a * kAtomBytes), &mapQ, qb,
-                                    64 * a, (pair * kTiles + t) * kBQ, h);
+        // Lane 0 loads the Q tiles, then K blocks; lane 1 the V blocks.  A K
+        // stage is freed by the S MMAs that read it, a V stage by the P V MMAs,
+        // so K runs ahead of the P V products.
+        if (lane < 2) {
+            const bool k_lane = lane == 0;
+            if (k_lane) {
+                const uint32_t qb = dg::smem_u32(q_full);
+                dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
+                for (int t = 0; t < kTiles; ++t)
+                    for (int a = 0; a < kAtoms; ++a)
+                        dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes + a * kAtomBytes), &mapQ, qb,
+                                        64 * a, (pair * kTiles + t) * kBQ, h);
+            }
+            uint64_t* empty = k_lane ? k_empty : v_empty;
             bool ok = true;
             for (int j = 0; ok && j < nkv_max; ++j) {
                 const int st = j % kStages;
@@ -219,25 +249,28 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                 // The stage held block j - kStages: every tile that used it must be done.
                 for (int t = 0; t < kTiles; ++t)
                     if (j >= kStages && j - kStages < nkv[t] &&
-                        !dg::mbar_wait(dg::smem_u32(&kv_empty[t * kStages + st]), ph ^ 1u,
-                                       abort_flag, p.timeout_ns))
+                        !dg::mbar_wait(dg::smem_u32(&empty[t * kStages + st]), ph ^ 1u, abort_flag,
+                                       p.timeout_ns))
                         ok = false;
                 if (!ok) {
                     fail();
                     break;
                 }
-                const uint32_t kb = dg::smem_u32(&k_full[st]);
-                dg::mbar_arrive_expect_tx(kb, kKBytes);
-                for (int a = 0; a < kAtoms; ++a)
-                    dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes + a * kAtomBytes), &mapK, kb,
-                                    64 * a, j * kBKV, h);
-                const uint32_t vb = dg::smem_u32(&v_full[st]);
-                dg::mbar_arrive_expect_tx(vb, kVBytes);
-                const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
-                for (int hh = 0; hh < 2; ++hh)
+                if (k_lane) {
+                    const uint32_t kb = dg::smem_u32(&k_full[st]);
+                    dg::mbar_arrive_expect_tx(kb, kKBytes);
                     for (int a = 0; a < kAtoms; ++a)
-                        dg::tma_load_3d(vdst + (hh * kAtoms + a) * kSubBytes, &mapV, vb, 64 * a,
-                                        j * kBKV + hh * (kBKV / 2), h);
+                        dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes + a * kAtomBytes), &mapK, kb,
+                                        64 * a, j * kBKV, h);
+                } else {
+                    const uint32_t vb = dg::smem_u32(&v_full[st]);
+                    dg::mbar_arrive_expect_tx(vb, kVBytes);
+                    const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
+                    for (int hh = 0; hh < 2; ++hh)
+                        for (int a = 0; a < kAtoms; ++a)
+                            dg::tma_load_3d(vdst + (hh * kAtoms + a) * kSubBytes, &mapV, vb, 64 * a,
+                                            j * kBKV + hh * (kBKV / 2), h);
+                }
             }
         }
         __syncwarp();
@@ -281,6 +314,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                                            dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
                                            idesc_s, k16 > 0 ? 1u : 0u);
                         dg::tc_commit(dg::smem_u32(&s_full[t * kSBufs + b]));
+                        dg::tc_commit(dg::smem_u32(&k_empty[t * kStages + jj % kStages]));
                     }
                 }
             } else {
@@ -307,9 +341,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                                                                      k16 & 3),
                                               idesc_pv, (j > 0 || k16 > 0) ? 1u : 0u);
                         dg::tc_commit(dg::smem_u32(&pv_done[t]));
-                        // K_j and V_j of this stage are free once this tile is done
-                        // with them (its S_t(j) finished before P_t(j) existed).
-                        dg::tc_commit(dg::smem_u32(&kv_empty[t * kStages + st]));
+                        dg::tc_commit(dg::smem_u32(&v_empty[t * kStages + st]));
                     }
                 }
             }
@@ -322,9 +354,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             dg::mbar_wait(dg::smem_u32(my_drain), 0u, &never, 100000000ull);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax
-        const int t = (warp - 3) >> 2;                  // query tile of this warpgroup
+        const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;              // query row in the tile == TMEM lane
         const int qrow = (pair * kTiles + t) * kBQ + r;
@@ -695,6 +727,17 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
                                      smem_bytes) != cudaSuccess) {
                 (void)cudaGetLastError();
                 return GEMM_ERR_CUDA;
+            }
+            // The register split of the two-tile kernel needs this many
+            // registers a thread at launch (otherwise its increase would wait
+            // forever): refuse to launch a build that has fewer.
+            if (d64) {
+                cudaFuncAttributes fa{};
+                if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) {
+                    (void)cudaGetLastError();
+                    return GEMM_ERR_CUDA;
+                }
+                if (fa.numRegs < AttnCfg<64>::kRegsMinLaunch) return GEMM_ERR_UNSUPPORTED;
             }
             g_attr_set[which] = true;
         }

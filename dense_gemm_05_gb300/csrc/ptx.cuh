@@ -361,6 +361,20 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Warpgroup register reallocation: every warp of the warpgroup executes the
+// same one.  dec lowers the warp's registers a thread to N and returns the
+// rest to the CTA's pool; inc waits until the pool can raise it to N.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "register count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // max(a, b, c) in one instruction (three-input max.f32).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
