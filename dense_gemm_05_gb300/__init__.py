@@ -78,7 +78,7 @@ ABI_FUNCTIONS = ("gemm_plan_create", "gemm_run", "gemm_plan_destroy", "gemm_stat
                  "softmax_rows", "softmax_rows_query", "attention_fwd", "attention_fwd_query",
                  "gemm_plan_create_model", "gemm_noop_launch", "gemm_plan_set_staging",
                  "gemm_plan_set_debug", "gemm_partition", "gemm_run_slice",
-                 "gemm_build_checked", "gemm_plan_device_status")
+                 "gemm_build_checked", "gemm_plan_device_status", "attention_set_debug")
 
 GEMM_SPLIT_AUTO = -1
 GEMM_SPLIT_M = 0
@@ -179,6 +179,8 @@ def lib() -> ctypes.CDLL:
         L.gemm_plan_set_staging.restype = i32
         L.gemm_plan_set_debug.argtypes = [vp, i32, ctypes.c_uint64]
         L.gemm_plan_set_debug.restype = i32
+        L.attention_set_debug.argtypes = [i32, ctypes.c_uint64]
+        L.attention_set_debug.restype = i32
         L.gemm_build_checked.argtypes = []
         L.gemm_build_checked.restype = i32
         L.gemm_plan_device_status.argtypes = [vp, ctypes.POINTER(i32)]
@@ -292,6 +294,12 @@ def gemm_plan_set_debug(plan: int, sync: int, timeout_ns: int = 0) -> int:
     """Debug-sync mode (gemm_run waits and reports device-side give-ups) and the
     limit of every bounded device wait (0 = the default)."""
     return int(lib().gemm_plan_set_debug(plan, int(sync), int(timeout_ns)))
+
+
+def attention_set_debug(sync: int, timeout_ns: int = 0) -> int:
+    """Process-wide debug settings of attention_fwd: sync 1 / 0 / -1 (= as
+    GEMM_DEBUG_SYNC says) and the limit of every bounded device wait (0 = default)."""
+    return int(lib().attention_set_debug(int(sync), int(timeout_ns)))
 
 
 def gemm_build_checked() -> int:

@@ -71,6 +71,20 @@ GEMM_API gemm_status_t attention_fwd_query(const void* Q, const void* K, const v
                                            gemm_dtype_t dtype, int32_t out_type,
                                            attention_config_t* out);
 
+/*
+ * Debug settings of every later attention_fwd call in the process (not tied to
+ * a stream or thread; for tests).  sync = 1: the call waits for its kernel and
+ * returns GEMM_ERR_TIMEOUT when a bounded device-side wait gave up; sync = 0:
+ * no waiting, whatever GEMM_DEBUG_SYNC says; sync = -1: as GEMM_DEBUG_SYNC says
+ * (the initial setting).  timeout_ns: the limit of every
+ * bounded wait in the kernel, 0 = the default of 2 s.  A wait that gives up
+ * stops its CTA after its MMAs have completed; O is then incomplete, and the
+ * context stays usable.  A limit far below a launch's run time makes real
+ * launches give up (a few to a few tens of microseconds after the limit).
+ * Errors: INVALID_ARG (sync not -1, 0 or 1).
+ */
+GEMM_API gemm_status_t attention_set_debug(int32_t sync, uint64_t timeout_ns);
+
 #ifdef __cplusplus
 }
 #endif

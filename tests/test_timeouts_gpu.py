@@ -8,7 +8,7 @@ GEMM_ERR_TIMEOUT.  The next GEMM on the same context, with the default limit,
 must then match the oracle -- the context stays usable and no state (tile
 counters, partial tiles) leaks into it.  Kernels covered: the 2-SM pair kernel
 with its stream-K phase, the one-CTA kernel, the swap-AB stream-K kernel with
-split tiles, and the split-K cluster kernel.
+split tiles, and the split-K cluster kernel; and the attention kernel (both head dimensions).
 
 The allocation path is tested on the host: GEMM_TEST_FAIL_ALLOC=k makes the
 k-th device allocation of gemm_plan_create fail, which must return
@@ -88,6 +88,47 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_survives(plan, M, K, N
     plan.run(a, b, c)
     torch.cuda.synchronize()
     check_sampled(c, A, B, M, N, K, seed=M + N + 1)
+
+
+@pytest.mark.parametrize("name", ["attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d128_bf16_causal"])
+def test_attention_wait_that_runs_out_is_reported_and_the_context_survives(plan, name):
+    """The attention kernel's roles (the K and V producer lanes, the S and P V
+    issuers, the softmax warpgroups): a 2 us limit makes a full-size launch give
+    up; the next launch with the default limit must match the oracle."""
+    from oracle import attention as oa
+    w = workloads.ATTN_WORKLOADS[name]
+    Q, K, V = workloads.make_qkv(w)
+    dev = torch.device("cuda:0")
+    q, k, v = Q.to(dev), K.to(dev), V.to(dev)
+    o = torch.full((w.BH, w.seq, w.d), float("nan"), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    BH, seq, d = w.BH, w.seq, w.d
+    try:
+        assert g.attention_set_debug(1, SHORT_NS) == g.GEMM_OK
+        st = g.attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), BH, seq, d, d,
+                             seq * d, d, seq * d, int(w.causal), g.GEMM_BF16, 0, stream)
+        assert st == g.GEMM_ERR_TIMEOUT, g.status_string(st)
+        assert g.attention_set_debug(1, 0) == g.GEMM_OK      # default limit, still synchronous
+        o.fill_(float("nan"))
+        st = g.attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), BH, seq, d, d,
+                             seq * d, d, seq * d, int(w.causal), g.GEMM_BF16, 0, stream)
+        assert st == g.GEMM_OK, g.status_string(st)
+    finally:
+        g.attention_set_debug(-1, 0)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o).any(), "an entry of O was not written"
+    for head in (0, BH - 1):
+        rows = np.linspace(0, seq - 1, 48).astype(np.int64)
+        ref = oa.attention_rows(Q, K, V, w.causal, head, rows)
+        got = o[head].cpu().double().numpy()[rows]
+        scale = np.abs(ref).max()
+        assert np.abs(got - ref).max() <= 1e-2 * scale, f"head {head}"
+
+
+def test_attention_debug_settings_are_checked():
+    assert g.attention_set_debug(2, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.attention_set_debug(-2, 0) == g.GEMM_ERR_INVALID_ARG
+    assert g.attention_set_debug(-1, 0) == g.GEMM_OK
 
 
 def test_debug_settings_are_checked(plan):
