@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
 
     auto fail = [&]() {
         *abort_flag = 1;
-        atomicExch(&g_attn_status, 1);
+        atomicOr(&g_attn_status, dg::kDevTimeout);
     };
     if constexpr (Cfg::kRegSplit) {
         if (warp < 4)
@@ -506,7 +506,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[ch * 32 + i] = __float_as_uint(__uint_as_float(v[i]) * inv);
             }
-            if (qrow < p.seq) {
+            // A checked build tests the row against the sequence first.
+            if (qrow < p.seq &&
+                DG_CHECK(&g_attn_status, dg::kChkC, dg::span_inside(qrow, 0, kD, p.seq, kD))) {
                 const int64_t off = int64_t(h) * p.hso + int64_t(qrow) * p.ldo;
                 if (p.out_type == dg::kOutF32) {
                     float* dst = static_cast<float*>(p.O) + off;
@@ -793,7 +795,7 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
         if (status != 0) {
             const int zero = 0;
             (void)cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int));
-            return GEMM_ERR_TIMEOUT;
+            return (status & dg::kDevBounds) ? GEMM_ERR_BOUNDS : GEMM_ERR_TIMEOUT;
         }
     }
     return GEMM_OK;

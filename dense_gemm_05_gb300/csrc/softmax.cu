@@ -95,9 +95,15 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
 // Load the W floats of one chunk that starts at column col (-inf beyond N).
 // NC: through the read-only data path (ld.global.nc), which measured faster
 // for the 512-thread rows; otherwise a streaming load (ld.global.cs).
+// row = X + r * ldx; a checked build tests each load against the M x N matrix.
 template <int W, bool NC = false>
-__device__ __forceinline__ void load_chunk(const float* row, int64_t col, int64_t N, float* v) {
+__device__ __forceinline__ void load_chunk(const float* row, int64_t r, int64_t M, int64_t col,
+                                           int64_t N, float* v) {
     if (W == 4 && col + 3 < N) {
+        if (!DG_CHECK(&g_softmax_status, dg::kChkA, dg::span_inside(r, col, 4, M, N))) {
+            v[0] = v[1] = v[2] = v[3] = -INFINITY;
+            return;
+        }
         const float4* p = reinterpret_cast<const float4*>(row + col);
         const float4 q = NC ? __ldg(p) : __ldcs(p);
         v[0] = q.x;
@@ -107,18 +113,26 @@ __device__ __forceinline__ void load_chunk(const float* row, int64_t col, int64_
     } else {
 #pragma unroll
         for (int e = 0; e < W; ++e)
-            v[e] = (col + e < N) ? (NC ? __ldg(row + col + e) : __ldcs(row + col + e)) : -INFINITY;
+            v[e] = (col + e < N &&
+                    DG_CHECK(&g_softmax_status, dg::kChkA, dg::span_inside(r, col + e, 1, M, N)))
+                       ? (NC ? __ldg(row + col + e) : __ldcs(row + col + e))
+                       : -INFINITY;
     }
 }
 
+// row = Y + r * ldy; a checked build tests each store against the M x N matrix.
 template <int W>
-__device__ __forceinline__ void store_chunk(float* row, int64_t col, int64_t N, const float* v) {
+__device__ __forceinline__ void store_chunk(float* row, int64_t r, int64_t M, int64_t col, int64_t N,
+                                            const float* v) {
     if (W == 4 && col + 3 < N) {
-        __stcs(reinterpret_cast<float4*>(row + col), make_float4(v[0], v[1], v[2], v[3]));
+        if (DG_CHECK(&g_softmax_status, dg::kChkC, dg::span_inside(r, col, 4, M, N)))
+            __stcs(reinterpret_cast<float4*>(row + col), make_float4(v[0], v[1], v[2], v[3]));
     } else {
 #pragma unroll
         for (int e = 0; e < W; ++e)
-            if (col + e < N) __stcs(row + col + e, v[e]);
+            if (col + e < N &&
+                DG_CHECK(&g_softmax_status, dg::kChkC, dg::span_inside(r, col + e, 1, M, N)))
+                __stcs(row + col + e, v[e]);
     }
 }
 
@@ -143,7 +157,7 @@ __global__ void __launch_bounds__(TPR == 32 ? kWarpRowsBlock : TPR)
         float v[kE];
 #pragma unroll
         for (int j = 0; j < C; ++j)
-            load_chunk<W, (TPR > 32)>(xr, int64_t(j * TPR + t) * W, N, v + j * W);
+            load_chunk<W, (TPR > 32)>(xr, r, M, int64_t(j * TPR + t) * W, N, v + j * W);
 
         // Max
         float m = -INFINITY;
@@ -165,7 +179,7 @@ __global__ void __launch_bounds__(TPR == 32 ? kWarpRowsBlock : TPR)
 #pragma unroll
         for (int i = 0; i < kE; ++i) v[i] *= inv;
 #pragma unroll
-        for (int j = 0; j < C; ++j) store_chunk<W>(yr, int64_t(j * TPR + t) * W, N, v + j * W);
+        for (int j = 0; j < C; ++j) store_chunk<W>(yr, r, M, int64_t(j * TPR + t) * W, N, v + j * W);
     }
 }
 
@@ -220,11 +234,12 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
                 if (!dg::mbar_wait(dg::smem_u32(&empty[slot]), (k & 1u) ^ 1u, &abort_flag,
                                    timeout_ns)) {
                     abort_flag = 1;
-                    atomicExch(&g_softmax_status, 1);
+                    atomicOr(&g_softmax_status, dg::kDevTimeout);
                     break;
                 }
                 const uint32_t fb = dg::smem_u32(&full[slot]);
-                if (bulk_bytes == 0u) {
+                if (bulk_bytes == 0u ||
+                    !DG_CHECK(&g_softmax_status, dg::kChkA, dg::span_inside(r0 + i, 0, n4, M, N))) {
                     dg::mbar_arrive(fb);
                     continue;
                 }
@@ -250,7 +265,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
             if (GROUPED) ok = dg::named_bar_and(1, kTpr, ok);
             if (!ok) {
                 abort_flag = 1;
-                atomicExch(&g_softmax_status, 1);
+                atomicOr(&g_softmax_status, dg::kDevTimeout);
                 break;
             }
             const float* srow = reinterpret_cast<const float*>(smem + size_t(slot) * slot_bytes);
@@ -268,7 +283,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        v[4 * j + e] = (col + e < N) ? __ldcs(xr + col + e) : -INFINITY;
+                        v[4 * j + e] = (col + e < N && DG_CHECK(&g_softmax_status, dg::kChkA,
+                                                                 dg::span_inside(r0 + i, col + e, 1, M, N)))
+                                           ? __ldcs(xr + col + e)
+                                           : -INFINITY;
                 }
             }
             // Max (the group's barrier also orders every thread's slot reads
@@ -312,12 +330,15 @@ __global__ void __launch_bounds__(32 * (NW + 1), 1)
             for (int j = 0; j < CPL; ++j) {
                 const int64_t col = int64_t(j * kTpr + t) * 4;
                 if (y_vec && col + 3 < N) {
-                    __stcs(reinterpret_cast<float4*>(yr + col),
-                           make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                    if (DG_CHECK(&g_softmax_status, dg::kChkC, dg::span_inside(r0 + i, col, 4, M, N)))
+                        __stcs(reinterpret_cast<float4*>(yr + col),
+                               make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (col + e < N) __stcs(yr + col + e, v[4 * j + e]);
+                        if (col + e < N &&
+                            DG_CHECK(&g_softmax_status, dg::kChkC, dg::span_inside(r0 + i, col + e, 1, M, N)))
+                            __stcs(yr + col + e, v[4 * j + e]);
                 }
             }
         }
@@ -354,7 +375,7 @@ __global__ void __launch_bounds__(kStreamThreads)
             float v[kStreamSlab];
 #pragma unroll
             for (int j = 0; j < kChunks; ++j)
-                load_chunk<W>(xr, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
+                load_chunk<W>(xr, r, M, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
             float mm = m;
 #pragma unroll
             for (int i = 0; i < kStreamSlab; ++i) mm = max_nan(mm, v[i]);
@@ -372,12 +393,12 @@ __global__ void __launch_bounds__(kStreamThreads)
             float v[kStreamSlab];
 #pragma unroll
             for (int j = 0; j < kChunks; ++j)
-                load_chunk<W>(xr, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
+                load_chunk<W>(xr, r, M, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
 #pragma unroll
             for (int i = 0; i < kStreamSlab; ++i) v[i] = expf(v[i] - mr) * inv;
 #pragma unroll
             for (int j = 0; j < kChunks; ++j)
-                store_chunk<W>(yr, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
+                store_chunk<W>(yr, r, M, base + int64_t(j * kStreamThreads + t) * W, N, v + j * W);
         }
     }
 }
@@ -621,7 +642,7 @@ gemm_status_t softmax_rows(const float* X, int64_t ldx, float* Y, int64_t ldy, i
         if (status != 0) {
             const int zero = 0;
             (void)cudaMemcpyToSymbol(g_softmax_status, &zero, sizeof(int));
-            return GEMM_ERR_TIMEOUT;
+            return (status & dg::kDevBounds) ? GEMM_ERR_BOUNDS : GEMM_ERR_TIMEOUT;
         }
     }
     return GEMM_OK;

@@ -30,7 +30,8 @@
  *
  * Ownership: the caller owns all buffers and the stream; nothing is allocated
  * and nothing synchronises (unless GEMM_DEBUG_SYNC=1: then the call waits and
- * reports a device-side wait that gave up as GEMM_ERR_TIMEOUT).
+ * reports a device-side wait that gave up as GEMM_ERR_TIMEOUT, and in the
+ * checked build an O store outside its rows as GEMM_ERR_BOUNDS).
  *
  * Errors: GEMM_ERR_INVALID_ARG for null pointers (when BH*seq > 0), negative
  * sizes, ld < d, ldo < d, misaligned pointers, or O overlapping Q, K or V;

@@ -272,7 +272,8 @@ GEMM_API gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint6
 /*
  * Checked builds.  The same sources compiled with DG_CHECKED=1 give a second
  * library, libgemm_checked.so, with this same ABI.  In it every ordinary
- * (non-TMA) global load and store of the kernels first tests the range it
+ * (non-TMA) global load and store of the kernels (the GEMM kernels, and those of
+ * softmax.h and attention.h) first tests the range it
  * touches against the matrix or buffer it belongs to: A, B and C against the
  * rows x columns rectangles the caller passed (so a row's padding between N and
  * ldc counts as outside), the staging copy against its source and destination,
@@ -281,7 +282,8 @@ GEMM_API gemm_status_t gemm_plan_set_debug(gemm_plan_t plan, int32_t sync, uint6
  * of the plan's device status word: 2 (out of range) plus one bit per kind of
  * access, 1<<8 C store, 1<<9 A load, 1<<10 B load, 1<<11 workspace,
  * 1<<12 tile counter, 1<<13 staging copy.  A debug-sync gemm_run (see
- * gemm_plan_set_debug) then returns GEMM_ERR_BOUNDS; without debug-sync the
+ * gemm_plan_set_debug) then returns GEMM_ERR_BOUNDS (softmax_rows and
+ * attention_fwd likewise under GEMM_DEBUG_SYNC=1); without debug-sync the
  * word is cleared unread by the next debug-sync call.  A partial tile whose
  * workspace range fails stops its kernel as a wait that gave up does.  TMA copies
  * are not tested: their tensor maps bound them in hardware (elements outside

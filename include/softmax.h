@@ -28,8 +28,11 @@
  * NaN, comes out NaN.
  *
  * Ownership: the caller owns X, Y (device memory, 4-byte aligned) and the
- * stream; nothing is allocated and the call does not synchronise.  Work runs
- * on the current CUDA device, which must be compute capability 10.3.
+ * stream; nothing is allocated and the call does not synchronise (unless
+ * GEMM_DEBUG_SYNC=1: then it waits and reports a bounded device-side wait that
+ * gave up as GEMM_ERR_TIMEOUT, and in the checked build a load or store outside
+ * the M x N matrices as GEMM_ERR_BOUNDS).  Work runs on the current CUDA
+ * device, which must be compute capability 10.3.
  *
  * Errors: GEMM_ERR_INVALID_ARG for a null pointer when M*N > 0, negative M or
  * N, ldx < N or ldy < N, a misaligned pointer, or X and Y overlapping other

@@ -3,12 +3,13 @@
 The checked build (``libgemm_checked.so``) tests every ordinary global load and
 store of the kernels against the matrix or buffer it belongs to and skips any
 that falls outside, recording it in the plan's status word; with debug-sync on,
-gemm_run then returns GEMM_ERR_BOUNDS, which the binding raises.  The GEMM
-parity suites -- every kernel, layout, staged and in-place operand, ragged
-edge, output type, partition slice and sampled full-size case -- are run in a
-child process with DG_GEMM_CHECKED=1 and GEMM_DEBUG_SYNC=1: they must pass
-there unchanged, i.e. no access of any of their launches leaves its range and
-the results still match the oracle.
+gemm_run (and softmax_rows, attention_fwd) then return GEMM_ERR_BOUNDS, which
+the binding raises.  The GEMM parity suites -- every kernel, layout, staged and
+in-place operand, ragged edge, output type, partition slice and sampled
+full-size case -- and the softmax and attention suites are run in a child
+process with DG_GEMM_CHECKED=1 and GEMM_DEBUG_SYNC=1: they must pass there
+unchanged, i.e. no access of any of their launches leaves its range and the
+results still match the oracle.
 """
 import os
 import subprocess
@@ -23,7 +24,8 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gemm_gpu.py", "tests/test_layouts_gpu.py", "tests/test_partition_gpu.py",
-          "tests/test_large_gpu.py", "tests/test_fuzz_gpu.py"]
+          "tests/test_large_gpu.py", "tests/test_fuzz_gpu.py", "tests/test_softmax_gpu.py",
+          "tests/test_attention_gpu.py"]
 
 
 def test_the_checked_library_is_the_one_loaded():
@@ -38,7 +40,7 @@ def test_the_checked_library_is_the_one_loaded():
         p.close()
 
 
-def test_gemm_suites_pass_on_the_checked_build():
+def test_parity_suites_pass_on_the_checked_build():
     if g.checked_requested():
         pytest.skip("this is the checked child process")
     if not torch.cuda.is_available():
