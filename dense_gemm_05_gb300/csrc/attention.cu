@@ -17,17 +17,19 @@
 // and B sharing every K/V block) query tiles of one head; TMEM per tile: the
 // score buffers S (two at d = 128, one at d = 64), P and O:
 //   warp 0      TMA producers: lane 0 the Q tiles once, then K blocks, lane 1
-//               V blocks, each into a 3-stage ring (3-D tensor maps over
-//               [BH, seq, d]).
+//               V blocks, each into a ring of 4 (d = 64) or 3 (d = 128)
+//               stages (3-D tensor maps over [BH, seq, d]).
 //   warp 1      S issuer (also owns TMEM): S_t(j) = Q_t K_j^T (M 128, N 128,
 //               K d) into score buffer j % kSBufs of tile t once K_j has
 //               landed and the tile's softmax has read that buffer.
-//   warp 2      P V issuer: O_t += P_t(j) V_j (M 128, N d, K 128) with P_t(j)
-//               read from TMEM once the softmax has stored it there.  With
-//               the two kinds on separate warps neither waits behind the
-//               other.  A K stage is refilled when every tile's S MMAs that
-//               read it have completed, a V stage when its P V MMAs have.
-//   warps 3..   one softmax warpgroup per tile, one thread per query row
+//   warp 2 + t  P V issuer of tile t: O_t += P_t(j) V_j (M 128, N d, K 128)
+//               with P_t(j) read from TMEM once the softmax has stored it
+//               there.  With S and each tile's P V on separate warps no MMA
+//               waits behind another that is not ready.  A K stage is
+//               refilled when every tile's S MMAs that read it have
+//               completed, a V stage when its P V MMAs have.  (Warp 3 is idle
+//               at d = 128.)
+//   warps 4..   one softmax warpgroup per tile, one thread per query row
 //               (= TMEM lane): read S_t(j) from TMEM, mask, row max,
 //               p = 2^(s*c - m*c) with c = log2(e)/sqrt(d), row sum, P_t(j)
 //               rounded to the input type into TMEM (the A operand of the
@@ -88,11 +90,12 @@ struct AttnCfg {
     static constexpr int kQBytes = kBQ * D * 2;       // per tile: kAtoms atoms
     static constexpr int kKBytes = kBKV * D * 2;      // kAtoms atoms, N = keys
     static constexpr int kVBytes = kBKV * D * 2;      // [64-key half][64-d sub-tile]
-    static constexpr int kNumBars = 1 + 2 * kStages + 2 * kTiles * kStages + kTiles * (2 * kSBufs + 2) + 2;
+    static constexpr int kNumBars = 1 + 2 * kStages + 2 * kTiles * kStages + kTiles * (2 * kSBufs + 3) + 1;
     static constexpr int kSmemBytes =
         1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + 8 * kNumBars + 16;
-    // Warpgroup 0: the producer, the two MMA warps and one idle warp; then one
-    // softmax warpgroup per tile (warpgroup-aligned, for the register split).
+    // Warpgroup 0: the producer warp, the S warp and one P V warp per tile (one
+    // idle warp at d = 128); then one softmax warpgroup per tile
+    // (warpgroup-aligned, for the register split).
     static constexpr int kThreads = 32 * (4 + 4 * kTiles);
     // With two tiles (384 threads) the launch allows at most 168 registers a
     // thread, fewer than a softmax thread's 128 scores and 64 packed weights
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     uint64_t* s_empty = s_full + kTiles * kSBufs;
     uint64_t* p_full = s_empty + kTiles * kSBufs;
     uint64_t* pv_done = p_full + kTiles;
-    uint64_t* drain = pv_done + kTiles;                  // [MMA warp]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+    uint64_t* drain = pv_done + kTiles;                  // [S issuer, then P V issuer t]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1 + kTiles);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             dg::mbar_init(dg::smem_u32(&p_full[t]), 128u);
             dg::mbar_init(dg::smem_u32(&pv_done[t]), 1u);
         }
-        for (int w = 0; w < 2; ++w) dg::mbar_init(dg::smem_u32(&drain[w]), 1u);
+        for (int w = 0; w < 1 + kTiles; ++w) dg::mbar_init(dg::smem_u32(&drain[w]), 1u);
         *abort_flag = 0;
         dg::fence_mbar_init();
     }
@@ -223,117 +226,116 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
         *abort_flag = 1;
         atomicOr(&g_attn_status, dg::kDevTimeout);
     };
-    if constexpr (Cfg::kRegSplit) {
-        if (warp < 4)
-            dg::setmaxnreg_dec<Cfg::kRegsLow>();
-        else
-            dg::setmaxnreg_inc<Cfg::kRegsHigh>();
-    }
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
-        // Lane 0 loads the Q tiles, then K blocks; lane 1 the V blocks.  A K
-        // stage is freed by the S MMAs that read it, a V stage by the P V MMAs,
-        // so K runs ahead of the P V products.
-        if (lane < 2) {
-            const bool k_lane = lane == 0;
-            if (k_lane) {
-                const uint32_t qb = dg::smem_u32(q_full);
-                dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
-                for (int t = 0; t < kTiles; ++t)
-                    for (int a = 0; a < kAtoms; ++a)
-                        dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes + a * kAtomBytes), &mapQ, qb,
-                                        64 * a, (pair * kTiles + t) * kBQ, h);
-            }
-            uint64_t* empty = k_lane ? k_empty : v_empty;
-            bool ok = true;
-            for (int j = 0; ok && j < nkv_max; ++j) {
-                const int st = j % kStages;
-                const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
-                // The stage held block j - kStages: every tile that used it must be done.
-                for (int t = 0; t < kTiles; ++t)
-                    if (j >= kStages && j - kStages < nkv[t] &&
-                        !dg::mbar_wait(dg::smem_u32(&empty[t * kStages + st]), ph ^ 1u, abort_flag,
-                                       p.timeout_ns))
-                        ok = false;
-                if (!ok) {
-                    fail();
-                    break;
-                }
+    if (warp < 4) {
+        // Warpgroup 0: each register-split instruction heads the code of the
+        // warpgroup that executes it, so the compiler sizes each side by it.
+        if constexpr (Cfg::kRegSplit) dg::setmaxnreg_dec<Cfg::kRegsLow>();
+        if (warp == 0) {
+            // ------------------------------------------------------------ TMA producer
+            // Lane 0 loads the Q tiles, then K blocks; lane 1 the V blocks.  A K
+            // stage is freed by the S MMAs that read it, a V stage by the P V MMAs,
+            // so K runs ahead of the P V products.
+            if (lane < 2) {
+                const bool k_lane = lane == 0;
                 if (k_lane) {
-                    const uint32_t kb = dg::smem_u32(&k_full[st]);
-                    dg::mbar_arrive_expect_tx(kb, kKBytes);
-                    for (int a = 0; a < kAtoms; ++a)
-                        dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes + a * kAtomBytes), &mapK, kb,
-                                        64 * a, j * kBKV, h);
-                } else {
-                    const uint32_t vb = dg::smem_u32(&v_full[st]);
-                    dg::mbar_arrive_expect_tx(vb, kVBytes);
-                    const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
-                    for (int hh = 0; hh < 2; ++hh)
+                    const uint32_t qb = dg::smem_u32(q_full);
+                    dg::mbar_arrive_expect_tx(qb, kTiles * kQBytes);
+                    for (int t = 0; t < kTiles; ++t)
                         for (int a = 0; a < kAtoms; ++a)
-                            dg::tma_load_3d(vdst + (hh * kAtoms + a) * kSubBytes, &mapV, vb, 64 * a,
-                                            j * kBKV + hh * (kBKV / 2), h);
+                            dg::tma_load_3d(dg::smem_u32(sQ + t * kQBytes + a * kAtomBytes), &mapQ, qb,
+                                            64 * a, (pair * kTiles + t) * kBQ, h);
                 }
-            }
-        }
-        __syncwarp();
-    } else if (warp <= 2) {
-        // ------------------------------------------------------------ MMA issuers
-        // Warp 1 issues every tile's S_t(j) = Q_t K_j^T, warp 2 every tile's
-        // O_t += P_t(j) V_j, so that neither kind waits behind the other: an S
-        // MMA waiting for its K block or for its score buffer to be read never
-        // holds up a P V MMA whose P is ready, and back.  S_t(j) goes into
-        // score buffer j % kSBufs once the tile's softmax has read that buffer's
-        // previous scores; P_t(j) V_j once P_t(j) is in TMEM and V_j has landed.
-        const bool s_role = warp == 1;
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = dg::idesc_f16(BF16, false, false, kBQ, kBKV);
-            constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
-            bool ok = true;
-            if (s_role) {
-                ok = nkv_max == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
-                for (int jj = 0; ok && jj < nkv_max; ++jj) {
-                    const int b = jj % kSBufs;
-                    ok = dg::mbar_wait(dg::smem_u32(&k_full[jj % kStages]),
-                                       static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
-                                       p.timeout_ns);
-                    const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
-#pragma unroll
-                    for (int t = 0; t < kTiles; ++t) {
-                        if (!ok || jj >= nkv[t]) continue;
-                        // the buffer's (jj / kSBufs)-th use: its previous scores were read
-                        ok = dg::mbar_wait(dg::smem_u32(&s_empty[t * kSBufs + b]),
-                                           (static_cast<uint32_t>(jj / kSBufs) & 1u) ^ 1u, abort_flag,
-                                           p.timeout_ns);
-                        if (!ok) break;
-                        dg::tc_fence_after();
-                        const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
-                        const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile +
-                                                static_cast<uint32_t>(b) * kTmemS;
-#pragma unroll
-                        for (int k16 = 0; k16 < kD / 16; ++k16)
-                            dg::tc_mma_f16(s_tmem,
-                                           dg::operand_desc<false>(q_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
-                                           dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
-                                           idesc_s, k16 > 0 ? 1u : 0u);
-                        dg::tc_commit(dg::smem_u32(&s_full[t * kSBufs + b]));
-                        dg::tc_commit(dg::smem_u32(&k_empty[t * kStages + jj % kStages]));
-                    }
-                }
-            } else {
+                uint64_t* empty = k_lane ? k_empty : v_empty;
+                bool ok = true;
                 for (int j = 0; ok && j < nkv_max; ++j) {
                     const int st = j % kStages;
-                    ok = dg::mbar_wait(dg::smem_u32(&v_full[st]), static_cast<uint32_t>(j / kStages) & 1u,
-                                       abort_flag, p.timeout_ns);
-                    const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
+                    const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
+                    // The stage held block j - kStages: every tile that used it must be done.
+                    for (int t = 0; t < kTiles; ++t)
+                        if (j >= kStages && j - kStages < nkv[t] &&
+                            !dg::mbar_wait(dg::smem_u32(&empty[t * kStages + st]), ph ^ 1u, abort_flag,
+                                           p.timeout_ns))
+                            ok = false;
+                    if (!ok) {
+                        fail();
+                        break;
+                    }
+                    if (k_lane) {
+                        const uint32_t kb = dg::smem_u32(&k_full[st]);
+                        dg::mbar_arrive_expect_tx(kb, kKBytes);
+                        for (int a = 0; a < kAtoms; ++a)
+                            dg::tma_load_3d(dg::smem_u32(sK + st * kKBytes + a * kAtomBytes), &mapK, kb,
+                                            64 * a, j * kBKV, h);
+                    } else {
+                        const uint32_t vb = dg::smem_u32(&v_full[st]);
+                        dg::mbar_arrive_expect_tx(vb, kVBytes);
+                        const uint32_t vdst = dg::smem_u32(sV + st * kVBytes);
+                        for (int hh = 0; hh < 2; ++hh)
+                            for (int a = 0; a < kAtoms; ++a)
+                                dg::tma_load_3d(vdst + (hh * kAtoms + a) * kSubBytes, &mapV, vb, 64 * a,
+                                                j * kBKV + hh * (kBKV / 2), h);
+                    }
+                }
+            }
+            __syncwarp();
+        } else if (warp == 1 || warp - 2 < kTiles) {
+            // ------------------------------------------------------------ MMA issuers
+            // Warp 1 issues every tile's S_t(j) = Q_t K_j^T; warp 2 + t issues
+            // tile t's O_t += P_t(j) V_j.  So no P V MMA waits behind an S MMA
+            // that waits for its K block or for its score buffer to be read, nor
+            // behind the other tile's P.  S_t(j) goes into score buffer
+            // j % kSBufs once the tile's softmax has read that buffer's previous
+            // scores; P_t(j) V_j once P_t(j) is in TMEM and V_j has landed.  (An S
+            // issuer per tile, as two lanes of warp 1, measured slower.)
+            const bool s_role = warp == 1;
+            const int pv_tile = warp - 2;
+            if (lane == 0) {
+                constexpr uint32_t idesc_s = dg::idesc_f16(BF16, false, false, kBQ, kBKV);
+                constexpr uint32_t idesc_pv = dg::idesc_f16(BF16, false, true, kBQ, kD);
+                bool ok = true;
+                if (s_role) {
+                    ok = nkv_max == 0 || dg::mbar_wait(dg::smem_u32(q_full), 0u, abort_flag, p.timeout_ns);
+                    for (int jj = 0; ok && jj < nkv_max; ++jj) {
+                        const int b = jj % kSBufs;
+                        ok = dg::mbar_wait(dg::smem_u32(&k_full[jj % kStages]),
+                                           static_cast<uint32_t>(jj / kStages) & 1u, abort_flag,
+                                           p.timeout_ns);
+                        const uint32_t k_addr = dg::smem_u32(sK + (jj % kStages) * kKBytes);
 #pragma unroll
-                    for (int t = 0; t < kTiles; ++t) {
-                        if (!ok || j >= nkv[t]) continue;
-                        ok = dg::mbar_wait(dg::smem_u32(&p_full[t]), static_cast<uint32_t>(j) & 1u,
+                        for (int t = 0; t < kTiles; ++t) {
+                            if (!ok || jj >= nkv[t]) continue;
+                            // the buffer's (jj / kSBufs)-th use: its previous scores were read
+                            ok = dg::mbar_wait(dg::smem_u32(&s_empty[t * kSBufs + b]),
+                                               (static_cast<uint32_t>(jj / kSBufs) & 1u) ^ 1u, abort_flag,
+                                               p.timeout_ns);
+                            if (!ok) break;
+                            dg::tc_fence_after();
+                            const uint32_t q_addr = dg::smem_u32(sQ + t * kQBytes);
+                            const uint32_t s_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile +
+                                                    static_cast<uint32_t>(b) * kTmemS;
+#pragma unroll
+                            for (int k16 = 0; k16 < kD / 16; ++k16)
+                                dg::tc_mma_f16(s_tmem,
+                                               dg::operand_desc<false>(q_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                               dg::operand_desc<false>(k_addr + (k16 >> 2) * kAtomBytes, k16 & 3),
+                                               idesc_s, k16 > 0 ? 1u : 0u);
+                            dg::tc_commit(dg::smem_u32(&s_full[t * kSBufs + b]));
+                            dg::tc_commit(dg::smem_u32(&k_empty[t * kStages + jj % kStages]));
+                        }
+                    }
+                } else {
+                    const int t = pv_tile;
+                    const int n = t == 0 ? nkv[0] : nkv[kTiles - 1];
+                    for (int j = 0; ok && j < n; ++j) {
+                        const int st = j % kStages;
+                        ok = dg::mbar_wait(dg::smem_u32(&v_full[st]), static_cast<uint32_t>(j / kStages) & 1u,
+                                           abort_flag, p.timeout_ns) &&
+                             dg::mbar_wait(dg::smem_u32(&p_full[t]), static_cast<uint32_t>(j) & 1u,
                                            abort_flag, p.timeout_ns);
                         if (!ok) break;
                         dg::tc_fence_after();
+                        const uint32_t v_addr = dg::smem_u32(sV + st * kVBytes);
                         const uint32_t tile_tmem = tmem_base + static_cast<uint32_t>(t) * kTmemTile;
                         // P_t(j) from TMEM (8 columns = 16 keys per MMA), V_j from
                         // shared memory (N = d: kAtoms sub-tiles 8 KiB apart).
@@ -348,17 +350,18 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                         dg::tc_commit(dg::smem_u32(&v_empty[t * kStages + st]));
                     }
                 }
+                if (!ok) fail();
+                // Every MMA this thread issued must have completed (and signalled its
+                // barriers) before the CTA's shared memory and TMEM go away.
+                const volatile int never = 0;
+                uint64_t* my_drain = &drain[s_role ? 0 : 1 + pv_tile];
+                dg::tc_commit(dg::smem_u32(my_drain));
+                dg::mbar_wait(dg::smem_u32(my_drain), 0u, &never, 100000000ull);
             }
-            if (!ok) fail();
-            // Every MMA this thread issued must have completed (and signalled its
-            // barriers) before the CTA's shared memory and TMEM go away.
-            const volatile int never = 0;
-            uint64_t* my_drain = &drain[warp - 1];
-            dg::tc_commit(dg::smem_u32(my_drain));
-            dg::mbar_wait(dg::smem_u32(my_drain), 0u, &never, 100000000ull);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp >= 4) {
+    } else {
+        if constexpr (Cfg::kRegSplit) dg::setmaxnreg_inc<Cfg::kRegsHigh>();
         // ------------------------------------------------------------ softmax
         const int t = (warp - 4) >> 2;                  // query tile of this warpgroup
         const int quarter = warp & 3;
