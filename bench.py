@@ -156,7 +156,9 @@ class ClockSampler:
         mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i] == "Active"})
+        pw = sorted(float(r[3]) for r in use if r[3].replace(".", "").isdigit())
         return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w": pw[len(pw) // 2] if pw else None,
                 "reasons": reasons, "samples": len(use),
                 "window": "timed region" if inside else "whole run (no sample inside the timed region)"}
 
@@ -334,8 +336,25 @@ def run_ours(args, rank: int, world: int, dist) -> None:
 
     also = {}
     if rank == 0 and not args.quick:
-        also["sustained_" + w.name] = sustained_leg(torch, step, w, stream, peaks, peak_src,
-                                                 args.sustained_s, local)
+        sus = sustained_leg(torch, step, w, stream, peaks, peak_src, args.sustained_s, local)
+        # cuBLAS (torch.matmul, bf16 output: torch has no fp32 output for bf16
+        # inputs) the same way, after ours and outside the timed region, for the
+        # per-clock comparison; the power cap sets different clocks per run.
+        cb = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+
+        def ref_step():
+            torch.matmul(a, b, out=cb)
+        ref = sustained_leg(torch, ref_step, w, stream, peaks, peak_src, args.sustained_s, local)
+        del cb
+
+        def per_ghz(leg):
+            mhz = (leg.get("clocks") or {}).get("sm_mhz")
+            return leg["tflops"] / (mhz / 1000.0) if mhz else None
+        sus["tflops_per_ghz"] = per_ghz(sus)
+        sus["torch_matmul"] = {"tflops": ref["tflops"], "seconds": ref["seconds"],
+                               "clocks": ref["clocks"], "tflops_per_ghz": per_ghz(ref),
+                               "what": "cuBLAS via torch.matmul, bf16 output; context"}
+        also["sustained_" + w.name] = sus
         also.update(secondary(torch, g, plan, workloads, dev, stream, peaks, peak_src))
 
     e2e = None
@@ -369,8 +388,13 @@ def run_ours(args, rank: int, world: int, dist) -> None:
 def sustained_leg(torch, step, w, stream, peaks, peak_src, seconds, device_index) -> dict:
     """The headline GEMM back to back for `seconds` (power-capped steady state),
     with clocks sampled inside the timed region; against the sustained peak."""
-    # one launch's time, to size the run
+    # one launch's time, to size the run (after warm-up calls: a library's first
+    # calls may set up handles and workspaces, which would undersize the run)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(5):
@@ -409,6 +433,13 @@ def summary(also: dict) -> dict:
             out[k] = {"tflops": r(v["tflops"]), "frac_sustained": r(v["frac_of_sustained_peak"], 3),
                       "s": r(v["seconds"], 2), "sm_mhz": c.get("sm_mhz"),
                       "clock_samples": c.get("samples"), "reasons": c.get("reasons")}
+            if "tflops_per_ghz" in v:
+                out[k]["per_ghz"] = r(v["tflops_per_ghz"])
+            if "torch_matmul" in v:
+                m = v["torch_matmul"]
+                out[k]["matmul"] = r(m["tflops"])
+                out[k]["matmul_per_ghz"] = r(m.get("tflops_per_ghz"))
+                out[k]["matmul_mhz"] = (m.get("clocks") or {}).get("sm_mhz")
         elif "gbs" in v:
             out[k] = {"gbs": r(v["gbs"], 0), "pct_hbm": r(v["pct_of_hbm_peak"])}
             for extra in ("torch_matmul_gbs", "torch_softmax_gbs"):

@@ -21,7 +21,11 @@ def fake_also():
     also = {
         "sustained_square8192_bf16": {"tflops": 1601.234, "launches": 4200, "seconds": 2.51,
                                       "frac_of_sustained_peak": 0.9438, "peak": 1696.4,
-                                      "peak_source": "measured", "clocks": clocks},
+                                      "peak_source": "measured", "clocks": clocks,
+                                      "tflops_per_ghz": 1111.97,
+                                      "torch_matmul": {"tflops": 1650.2, "seconds": 2.6,
+                                                       "clocks": dict(clocks, sm_mhz=1425.0),
+                                                       "tflops_per_ghz": 1158.0, "what": "w" * 60}},
         "square4096_bf16": {"tflops": 1633.21, "pct_of_peak": 86.3, "median_ms": 0.084,
                             "torch_matmul_tflops": 1756.2, "torch_matmul": "y" * 80},
         "skinny16x4096x14336_bf16": {"gbs": 6133.3, "pct_of_hbm_peak": 90.51,
@@ -45,6 +49,8 @@ def test_summary_line_is_short_and_complete():
     assert set(summ) == set(also)
     assert summ["skinny16x4096x14336_bf16"]["gbs"] == 6133.0
     assert summ["sustained_square8192_bf16"]["clock_samples"] == 12
+    assert summ["sustained_square8192_bf16"]["per_ghz"] == 1112.0
+    assert summ["sustained_square8192_bf16"]["matmul_per_ghz"] == 1158.0
     assert summ["gemm256_f16"]["floor_us"] == 0.66
     assert summ["square4096_bf16"]["matmul"] == 1756.2
 
