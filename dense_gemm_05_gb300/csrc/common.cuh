@@ -207,11 +207,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // a_mn: A is stored K x M (transposed, M contiguous); otherwise M x K.
 // b_mn: B is stored K x N (N contiguous); otherwise N x K (transposed).
 
-// Persistent tcgen05 kernel, operands by TMA. bn in {128, 256}.
-int tma_smem_bytes(int bn);
+// Persistent tcgen05 kernel, operands by TMA: tiles of bm x bn, bn in {64, 128,
+// 256}, bm = 128 (or 64 with bn = 64: M = 64 MMAs, for problems with few tiles).
+int tma_smem_bytes(int bm, int bn);
 int tma_stages(int bn);
 cudaError_t tma_prepare();
-cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+cudaError_t launch_tma(int bm, int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
                        const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
                        uint32_t idesc, int grid, cudaStream_t stream);
 

@@ -189,6 +189,7 @@ struct Args {
 struct Choice {
     int kernel = GEMM_KERNEL_NONE;
     int bn = 0;          // TMA/GENERIC: tile columns
+    int bm = 128;        // TMA: tile rows (128, or 64 with bn = 64)
     int ms = 0;          // SKINNY, SPLIT_PAIR: padded M
     int split = 1;       // SKINNY: most stream-K shares that touch one tile
     int shares = 0;      // SKINNY: stream-K shares
@@ -561,13 +562,21 @@ gemm_status_t choose(const gemm_plan_s* plan, const Args& a, Choice* c, bool b_g
         }
         return GEMM_OK;
     } else {
-        const int64_t tm = cdiv(a.M, dg::kBM);
+        int64_t tm = cdiv(a.M, dg::kBM);
         if (kernel == GEMM_KERNEL_TMA) {
             const int64_t t256 = tm * cdiv(a.N, 256);
             c->bn = plan->force_bn ? plan->force_bn
                                    : (auto_bn ? auto_bn
                                               : ((t256 >= 2 * int64_t(plan->num_sms)) ? 256 : 128));
             c->stages = dg::tma_stages(c->bn);
+            // 128 x 64 tiles that fill less than half the SMs: 64 x 64 tiles (M = 64
+            // MMAs) if they still fit one wave -- twice the CTAs, each with half
+            // the A loads and half the stores.
+            if (c->bn == 64 && 2 * tm * cdiv(a.N, 64) <= plan->num_sms &&
+                cdiv(a.M, 64) * cdiv(a.N, 64) <= plan->num_sms) {
+                c->bm = 64;
+                tm = cdiv(a.M, 64);
+            }
         } else {
             c->bn = 128;
             c->stages = dg::generic_stages();
@@ -855,7 +864,8 @@ gemm_status_t query_impl(gemm_plan_t plan, const Args& a_in, gemm_config_t* out)
     cfg.kernel = c.kernel;
     cfg.block_m = (c.kernel == GEMM_KERNEL_SKINNY || c.kernel == GEMM_KERNEL_SPLIT_PAIR)
                       ? c.ms
-                      : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM : dg::kBM);
+                      : (c.kernel == GEMM_KERNEL_PAIR ? 2 * dg::kBM
+                                                        : (c.kernel == GEMM_KERNEL_TMA ? c.bm : dg::kBM));
     cfg.block_n = (c.kernel == GEMM_KERNEL_SKINNY) ? 128 : c.bn;
     cfg.block_k = (c.kernel == GEMM_KERNEL_NONE || c.kernel == GEMM_KERNEL_ZERO_FILL) ? 0 : dg::kBK;
     cfg.stages = c.stages;
@@ -960,27 +970,28 @@ gemm_status_t run_impl(gemm_plan_t plan, const Args& a_in, cudaStream_t stream) 
             return b_mn ? cached_encode_2d(plan, m, in, a.B, a.N, a.K, a.ldb, dg::kSubN, dg::kBK)
                         : cached_encode_2d(plan, m, in, a.B, a.K, a.N, a.ldb, dg::kBK, rows);
         };
-        // C written by TMA stores of {128 bytes of columns, 32 rows} boxes when its
+        // C written by TMA stores of {128 bytes of columns, 32 rows (16 for 64-row
+        // tiles)} boxes when its
         // base, pitch and row length are 16-byte multiples; otherwise by ordinary
         // stores.  (With a row length that is not, the right edge of C was seen
         // to be written in whole 16-byte pieces, past column N: the guard-band
         // tests catch that.)
         CUtensorMap mc;
         memset(&mc, 0, sizeof(mc));
-        auto map_c = [&]() {
+        auto map_c = [&](uint32_t rows = 32u) {
             p.c_tma = 0;
             if (!p.c_vec || (a.N * esize) % 16 != 0) return;
             const uint32_t cols = a.c_type == GEMM_OUT_F32 ? 32u : 64u;
-            if (cached_encode_2d(plan, &mc, elem_of_out(a.c_type), a.C, a.N, a.M, a.ldc, cols, 32u))
+            if (cached_encode_2d(plan, &mc, elem_of_out(a.c_type), a.C, a.N, a.M, a.ldc, cols, rows))
                 p.c_tma = 1;
         };
         if (c.kernel == GEMM_KERNEL_TMA) {
             CUtensorMap ma, mb;
-            if (!map_a(&ma, dg::kBM) || !map_b(&mb, static_cast<uint32_t>(c.bn)))
+            if (!map_a(&ma, static_cast<uint32_t>(c.bm)) || !map_b(&mb, static_cast<uint32_t>(c.bn)))
                 return GEMM_ERR_CUDA;
-            map_c();
-            err = dg::launch_tma(c.bn, a_mn, b_mn, ma, mb, mc, p,
-                                 dg::idesc_f16(bf16, a_mn, b_mn, dg::kBM, c.bn), c.grid, stream);
+            map_c(static_cast<uint32_t>(c.bm / 4));     // each epilogue warp's rows
+            err = dg::launch_tma(c.bm, c.bn, a_mn, b_mn, ma, mb, mc, p,
+                                 dg::idesc_f16(bf16, a_mn, b_mn, c.bm, c.bn), c.grid, stream);
         } else if (c.kernel == GEMM_KERNEL_PAIR) {
             // Each CTA of a pair loads 128 rows of A and its half (bn / 2) of the B tile.
             CUtensorMap ma, mb;

@@ -28,10 +28,16 @@
 
 namespace dg {
 
-template <int BN, int STAGES, bool GENERIC>
+template <int BM, int BN, int STAGES, bool GENERIC>
 struct TcCfg {
+    static_assert(BM == 128 || (BM == 64 && !GENERIC), "tile rows");
+    static constexpr int kAStageBytes = BM * kBK * 2;
     static constexpr int kBStageBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+    // Accumulator rows each epilogue warp holds: an M = 128 MMA puts row r in
+    // TMEM lane r; an M = 64 one puts rows 16 q .. 16 q + 15 in lanes 0 .. 15 of
+    // lane quarter q.
+    static constexpr int kRowsPerWarp = BM / 4;
     static constexpr int kTmemCols = 2 * BN;               // two fp32 accumulators, power of 2
     static constexpr int kProducerWarps = GENERIC ? 4 : 1;
     static constexpr int kThreads = 32 * (1 + 4 + kProducerWarps);
@@ -104,13 +110,14 @@ __device__ __forceinline__ void load_tile_generic(uint32_t dst, const uint16_t* 
     }
 }
 
-template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
+template <int BM, int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(TcCfg<BM, BN, STAGES, GENERIC>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                    const __grid_constant__ CUtensorMap mapB,
                    const __grid_constant__ CUtensorMap mapC, const Params p,
                    const uint32_t idesc) {
-    using Cfg = TcCfg<BN, STAGES, GENERIC>;
+    using Cfg = TcCfg<BM, BN, STAGES, GENERIC>;
+    constexpr int kAStageBytes = Cfg::kAStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         uint32_t eseq = 0;                      // chunk counter of this warp's two buffers
-        const int row_in_tile = q * 32 + lane;
+        const int row_in_tile = q * Cfg::kRowsPerWarp + lane;   // valid for lane < kRowsPerWarp
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -227,20 +234,20 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const int row = tm * kBM + row_in_tile;
+            const int row = tm * BM + row_in_tile;
             const int col0 = tn * BN;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                    static_cast<uint32_t>(acc * BN);
             const uint32_t tempty_bar = smem_u32(&tempty[acc]);
             if (!GENERIC) {
-                epilogue_staged<BN>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiWarpBytes, eseq,
+                epilogue_staged<BN, Cfg::kRowsPerWarp>(p, &mapC, smem_u32(sEpi) + (warp - 1) * kEpiWarpBytes, eseq,
                                     taddr, lane,
                                  row - lane, col0, [&] {
                                      tc_fence_before();
                                      mbar_arrive(tempty_bar);
                                  });
             } else {
-                const bool row_ok = row < p.M;
+                const bool row_ok = row < p.M && lane < Cfg::kRowsPerWarp;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t v[32];
@@ -276,8 +283,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Cfg::kStageBytes));
-                    load_operand<A_MN>(smem_u32(sA + stage * kAStageBytes), &mapA, fb, tm * kBM,
-                                       kb * kBK, kBM);
+                    load_operand<A_MN>(smem_u32(sA + stage * kAStageBytes), &mapA, fb, tm * BM,
+                                       kb * kBK, BM);
                     load_operand<B_MN>(smem_u32(sB + stage * Cfg::kBStageBytes), &mapB, fb,
                                        tn * BN, kb * kBK, BN);
                     ++armed;
@@ -320,8 +327,8 @@ __global__ void __launch_bounds__(TcCfg<BN, STAGES, GENERIC>::kThreads, 1)
                     failed = true;
                     break;
                 }
-                load_tile_generic<A_MN, kBM>(smem_u32(sA + stage * kAStageBytes), p.A, p.lda,
-                                             tm * kBM, kb * kBK, p.M, p.K, p.a_vec, pt, p.status,
+                load_tile_generic<A_MN, BM>(smem_u32(sA + stage * kAStageBytes), p.A, p.lda,
+                                            tm * BM, kb * kBK, p.M, p.K, p.a_vec, pt, p.status,
                                              kChkA);
                 load_tile_generic<B_MN, BN>(smem_u32(sB + stage * Cfg::kBStageBytes), p.B, p.ldb,
                                             tn * BN, kb * kBK, p.N, p.K, p.b_vec, pt, p.status,
@@ -358,48 +365,50 @@ constexpr int kTmaStages128 = 6;
 constexpr int kTmaStages64 = 6;
 constexpr int kGenericStages = 4;
 
-template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
+template <int BM, int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
 cudaError_t set_attrs_one() {
-    using Cfg = TcCfg<BN, STAGES, GENERIC>;
-    return cudaFuncSetAttribute(gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>,
+    using Cfg = TcCfg<BM, BN, STAGES, GENERIC>;
+    return cudaFuncSetAttribute(gemm_tc_kernel<BM, BN, STAGES, GENERIC, A_MN, B_MN>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
 }
 
-template <int BN, int STAGES, bool GENERIC>
+template <int BM, int BN, int STAGES, bool GENERIC>
 cudaError_t set_attrs() {
-    cudaError_t e = set_attrs_one<BN, STAGES, GENERIC, false, true>();
-    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, false, false>();
-    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, true, true>();
-    if (e == cudaSuccess) e = set_attrs_one<BN, STAGES, GENERIC, true, false>();
+    cudaError_t e = set_attrs_one<BM, BN, STAGES, GENERIC, false, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BM, BN, STAGES, GENERIC, false, false>();
+    if (e == cudaSuccess) e = set_attrs_one<BM, BN, STAGES, GENERIC, true, true>();
+    if (e == cudaSuccess) e = set_attrs_one<BM, BN, STAGES, GENERIC, true, false>();
     return e;
 }
 
-template <int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
+template <int BM, int BN, int STAGES, bool GENERIC, bool A_MN, bool B_MN>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const Params& p, uint32_t idesc, int grid, cudaStream_t s) {
-    using Cfg = TcCfg<BN, STAGES, GENERIC>;
-    return launch_pdl(gemm_tc_kernel<BN, STAGES, GENERIC, A_MN, B_MN>, dim3(grid),
+    using Cfg = TcCfg<BM, BN, STAGES, GENERIC>;
+    return launch_pdl(gemm_tc_kernel<BM, BN, STAGES, GENERIC, A_MN, B_MN>, dim3(grid),
                       dim3(Cfg::kThreads), Cfg::kSmemBytes, s, a, b, c, p, idesc);
 }
 
-template <int BN, int STAGES, bool GENERIC>
+template <int BM, int BN, int STAGES, bool GENERIC>
 cudaError_t launch(bool a_mn, bool b_mn, const CUtensorMap& a, const CUtensorMap& b,
                    const CUtensorMap& c, const Params& p, uint32_t idesc, int grid,
                    cudaStream_t s) {
     if (!a_mn && b_mn)
-        return launch_one<BN, STAGES, GENERIC, false, true>(a, b, c, p, idesc, grid, s);
+        return launch_one<BM, BN, STAGES, GENERIC, false, true>(a, b, c, p, idesc, grid, s);
     if (!a_mn && !b_mn)
-        return launch_one<BN, STAGES, GENERIC, false, false>(a, b, c, p, idesc, grid, s);
+        return launch_one<BM, BN, STAGES, GENERIC, false, false>(a, b, c, p, idesc, grid, s);
     if (a_mn && b_mn)
-        return launch_one<BN, STAGES, GENERIC, true, true>(a, b, c, p, idesc, grid, s);
-    return launch_one<BN, STAGES, GENERIC, true, false>(a, b, c, p, idesc, grid, s);
+        return launch_one<BM, BN, STAGES, GENERIC, true, true>(a, b, c, p, idesc, grid, s);
+    return launch_one<BM, BN, STAGES, GENERIC, true, false>(a, b, c, p, idesc, grid, s);
 }
 }  // namespace
 
-int tma_smem_bytes(int bn) {
-    return bn == 256 ? TcCfg<256, kTmaStages256, false>::kSmemBytes
-                     : (bn == 64 ? TcCfg<64, kTmaStages64, false>::kSmemBytes
-                                 : TcCfg<128, kTmaStages128, false>::kSmemBytes);
+int tma_smem_bytes(int bm, int bn) {
+    if (bn == 256) return TcCfg<128, 256, kTmaStages256, false>::kSmemBytes;
+    if (bn == 64)
+        return bm == 64 ? TcCfg<64, 64, kTmaStages64, false>::kSmemBytes
+                        : TcCfg<128, 64, kTmaStages64, false>::kSmemBytes;
+    return TcCfg<128, 128, kTmaStages128, false>::kSmemBytes;
 }
 
 int tma_stages(int bn) {
@@ -407,37 +416,41 @@ int tma_stages(int bn) {
 }
 
 cudaError_t tma_prepare() {
-    cudaError_t e = set_attrs<256, kTmaStages256, false>();
-    if (e == cudaSuccess) e = set_attrs<128, kTmaStages128, false>();
-    if (e == cudaSuccess) e = set_attrs<64, kTmaStages64, false>();
+    cudaError_t e = set_attrs<128, 256, kTmaStages256, false>();
+    if (e == cudaSuccess) e = set_attrs<128, 128, kTmaStages128, false>();
+    if (e == cudaSuccess) e = set_attrs<128, 64, kTmaStages64, false>();
+    if (e == cudaSuccess) e = set_attrs<64, 64, kTmaStages64, false>();
     return e;
 }
 
-cudaError_t launch_tma(int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
+cudaError_t launch_tma(int bm, int bn, bool a_mn, bool b_mn, const CUtensorMap& mapA,
                        const CUtensorMap& mapB, const CUtensorMap& mapC, const Params& p,
                        uint32_t idesc, int grid, cudaStream_t stream) {
     if (bn == 256)
-        return launch<256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
-                                                 stream);
+        return launch<128, 256, kTmaStages256, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc,
+                                                      grid, stream);
+    if (bn == 64 && bm == 64)
+        return launch<64, 64, kTmaStages64, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                                   stream);
     if (bn == 64)
-        return launch<64, kTmaStages64, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
-                                               stream);
-    return launch<128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
-                                             stream);
+        return launch<128, 64, kTmaStages64, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                                    stream);
+    return launch<128, 128, kTmaStages128, false>(a_mn, b_mn, mapA, mapB, mapC, p, idesc, grid,
+                                                  stream);
 }
 
-int generic_smem_bytes() { return TcCfg<128, kGenericStages, true>::kSmemBytes; }
+int generic_smem_bytes() { return TcCfg<128, 128, kGenericStages, true>::kSmemBytes; }
 
 int generic_stages() { return kGenericStages; }
 
-cudaError_t generic_prepare() { return set_attrs<128, kGenericStages, true>(); }
+cudaError_t generic_prepare() { return set_attrs<128, 128, kGenericStages, true>(); }
 
 cudaError_t launch_generic(bool a_mn, bool b_mn, const Params& p, uint32_t idesc, int grid,
                            cudaStream_t stream) {
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof(dummy));
-    return launch<128, kGenericStages, true>(a_mn, b_mn, dummy, dummy, dummy, p, idesc, grid,
-                                             stream);
+    return launch<128, 128, kGenericStages, true>(a_mn, b_mn, dummy, dummy, dummy, p, idesc,
+                                                  grid, stream);
 }
 
 }  // namespace dg

@@ -180,7 +180,7 @@ __device__ __forceinline__ int epi_chunk_cols(int c_type) { return c_type == kOu
 __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorMap* mapC,
                                                 uint32_t warp_buf, uint32_t& seq, int lane,
                                                 int row0, int col, const uint32_t (&lo)[32],
-                                                const uint32_t (&hi)[32]) {
+                                                const uint32_t (&hi)[32], int rows = 32) {
     // A chunk wholly outside C (rows from row0 or columns from col beyond M or N)
     // is skipped without touching a buffer: the two buffers then alternate over
     // the stores actually issued, so the wait below always covers the store that
@@ -237,7 +237,7 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
             const int r = row0 + rr;
             const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
             const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
-            if (r < p.M && h + 4 * k + 4 <= 32 &&
+            if (rr < rows && r < p.M && h + 4 * k + 4 <= 32 &&
                 DG_CHECK(p.status, kChkC, span_inside(r, col + h + 4 * k, 4, p.M, p.N))) {
                 const int e = h + 4 * k;
                 const uint32_t rowb = buf + static_cast<uint32_t>(rr * 128);
@@ -252,7 +252,8 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
         const int r = row0 + lane;
         const int64_t off = static_cast<int64_t>(r) * p.ldc + col;
         const int h = static_cast<int>((4u - ((reinterpret_cast<uintptr_t>(cbase + off) >> 2) & 3u)) & 3u);
-        if (r < p.M && h != 0 && DG_CHECK(p.status, kChkC, span_inside(r, col, 32, p.M, p.N))) {
+        if (lane < rows && r < p.M && h != 0 &&
+            DG_CHECK(p.status, kChkC, span_inside(r, col, 32, p.M, p.N))) {
             const uint32_t rowb = buf + static_cast<uint32_t>(lane * 128);
             auto elem = [&](int e) {
                 return __uint_as_float(ld_shared_b32(
@@ -270,7 +271,7 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
     // Lane l reads 32-bit word l of each 128-byte row (in 16-byte piece l / 4).
     const uint32_t word = static_cast<uint32_t>(lane & 3) * 4u;
 #pragma unroll 4
-    for (int rr = 0; rr < 32; ++rr) {
+    for (int rr = 0; rr < rows; ++rr) {
         const int r = row0 + rr;
         if (r >= p.M) break;
         const uint32_t w = ld_shared_b32(buf + static_cast<uint32_t>(rr * 128) +
@@ -296,7 +297,9 @@ __device__ __forceinline__ void epi_store_chunk(const Params& p, const CUtensorM
 // address `taddr` (this warp's lanes), through the staged chunks above.  `release` is called
 // after the last TMEM load, so the MMA issuer may reuse the accumulator while
 // the final chunks are still being stored.
-template <int BN, typename Release>
+// ROWS: the accumulator rows this warp holds in its lanes 0 .. ROWS-1 (32, or 16
+// for a 64-row tile; the TMA box of mapC is then ROWS rows high).
+template <int BN, int ROWS = 32, typename Release>
 __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorMap* mapC,
                                              uint32_t warp_buf, uint32_t& seq, uint32_t taddr,
                                              int lane, int row0, int col0, Release release) {
@@ -316,8 +319,8 @@ __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorM
             tmem_ld_wait(a);
             tmem_ld_wait(b);
             if (ch + 2 == BN / 32) release();
-            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * 32, a, none);
-            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + (ch + 1) * 32, b, none);
+            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * 32, a, none, ROWS);
+            epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + (ch + 1) * 32, b, none, ROWS);
         }
         return;
     }
@@ -334,7 +337,7 @@ __device__ __forceinline__ void epilogue_staged(const Params& p, const CUtensorM
         }
         tmem_ld_wait(lo);
         if (ch == nchunks - 1) release();
-        epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * cw, lo, hi);
+        epi_store_chunk(p, mapC, warp_buf, seq, lane, row0, col0 + ch * cw, lo, hi, ROWS);
     }
 }
 

@@ -47,8 +47,9 @@ def test_the_five_workloads(model):
     r = q(model, 16, 14336, 4096)
     assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["split_k"], r["tiles"]) == \
         (g.GEMM_KERNEL_SPLIT_PAIR, 16, 256, 112, 2, 56), r
-    r = q(model, 256, 256, 256, dtype=g.GEMM_F16)       # 128 x 64 tiles: 8 CTAs
-    assert (r["kernel"], r["block_n"], r["grid"], r["tiles"]) == (g.GEMM_KERNEL_TMA, 64, 8, 8), r
+    r = q(model, 256, 256, 256, dtype=g.GEMM_F16)       # 64 x 64 tiles (M = 64 MMAs): 16 CTAs
+    assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["tiles"]) == \
+        (g.GEMM_KERNEL_TMA, 64, 64, 16, 16), r
     r = q(model, 1023, 1029, 1000, dtype=g.GEMM_F16)      # tight pitches: ldb = 1029 halves
     assert (r["kernel"], r["block_m"], r["block_n"], r["grid"], r["staged"]) == \
         (g.GEMM_KERNEL_SPLIT_PAIR, 128, 128, 144, 2), r
@@ -87,7 +88,10 @@ def test_every_choice_is_consistent(model, M, N, K):
     elif k == g.GEMM_KERNEL_PAIR:
         assert M > 64 and r["block_m"] == 256 and r["grid"] <= 152 and r["grid"] % 2 == 0, r
     else:
-        assert r["grid"] <= 152 and r["block_m"] == 128, r
+        assert r["grid"] <= 152 and r["block_m"] in (64, 128), r
+        if r["block_m"] == 64:                         # 64 x 64 tiles, one wave, small problems
+            assert r["block_n"] == 64 and r["tiles"] == -(-M // 64) * -(-N // 64) <= 152, r
+            assert 2 * -(-M // 128) * -(-N // 64) <= 152, r
     if M <= 64:
         assert k in (g.GEMM_KERNEL_SKINNY, g.GEMM_KERNEL_SPLIT_PAIR), r
 
