@@ -201,3 +201,27 @@ def test_layout_argument_errors(plan):
     assert g.gemm_run_ex(h, N_, N_, a.data_ptr(), 64, a.data_ptr(), 64, c.data_ptr() + 1, 64,
                          g.GEMM_OUT_F16, 64, 64, 64, g.GEMM_BF16, s) == E
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("op_a,op_b", OPS)
+@pytest.mark.parametrize("out", [g.GEMM_OUT_F32, g.GEMM_OUT_F16, g.GEMM_OUT_BF16])
+@pytest.mark.parametrize("M,K,N,ldc_pad", [(256, 256, 256, 0), (200, 136, 72, 8), (96, 128, 136, 8),
+                                           (184, 64, 248, 0)])
+def test_64_row_tiles_every_layout_and_output(plan, op_a, op_b, out, M, K, N, ldc_pad):
+    """Small problems run on 64 x 64 tiles with M = 64 MMAs (16 accumulator rows
+    per epilogue warp): integer inputs, exact in every output type, ragged edges
+    and guard cells, every operand layout.  The planner must pick those tiles."""
+    gen = torch.Generator().manual_seed(M + N + 3 * op_a + op_b + 7 * out)
+    A = torch.randint(-1, 2, (M, K), generator=gen).to(torch.float16)   # |C| <= K <= 256: exact
+    B = torch.randint(-1, 2, (K, N), generator=gen).to(torch.float16)   # in fp16 and bf16 too
+    dev = torch.device("cuda:0")
+    a, b = stored(A, op_a).to(dev), stored(B, op_b).to(dev)
+    ldc = N + ldc_pad
+    cbuf = torch.full((M + 2, ldc), SENTINEL, dtype=TORCH_OUT[out], device=dev)
+    cfg = g.gemm_query_ex(plan.handle, op_a, op_b, a.data_ptr(), a.stride(0), b.data_ptr(),
+                          b.stride(0), cbuf.data_ptr(), ldc, out, M, N, K, g.GEMM_F16)
+    assert (cfg["kernel"], cfg["block_m"], cfg["block_n"]) == (g.GEMM_KERNEL_TMA, 64, 64), cfg
+    got = run_ex(plan, stored(A, op_a), stored(B, op_b), op_a, op_b, M, N, K, out, ldc=ldc)
+    assert np.all(got[:M, N:] == SENTINEL) and np.all(got[M:] == SENTINEL), "guard cells"
+    ref = oracle.gemm(A, B)
+    assert np.array_equal(got[:M, :N], ref), f"max diff {np.abs(got[:M, :N] - ref).max()}"
