@@ -1,6 +1,7 @@
 // gemm_tc.cu -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
-// One CTA per SM walks output tiles of 128 x BN in the scheduler's order.
+// One CTA per SM walks output tiles of BM x BN (BM = 128, or 64 for small
+// problems: M = 64 MMAs) in the scheduler's order.
 // Each tile is the K-loop of "acc += A_tile @ B_tile" ("Writing GPU kernels in
 // Triton: Vector Add, Softmax, MatMul", section 3.3; "Triton 04", section
 // "Why have acc"), with the fp32 accumulator held in tensor memory.
@@ -11,11 +12,11 @@
 //   warp 5        TMA producer (TMA variant), or
 //   warps 5..8    load/store producer (generic variant, any alignment)
 //
-// Shared memory holds a ring of STAGES {A 128x64, B 64xBN} tiles in the
+// Shared memory holds a ring of STAGES {A BMx64, B 64xBN} tiles in the
 // 128-byte-swizzled layouts of tiles.cuh (A_MN / B_MN: the operand is stored
 // with M / N contiguous, i.e. A transposed, or B in its natural K x N layout);
 // "full" barriers hand a stage to the MMA issuer, "empty" barriers
-// (tcgen05.commit) hand it back.  Two TMEM accumulators of 128 x BN fp32 let
+// (tcgen05.commit) hand it back.  Two TMEM accumulators of BM x BN fp32 let
 // the epilogue drain tile i while the MMAs of tile i+1 run.
 //
 // Masking: TMA fills elements outside the global tensor with zeros (the

@@ -85,7 +85,9 @@ typedef enum { GEMM_OUT_F32 = 0, GEMM_OUT_F16 = 1, GEMM_OUT_BF16 = 2 } gemm_out_
 typedef enum {
     GEMM_KERNEL_NONE = 0,       /* M == 0 or N == 0: nothing is launched */
     GEMM_KERNEL_ZERO_FILL = 1,  /* K == 0: C is set to zero (the empty sum) */
-    GEMM_KERNEL_TMA = 2,        /* persistent warp-specialised tcgen05 kernel fed by TMA */
+    GEMM_KERNEL_TMA = 2,        /* persistent warp-specialised tcgen05 kernel fed by TMA;
+                                   tiles of 128 x 64/128/256, or 64 x 64 (M = 64 MMAs) for
+                                   problems whose 128 x 64 tiles fill at most half the SMs */
     GEMM_KERNEL_GENERIC = 3,    /* same pipeline, operands staged by ordinary loads
                                    (leading dimensions or pointers not 16-byte aligned) */
     GEMM_KERNEL_SKINNY = 4,     /* small M: swap-AB + split-K, deterministic reduction */
@@ -101,8 +103,8 @@ typedef enum {
 
 typedef struct {
     int32_t kernel;       /* gemm_kernel_t */
-    int32_t block_m;      /* rows of C per tile (per CTA pair for GEMM_KERNEL_PAIR; the padded
-                             M, 16, 32 or 64, for SKINNY and SPLIT_PAIR) */
+    int32_t block_m;      /* rows of C per tile (per CTA pair for GEMM_KERNEL_PAIR; 128 or 64
+                             for TMA; the padded M, 16, 32 or 64, for SKINNY and SPLIT_PAIR) */
     int32_t block_n;      /* columns of C per tile (SPLIT_PAIR: 128, 192 or 256 per strip) */
     int32_t block_k;      /* K depth of one pipeline stage */
     int32_t stages;       /* shared-memory ring depth */
