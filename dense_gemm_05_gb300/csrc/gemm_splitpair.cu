@@ -321,7 +321,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             uint32_t eseq = 0;
             const int col_base = n0 + static_cast<int>(rank) * Cfg::kHalf;
             const int row0 = m0 + q * 32;
-            if (p.c_type == kOutF32 || Cfg::kHalf % 64 == 0) {
+            if (MS <= 64 && p.c_type == kOutF32 && p.c_vec) {
+                // A strip of at most 64 rows with 16-byte-aligned fp32 C: each thread
+                // writes its own row's sums straight to C (16-byte stores), which
+                // measured faster here than staging 32-row chunks of which only the
+                // strip's rows exist.  Every lane runs the (warp-collective) TMEM
+                // loads; only the rows of the strip are stored.
+                if (got) {
+                    const int row = m0 + r;
+                    const int rx = r < MS ? r : 0;
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::kHalf; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(trow + rank * Cfg::kHalf + c, v);
+                        tmem_ld_wait(v);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 x = sX[(c / 4 + j) * MS + rx];
+                            v[4 * j] = __float_as_uint(__uint_as_float(v[4 * j]) + x.x);
+                            v[4 * j + 1] = __float_as_uint(__uint_as_float(v[4 * j + 1]) + x.y);
+                            v[4 * j + 2] = __float_as_uint(__uint_as_float(v[4 * j + 2]) + x.z);
+                            v[4 * j + 3] = __float_as_uint(__uint_as_float(v[4 * j + 3]) + x.w);
+                        }
+                        if (r < MS && row < p.M) store_c32(p, row, col_base + c, v);
+                    }
+                }
+            } else if (p.c_type == kOutF32 || Cfg::kHalf % 64 == 0) {
                 if (got) {
                     const int cw = epi_chunk_cols(p.c_type);
 #pragma unroll 1
