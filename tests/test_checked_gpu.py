@@ -6,7 +6,8 @@ that falls outside, recording it in the plan's status word; with debug-sync on,
 gemm_run (and softmax_rows, attention_fwd) then return GEMM_ERR_BOUNDS, which
 the binding raises.  The GEMM parity suites -- every kernel, layout, staged and
 in-place operand, ragged edge, output type, partition slice and sampled
-full-size case -- and the softmax and attention suites are run in a child
+full-size case -- the softmax and attention suites, the waits made to run out
+(the abort and drain paths) and two plans used at once are run in a child
 process with DG_GEMM_CHECKED=1 and GEMM_DEBUG_SYNC=1: they must pass there
 unchanged, i.e. no access of any of their launches leaves its range and the
 results still match the oracle.
@@ -25,7 +26,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SUITES = ["tests/test_gemm_gpu.py", "tests/test_layouts_gpu.py", "tests/test_partition_gpu.py",
           "tests/test_large_gpu.py", "tests/test_fuzz_gpu.py", "tests/test_softmax_gpu.py",
-          "tests/test_attention_gpu.py"]
+          "tests/test_attention_gpu.py", "tests/test_timeouts_gpu.py",
+          "tests/test_concurrency_gpu.py"]
 
 
 def test_the_checked_library_is_the_one_loaded():
