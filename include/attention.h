@@ -15,7 +15,10 @@
  * online softmax), so the seq x seq score matrix is never written to memory.
  * Q K^T and P V run on the tensor cores (fp16/bf16 operands, fp32
  * accumulation); the probabilities P are rounded to the input type before the
- * second product; the row sum is kept in fp32.
+ * second product; the row sum is kept in fp32.  The launch is persistent: at
+ * most one CTA per SM, each walking a fixed share of the work items (one
+ * block of 128 queries of one head for d = 128, two for d = 64); a query
+ * block's result does not depend on which CTA computes it.
  *
  * Layout: Q, K and V share one layout: element (h, i, c) at
  *     ptr + h*head_stride + i*ld + c          (c < d, i < seq, h < BH)
@@ -53,8 +56,8 @@ typedef struct {
     int32_t block_kv;     /* keys per step of the online softmax */
     int32_t head_dim;
     int32_t stages;       /* K/V shared-memory ring depth */
-    int32_t grid_x;       /* CTAs per head (each holds two query blocks for d = 64, one for 128) */
-    int32_t grid_y;       /* heads */
+    int32_t grid_x;       /* work items per head (two query blocks each for d = 64, one for 128) */
+    int32_t grid_y;       /* heads; the persistent launch has min(grid_x * grid_y, SMs) CTAs */
     int32_t causal;
 } attention_config_t;
 
