@@ -672,8 +672,9 @@ def attention_secondary(torch, g, workloads, dev, stream, peaks, peak_src) -> di
         out[name] = {"tflops": tf, "pct_of_peak": 100 * tf / peaks["bf16_tflops"],
                      "median_us": t * 1e6, "flops": w.flops,
                      "flops_counted": "4 * BH * d * (query, key) pairs kept by the mask",
-                     "kernel": (f"attention_fwd_kernel: {2 if w.d == 64 else 1} query tile(s) "
-                                "of 128 per CTA, 128-key blocks"),
+                     "kernel": (f"attention_fwd_kernel: persistent, one CTA per SM walking items of "
+                                f"{2 if w.d == 64 else 1} query tile(s) of 128, 128-key blocks"
+                                + (", epilogue warpgroup" if w.d == 128 else "")),
                      "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst",
                      "torch_sdpa_tflops": w.flops / (tms[len(tms) // 2] / 1e3) / 1e12}
         del q, k, v, o

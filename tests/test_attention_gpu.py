@@ -145,6 +145,22 @@ def test_repeatable_bits():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bits_do_not_depend_on_the_schedule(d, causal):
+    """The launch is persistent (at most one CTA per SM, each walking several
+    work items): a head computed alone and the same heads inside a 20-head
+    batch (several items per CTA, other CTAs and rounds) give identical bits."""
+    BH, seq = 20, 4096
+    Q, K, V = workloads.custom_qkv(BH, seq, d, "bf16", seed=31 + d + causal)
+    items = BH * (seq // 128 // (2 if d == 64 else 1))
+    assert items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    batch = run(Q, K, V, causal)
+    for h in (0, 7, BH - 1):
+        alone = run(Q[h:h + 1], K[h:h + 1], V[h:h + 1], causal)
+        assert np.array_equal(alone[0], batch[h]), h
+
+
 @pytest.mark.parametrize("name", ["attn_bh16_s8192_d64_bf16_causal", "attn_bh16_s8192_d64_bf16",
                                   "attn_bh16_s8192_d128_bf16_causal"])
 def test_full_size_sampled(name):
