@@ -62,6 +62,22 @@ namespace {
 
 __device__ int g_attn_status;
 
+// 32-byte global store of eight 32-bit words; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// 3-D tiled bulk tensor prefetch global -> L2 of one box that lies inside the
+// tensor (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 constexpr int kBQ = 128;                  // queries per tile (TMEM lanes)
 constexpr int kBKV = 128;                 // keys per block
 constexpr int kAtomBytes = 128 * 128;     // 128 rows x 64 elements of a K-major operand (16 KiB)
@@ -196,7 +212,7 @@ __device__ __forceinline__ void store_o_row(const AttnParams& p, int h, int qrow
         float* dst = static_cast<float*>(p.O) + off;
         if (kWide && p.o_vec == 2) {
 #pragma unroll
-            for (int i = 0; i < kD / 8; ++i) dg::st_global_v8(dst + 8 * i, o + 8 * i);
+            for (int i = 0; i < kD / 8; ++i) st_global_v8(dst + 8 * i, o + 8 * i);
         } else if (p.o_vec) {
 #pragma unroll
             for (int i = 0; i < kD / 4; ++i)
@@ -215,7 +231,7 @@ __device__ __forceinline__ void store_o_row(const AttnParams& p, int h, int qrow
             w[i] = dg::pack_out(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]), p.out_type);
         if (kWide && p.o_vec == 2) {
 #pragma unroll
-            for (int i = 0; i < kD / 16; ++i) dg::st_global_v8(dst + 16 * i, w + 8 * i);
+            for (int i = 0; i < kD / 16; ++i) st_global_v8(dst + 16 * i, w + 8 * i);
         } else if (p.o_vec) {
 #pragma unroll
             for (int i = 0; i < kD / 8; ++i)
@@ -360,7 +376,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                             for (int t = 0; t < kTiles; ++t)
                                 if ((pn * kTiles + t + 1) * kBQ <= p.seq)
                                     for (int a = 0; a < kAtoms; ++a)
-                                        dg::tma_prefetch_3d(&mapQ, 64 * a, (pn * kTiles + t) * kBQ, hn);
+                                        tma_prefetch_3d(&mapQ, 64 * a, (pn * kTiles + t) * kBQ, hn);
                         }
                     }
                     const bool k_lane = lane == 0;

@@ -187,23 +187,6 @@ __device__ __forceinline__ void tma_prefetch_2d_hint(const CUtensorMap* map, int
         : "memory");
 }
 
-// 32-byte global store of eight 32-bit words; the address must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]), "r"(w[1]),
-                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-// 3-D tiled bulk tensor prefetch global -> L2 of one box that lies inside the
-// tensor (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y,
-                                                int32_t z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // 3-D tiled bulk tensor load (x innermost, then y, then z), completion on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y, int32_t z) {
