@@ -19,10 +19,10 @@
 // that does not drain between them (the next item's K/V blocks and Q load
 // while the softmax finishes the previous one and writes its O).  TMEM per
 // tile: the score buffers S (two at d = 128, one at d = 64), P and O:
-//   warp 0      TMA producers: lane 2 each item's Q tiles (once the previous
-//               item's S MMAs have read the Q buffer), lane 0 K blocks, lane 1
-//               V blocks, each into a ring of 4 (d = 64) or 3 (d = 128)
-//               stages (3-D tensor maps over [BH, seq, d]).
+//   warp 0      TMA producers: lane 0 each item's Q tiles (once the previous
+//               item's S MMAs have read the Q buffer) and then its K blocks,
+//               lane 1 the V blocks, each into a ring of 4 (d = 64) or 3
+//               (d = 128) stages (3-D tensor maps over [BH, seq, d]).
 //   warp 1      S issuer (also owns TMEM): S_t(j) = Q_t K_j^T (M 128, N 128,
 //               K d) into score buffer j % kSBufs of tile t once K_j has
 //               landed and the tile's softmax has read that buffer.
@@ -39,9 +39,14 @@
 //               rounded to the input type into TMEM (the A operand of the
 //               second MMA), and when the reference maximum moves the rescale
 //               of O_t in TMEM (load, multiply by alpha, store) after
-//               P_t(j-1) V_{j-1} has finished.  At the end O_t / l goes to
-//               global memory.  At d = 64 the two warpgroups interleave on the
-//               SM's exponential units and issue slots.
+//               P_t(j-1) V_{j-1} has finished.  At d = 64 they also write
+//               O_t / l to global memory at the end of each item, and the two
+//               warpgroups interleave on the SM's exponential units and issue
+//               slots.
+//   warps 8..11 (d = 128) the epilogue warpgroup: the softmax hands it each
+//               finished item (1/l and the last P) and goes on with the next;
+//               it reads O_t from TMEM after the item's last P V, hands O_t
+//               back to the next item's first P V, and writes O_t / l.
 // Every mbarrier wait is bounded; a role that gives up raises the CTA's abort
 // flag and records the failure in a device status word.
 #include <atomic>
