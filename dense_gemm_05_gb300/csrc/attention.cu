@@ -121,8 +121,8 @@ struct AttnCfg {
     // about 9 % at d = 128.  With two tiles the softmax warpgroups write O
     // themselves (no registers are left for a fourth warpgroup).
     static constexpr bool kEpiWG = kTiles == 1;
-    static constexpr int kNumBars = 2 + 4 * kStages + kTiles * (2 * kSBufs + 3) + 1 + (kEpiWG ? 3 : 0);
-    static constexpr int kInvBytes = kEpiWG ? 2 * kBQ * 4 : 0;     // 1/l per row, two items
+    static constexpr int kNumBars = 2 + 4 * kStages + kTiles * (2 * kSBufs + 3) + 1 + (kEpiWG ? 3 * kTiles : 0);
+    static constexpr int kInvBytes = kEpiWG ? kTiles * 2 * kBQ * 4 : 0;     // 1/l per row, two items
     static constexpr int kSmemBytes =
         1024 + kTiles * kQBytes + kStages * (kKBytes + kVBytes) + kInvBytes + 8 * kNumBars + 16;
     // Warpgroup 0: the producer warp, the S warp and one P V warp per tile (one
@@ -158,6 +158,7 @@ struct AttnParams {
     int32_t ntiles;        // query tiles per head
     int32_t npairs;        // work items per head (tiles kTiles p .. kTiles p + kTiles - 1)
     int32_t heads;
+    int32_t d;             // head dimension
     float c;               // log2(e) / sqrt(d)
     uint64_t timeout_ns;
 };
@@ -206,13 +207,17 @@ __device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, 
     return false;
 }
 
-// One row of O (already scaled by 1/l) to global memory: 32-byte stores when
-// kWide and the layout allows them (o_vec 2), 16-byte (o_vec 1), else one
-// element at a time.  A checked build tests the row against the sequence.
+// Columns [col0, col0 + kD) of one row of O (already scaled by 1/l) to global
+// memory: 32-byte stores when kWide and the layout allows them (o_vec 2),
+// 16-byte (o_vec 1), else one element at a time.  A checked build tests the
+// span against the sequence and the row (width p.d).
 template <int kD, bool kWide>
-__device__ __forceinline__ void store_o_row(const AttnParams& p, int h, int qrow, const uint32_t (&o)[kD]) {
-    if (qrow >= p.seq || !DG_CHECK(&g_attn_status, dg::kChkC, dg::span_inside(qrow, 0, kD, p.seq, kD))) return;
-    const int64_t off = int64_t(h) * p.hso + int64_t(qrow) * p.ldo;
+__device__ __forceinline__ void store_o_span(const AttnParams& p, int h, int qrow, int col0,
+                                             const uint32_t (&o)[kD]) {
+    if (qrow >= p.seq ||
+        !DG_CHECK(&g_attn_status, dg::kChkC, dg::span_inside(qrow, col0, kD, p.seq, p.d)))
+        return;
+    const int64_t off = int64_t(h) * p.hso + int64_t(qrow) * p.ldo + col0;
     if (p.out_type == dg::kOutF32) {
         float* dst = static_cast<float*>(p.O) + off;
         if (kWide && p.o_vec == 2) {
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     uint8_t* sQ = smem;                                  // tile t at t * kQBytes
     uint8_t* sK = sQ + kTiles * kQBytes;
     uint8_t* sV = sK + kStages * kKBytes;
-    float* sInv = reinterpret_cast<float*>(sV + kStages * kVBytes);   // [item parity][row] (one tile)
+    float* sInv = reinterpret_cast<float*>(sV + kStages * kVBytes);   // [tile][item parity][row]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sV + kStages * kVBytes + Cfg::kInvBytes);
     uint64_t* q_full = bars;
     uint64_t* q_empty = q_full + 1;
@@ -282,9 +287,9 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     uint64_t* p_full = s_empty + kTiles * kSBufs;
     uint64_t* pv_done = p_full + kTiles;
     uint64_t* drain = pv_done + kTiles;                  // [S issuer, then P V issuer t]
-    uint64_t* o_full = drain + 1 + kTiles;               // (one tile) [item parity]: last P, 1/l
-    uint64_t* o_free = o_full + 2;                       // (one tile) O read by the epilogue
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1 + kTiles + (Cfg::kEpiWG ? 3 : 0));
+    uint64_t* o_full = drain + 1 + kTiles;               // [tile][item parity]: last P, 1/l
+    uint64_t* o_free = o_full + 2 * kTiles;              // [tile]: O read by the epilogue
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1 + kTiles + (Cfg::kEpiWG ? 3 * kTiles : 0));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -311,9 +316,11 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
         }
         for (int w = 0; w < 1 + kTiles; ++w) dg::mbar_init(dg::smem_u32(&drain[w]), 1u);
         if constexpr (Cfg::kEpiWG) {
-            dg::mbar_init(dg::smem_u32(&o_full[0]), 128u);
-            dg::mbar_init(dg::smem_u32(&o_full[1]), 128u);
-            dg::mbar_init(dg::smem_u32(o_free), 128u);
+            for (int t = 0; t < kTiles; ++t) {
+                dg::mbar_init(dg::smem_u32(&o_full[2 * t]), 128u);
+                dg::mbar_init(dg::smem_u32(&o_full[2 * t + 1]), 128u);
+                dg::mbar_init(dg::smem_u32(&o_free[t]), 128u);
+            }
         }
         *abort_flag = 0;
         dg::fence_mbar_init();
@@ -493,7 +500,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                                 // With an epilogue warpgroup the first P V of an item
                                 // overwrites O_t only once it has read the previous item's.
                                 if (Cfg::kEpiWG && j == 0 && epi_items > 0)
-                                    ok = dg::mbar_wait(dg::smem_u32(o_free), (epi_items - 1u) & 1u, abort_flag,
+                                    ok = dg::mbar_wait(dg::smem_u32(&o_free[t]), (epi_items - 1u) & 1u, abort_flag,
                                                        p.timeout_ns);
                                 ok = ok && dg::mbar_wait(dg::smem_u32(&p_full[t]), cnt[0] & 1u, abort_flag,
                                                          p.timeout_ns);
@@ -670,8 +677,8 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
             if constexpr (Cfg::kEpiWG) {
                 // Hand the item to the epilogue warpgroup: 1/l, then the arrival
                 // (after the last P hand-over) that releases it.
-                sInv[(items & 1u) * kBQ + r] = 1.0f / l;
-                dg::mbar_arrive(dg::smem_u32(&o_full[items & 1u]));
+                sInv[(t * 2 + (items & 1u)) * kBQ + r] = 1.0f / l;
+                dg::mbar_arrive(dg::smem_u32(&o_full[t * 2 + (items & 1u)]));
                 ++items;
                 continue;
             }
@@ -696,58 +703,66 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
                 for (int i = 0; i < 32; ++i) o[ch * 32 + i] = __float_as_uint(__uint_as_float(v[i]) * inv);
             }
             dg::tc_fence_before();
-            store_o_row<kD, false>(p, h, qrow, o);
+            store_o_span<kD, false>(p, h, qrow, 0, o);
         }
         if (!ok) fail();
     } else {
         // ------------------------------------------------------------ epilogue (one tile)
-        // Per item: once the softmax has handed over the last P with 1/l and
-        // the last P V product is done, read O from TMEM, hand it back (the
-        // next item's first P V may overwrite it), scale and write it.  The
-        // softmax hands an item over only after seeing P V of its block n - 2
-        // done (and this warpgroup saw the previous item's last one), so the
-        // awaited P V completion is never more than one phase away.
+        // Per item and tile: once the softmax has handed over the last P with
+        // 1/l and the last P V product is done, read O from TMEM, hand it back
+        // (the next item's first P V may overwrite it), scale and write it.
+        // The softmax hands an item over only after seeing P V of its block
+        // n - 2 done (and this warpgroup saw the previous item's last one), so
+        // the awaited P V completion is never more than one phase away.
         if constexpr (Cfg::kEpiWG) {
             const int quarter = warp & 3;
             const int r = quarter * 32 + lane;
-            const uint32_t o_addr =
-                tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + Cfg::kTmemO;
-            uint32_t cp = 0;                             // P V products so far
-            uint32_t items = 0;
+            const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+            uint32_t cp[kTiles], items[kTiles];          // P V products and items so far, per tile
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t) cp[t] = items[t] = 0;
             bool ok = true;
             for (int64_t k = 0; ok; ++k) {
                 const int64_t L = item_of(k, cta, G);
                 if (L >= p.items) break;
                 int h, pair;
                 item_coords(p, L, &h, &pair);
-                const int n = tile_blocks<kTiles>(p, pair, 0);
-                if (n == 0) continue;
-                cp += static_cast<uint32_t>(n);
-                bool got = mbar_wait_sleepy(dg::smem_u32(&o_full[items & 1u]), (items >> 1) & 1u, abort_flag,
-                                            p.timeout_ns);
-                got = got && mbar_wait_sleepy(dg::smem_u32(&pv_done[0]), (cp - 1u) & 1u, abort_flag,
-                                              p.timeout_ns);
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    const int n = tile_blocks<kTiles>(p, pair, t);
+                    if (!ok || n == 0) continue;
+                    cp[t] += static_cast<uint32_t>(n);
+                    const uint32_t par = items[t] & 1u;
+                    bool got = mbar_wait_sleepy(dg::smem_u32(&o_full[t * 2 + par]), (items[t] >> 1) & 1u,
+                                                abort_flag, p.timeout_ns);
+                    got = got && mbar_wait_sleepy(dg::smem_u32(&pv_done[t]), (cp[t] - 1u) & 1u, abort_flag,
+                                                  p.timeout_ns);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        continue;
+                    }
+                    dg::tc_fence_after();
+                    const float inv = sInv[(t * 2 + par) * kBQ + r];
+                    const uint32_t o_addr = lane_addr + static_cast<uint32_t>(t) * kTmemTile + Cfg::kTmemO;
+                    const int qrow = (pair * kTiles + t) * kBQ + r;
+                    ++items[t];
+                    // All of the row in registers, O handed back, then the stores
+                    // 32 columns at a time.
+                    uint32_t v[kD / 32][32];
+#pragma unroll
+                    for (int ch = 0; ch < kD / 32; ++ch)
+                        dg::tmem_ld_32x32b_x32(o_addr + static_cast<uint32_t>(ch * 32), v[ch]);
+#pragma unroll
+                    for (int ch = 0; ch < kD / 32; ++ch) dg::tmem_ld_wait(v[ch]);
+                    dg::tc_fence_before();
+                    dg::mbar_arrive(dg::smem_u32(&o_free[t]));
+#pragma unroll
+                    for (int ch = 0; ch < kD / 32; ++ch) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[ch][i] = __float_as_uint(__uint_as_float(v[ch][i]) * inv);
+                        store_o_span<32, true>(p, h, qrow, ch * 32, v[ch]);
+                    }
                 }
-                dg::tc_fence_after();
-                const float inv = sInv[(items & 1u) * kBQ + r];
-                uint32_t v[kD / 32][32];
-#pragma unroll
-                for (int ch = 0; ch < kD / 32; ++ch)
-                    dg::tmem_ld_32x32b_x32(o_addr + static_cast<uint32_t>(ch * 32), v[ch]);
-#pragma unroll
-                for (int ch = 0; ch < kD / 32; ++ch) dg::tmem_ld_wait(v[ch]);
-                dg::tc_fence_before();
-                dg::mbar_arrive(dg::smem_u32(o_free));
-                ++items;
-                uint32_t o[kD];
-#pragma unroll
-                for (int ch = 0; ch < kD / 32; ++ch)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[ch * 32 + i] = __float_as_uint(__uint_as_float(v[ch][i]) * inv);
-                store_o_row<kD, true>(p, h, pair * kBQ + r, o);
             }
             if (!ok) fail();
         }
@@ -992,6 +1007,7 @@ gemm_status_t attention_fwd(const void* Q, const void* K, const void* V, void* O
     p.ntiles = static_cast<int32_t>((seq + kBQ - 1) / kBQ);
     p.npairs = (p.ntiles + tiles_per_cta - 1) / tiles_per_cta;
     p.heads = static_cast<int32_t>(BH);
+    p.d = static_cast<int32_t>(d);
     p.items = int64_t(p.npairs) * BH;
     p.c = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
     p.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
