@@ -107,6 +107,25 @@ def test_lengths(seq, causal, d):
                           f"d {d} seq {seq} causal {causal} head {h}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_several_items_per_cta_with_ragged_tiles(d, causal):
+    """More work items than SMs, so CTAs walk several items whose last query
+    tile is ragged (seq 1100 = 8 tiles + 76 rows) and, for d = 64, whose
+    second tile of the last pair lies beyond the sequence; every head against
+    the oracle on a row sample that covers both edges."""
+    BH, seq = 40, 1100
+    Q, K, V = workloads.custom_qkv(BH, seq, d, "bf16" if causal else "f16", seed=77 + d + causal)
+    items = BH * ((seq + 127) // 128 + (1 if d == 64 else 0)) // (2 if d == 64 else 1)
+    assert items > torch.cuda.get_device_properties(0).multi_processor_count
+    got = run(Q, K, V, causal)
+    assert np.all(np.isfinite(got))
+    rows = np.unique(np.concatenate([np.arange(0, 4), np.arange(1020, seq), np.arange(5, 1020, 97)]))
+    for h in range(0, BH, 3):
+        assert_attn_close(got[h][rows], Q, K, V, causal, h, rows, torch.float32,
+                          f"d {d} causal {causal} head {h}")
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("layout", ["heads", "interleaved", "padded"])
 @pytest.mark.parametrize("d", [64, 128])
