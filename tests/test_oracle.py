@@ -97,7 +97,7 @@ def test_offsets_select_rows_and_ks(golden):
 
 
 def test_load_tiles_program00(golden):
-    """Section 4.4: program (0, 0), round 1 loads A[0:2, 0:2] and B[0:2, 0:2]."""
+    """Section 4.4: program (0, 0), in its first K step, loads A[0:2, 0:2] and B[0:2, 0:2]."""
     g4 = golden("matmul_4x4.txt")
     gl = golden("load_program00.txt")
     A = np.array(g4["A"]).reshape(-1)
