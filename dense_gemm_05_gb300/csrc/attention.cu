@@ -881,7 +881,9 @@ gemm_status_t check(const void* Q, const void* K, const void* V, const void* O, 
         reinterpret_cast<uintptr_t>(O) % static_cast<uintptr_t>(osz) != 0u)
         return GEMM_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return GEMM_ERR_UNSUPPORTED;
-    if (ld % 8 != 0 || hs % 8 != 0 || BH > 65535 || seq > INT32_MAX ||
+    // seq <= 2^31 - 256 keeps every row and key index the kernel forms (the
+    // first row of the block after the last, a key block's end) inside int32.
+    if (ld % 8 != 0 || hs % 8 != 0 || BH > 65535 || seq > int64_t(INT32_MAX) - 255 ||
         ld > (int64_t(1) << 36) || hs > (int64_t(1) << 36) || ldo > (int64_t(1) << 36) ||
         hso > (int64_t(1) << 36))
         return GEMM_ERR_UNSUPPORTED;

@@ -29,7 +29,7 @@
  * kernel leaves that boundary handling out).
  *
  * Limits: d == 64 or 128; ld and head_stride multiples of 8 elements and Q, K, V
- * 16-byte aligned (tensor-memory-access boxes); BH <= 65535; seq < 2^31.
+ * 16-byte aligned (tensor-memory-access boxes); BH <= 65535; seq <= 2^31 - 256.
  *
  * Ownership: the caller owns all buffers and the stream; nothing is allocated
  * and nothing synchronises (unless GEMM_DEBUG_SYNC=1: then the call waits and
@@ -39,7 +39,7 @@
  * Errors: GEMM_ERR_INVALID_ARG for null pointers (when BH*seq > 0), negative
  * sizes, ld < d, ldo < d, misaligned pointers, or O overlapping Q, K or V;
  * GEMM_ERR_UNSUPPORTED for d other than 64 or 128, strides that are not multiples of 8,
- * BH > 65535, an unknown dtype/out_type, or a device that is not sm_103;
+ * BH > 65535, seq > 2^31 - 256, an unknown dtype/out_type, or a device that is not sm_103;
  * GEMM_ERR_CUDA when the launch fails.  BH == 0 or seq == 0 is a no-op.
  */
 #ifndef DENSE_GEMM_05_GB300_ATTENTION_H

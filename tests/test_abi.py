@@ -124,3 +124,10 @@ def test_attention_argument_checks_need_no_gpu():
     assert cfg["grid_x"] == 4 and cfg["grid_y"] == 3 and cfg["block_q"] == 128 and cfg["causal"] == 1
     cfg = g.attention_fwd_query(a, b, c, o, 3, 1000, 128, 128, 128000, 128, 128000, 0, BF16, F32)
     assert cfg["grid_x"] == 8 and cfg["head_dim"] == 128
+    # The longest sequence whose row and key indices stay inside int32 (one
+    # head, rows 8 elements apart, the four tensors far apart), and one longer.
+    longest = (1 << 31) - 256
+    far = [(1 << 44) * i for i in (1, 2, 3, 4)]
+    cfg = g.attention_fwd_query(*far, 1, longest, 64, 64, 0, 64, 0, 0, BF16, F32)
+    assert cfg["grid_x"] == (longest + 255) // 256
+    assert af(*far, 1, longest + 1, 64, 64, 0, 64, 0, 0, BF16, F32, 0) == g.GEMM_ERR_UNSUPPORTED
