@@ -169,7 +169,8 @@ def test_repeatable_bits():
 def test_bits_do_not_depend_on_the_schedule(d, causal):
     """The launch is persistent (at most one CTA per SM, each walking several
     work items): a head computed alone and the same heads inside a 20-head
-    batch (several items per CTA, other CTAs and rounds) give identical bits."""
+    batch (several items per CTA, other CTAs and places in their sequences) give
+    identical bits."""
     BH, seq = 20, 4096
     Q, K, V = workloads.custom_qkv(BH, seq, d, "bf16", seed=31 + d + causal)
     items = BH * (seq // 128 // (2 if d == 64 else 1))
